@@ -1,0 +1,639 @@
+"""Benchmark of the paged BF16 hot path on GB300.
+
+Default workload: one synthetic transformer block (d_model 4096, 6144
+tokens, fused QKV [12288 x 4096], out-proj [4096 x 4096], FFN 4096 -> 16384
+-> 4096 tanh-GELU) whose 402,653,184 bytes of BF16 weights sit in pinned
+host memory and stream as 16 MiB pages through an 80 MiB arena every step.
+A step is one block forward: paged QKV projection, partitioned attention,
+paged out-projection (+ residual), paged FFN (+ residual).
+
+Printed: one JSON line (rank 0).  value = algorithmic block TFLOP/s
+(3.092 TFLOP per block per GPU, summed over ranks); page ingest GB/s and
+the roofline of the dominant kernel (the page GEMM) are reported beside it.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl psi|reference]
+                    [--workload block|ffn|linear|attention|stack]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged BF16 block TFLOP/s and page-ingest GB/s at 1 GB300, % of roofline"
+MiB = 1 << 20
+L2_FLUSH_BYTES = 256 * MiB
+
+
+# ------------------------------------------------------------------ utils --
+def env_rank():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def source_digest(*names):
+    h = hashlib.sha256()
+    for n in names:
+        h.update(open(os.path.join(ROOT, "weight_streamed_bf16_gb300", "csrc", n), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profile_traffic(kernel_file: str, digest: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", kernel_file)
+    if not os.path.exists(p):
+        return None
+    vals = {}
+    for line in open(p):
+        if ":" in line:
+            k, v = line.split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("source_digest") != digest:
+        return None
+    try:
+        return float(vals["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) >= 9:
+                rows.append(f)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1])]
+        mx = [num(r[2]) for r in rows if num(r[2])]
+        pw = [num(r[3]) for r in rows if num(r[3])]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None,
+                "samples": len(rows), "reasons": reasons}
+
+
+def h2d_probe(torch, dev, nbytes=1 << 30, reps=3):
+    """Host-to-device bandwidth of one large pinned cudaMemcpyAsync (GB/s)."""
+    src = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    dst = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    s = torch.cuda.current_stream()
+    best = 0.0
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        dst.copy_(src, non_blocking=True)
+        e1.record(s)
+        e1.synchronize()
+        best = max(best, nbytes / (e0.elapsed_time(e1) * 1e-3) / 1e9)
+    del src, dst
+    return best
+
+
+# -------------------------------------------------------------- workloads --
+class Workload:
+    name = ""
+    flops = 0.0            # algorithmic FLOPs per step
+    weight_h2d = 0         # weight bytes streamed per step
+    timed_alone = False    # dominant kernel timed alone (burst peak) or in a long step
+
+    def step(self):
+        raise NotImplementedError
+
+    def launches(self) -> int:
+        raise NotImplementedError
+
+
+class BlockWorkload(Workload):
+    def __init__(self, torch, dev, blocks=1, arena_mib=80, resident=False):
+        import psi_synth
+        from weight_streamed_bf16_gb300.block import BlockRunner, BlockShape, BlockWeights
+        from weight_streamed_bf16_gb300.torch_io import Arena, pinned_like
+        cfg = psi_synth.BLOCK
+        self.torch = torch
+        self.shape = BlockShape(d=cfg.d, N=cfg.N, heads=cfg.heads, dh=cfg.dh,
+                                hidden=cfg.hidden, slice=cfg.slice, page_bytes=cfg.page_bytes)
+        self.blocks = []
+        for b in range(blocks):
+            w = psi_synth.block_weights(cfg, block=b, device=dev)  # drawn on the GPU
+            # projection weights are streamed straight from pinned copies; the
+            # FFN weights are packed into a pinned page image by BlockWeights
+            w = {k: (pinned_like(v.cpu()) if k in ("Wqkv", "Wo") else
+                     (v.cpu() if v.dim() == 2 else v)) for k, v in w.items()}
+            self.blocks.append(BlockWeights(w, self.shape, resident=resident, device=dev))
+            del w
+        slots = arena_mib * MiB // cfg.page_bytes
+        self.arena = Arena(cfg.page_bytes, slots, device=dev)
+        self.runner = BlockRunner(self.shape, self.arena, device=dev)
+        self.X = psi_synth.block_input(cfg, device=dev)
+        self.Y = torch.empty_like(self.X)
+        self.tmp = torch.empty_like(self.X)
+        self.flags = 1 if resident else 0
+        self.flops = float(cfg.flops) * blocks
+        self.linear_flops = float(cfg.linear_flops) * blocks
+        self.weight_h2d = 0 if resident else cfg.weight_bytes * blocks
+        self.name = (f"synthetic transformer block x{blocks}: d_model {cfg.d}, {cfg.N} tokens, "
+                     f"{cfg.heads} heads x {cfg.dh}, QKV {cfg.qkv_rows}x{cfg.d} + out "
+                     f"{cfg.d}x{cfg.d} + FFN {cfg.d}->{cfg.hidden}->{cfg.d} tanh-GELU, "
+                     f"{cfg.page_bytes // MiB} MiB pages, {arena_mib} MiB arena "
+                     f"({slots} slots), weights {'resident' if resident else 'streamed from pinned host'}")
+
+    @property
+    def stream(self):
+        return self.arena.compute
+
+    def step(self, X=None, Y=None):
+        X = self.X if X is None else X
+        Y = self.Y if Y is None else Y
+        if len(self.blocks) == 1:
+            self.runner.forward(X, self.blocks[0], Y, self.flags)
+        else:
+            self.runner.stack(X, self.blocks, Y, self.tmp, self.flags)
+
+    def io(self):
+        return self.X, self.Y
+
+
+class FfnWorkload(Workload):
+    def __init__(self, torch, dev):
+        import psi_synth
+        from weight_streamed_bf16_gb300.torch_io import Arena, FfnWeight, ffn_workspace
+        cfg = psi_synth.FFN
+        self.cfg = cfg
+        X, U, V, a, b = psi_synth.ffn_inputs(cfg)
+        self.w = FfnWeight(U, V, cfg.slice)
+        self.arena = Arena(cfg.page_bytes, cfg.slots, device=dev)
+        self.X, self.a, self.b = X.to(dev), a.to(dev), b.to(dev)
+        self.Y = torch.empty(cfg.N, cfg.r, dtype=torch.bfloat16, device=dev)
+        self.hid, self.acc = ffn_workspace(cfg.N, cfg.r, cfg.slice, dev)
+        self.flops = float(cfg.flops)
+        self.weight_h2d = (cfg.h // cfg.slice) * cfg.page_bytes
+        self.name = (f"paged FFN: X {cfg.N}x{cfg.d}, W1 {cfg.h}x{cfg.d}, W2 {cfg.d}x{cfg.h}, "
+                     f"{cfg.slice}-wide hidden slices, {cfg.slots}-slice arena, streamed")
+
+    @property
+    def stream(self):
+        return self.arena.compute
+
+    def step(self, X=None, Y=None):
+        from weight_streamed_bf16_gb300 import psi
+        X = self.X if X is None else X
+        Y = self.Y if Y is None else Y
+        psi.psi_ffn_paged(self.arena.handle, X.data_ptr(), self.cfg.N, self.w.desc(),
+                          self.a.data_ptr(), self.b.data_ptr(), self.hid.data_ptr(),
+                          self.acc.data_ptr(), None, Y.data_ptr(), 0)
+
+    def io(self):
+        return self.X, self.Y
+
+
+class LinearWorkload(Workload):
+    def __init__(self, torch, dev):
+        import psi_synth
+        from weight_streamed_bf16_gb300.torch_io import Arena, LinearWeight
+        cfg = psi_synth.LINEAR
+        self.cfg = cfg
+        X, W, b = psi_synth.linear_inputs(cfg)
+        self.w = LinearWeight(W, cfg.page_bytes, page_rows=cfg.page_rows)
+        self.arena = Arena(cfg.page_bytes, cfg.slots, device=dev)
+        self.X, self.b = X.to(dev), b.to(dev)
+        self.Y = torch.empty(cfg.N, cfg.M, dtype=torch.bfloat16, device=dev)
+        self.flops = float(cfg.flops)
+        self.weight_h2d = cfg.M * cfg.K * 2
+        self.name = (f"single paged linear: X {cfg.N}x{cfg.K}, W {cfg.M}x{cfg.K}, "
+                     f"{cfg.page_rows}-row pages, {cfg.slots}-page arena (latency-bound)")
+
+    @property
+    def stream(self):
+        return self.arena.compute
+
+    def step(self, X=None, Y=None):
+        from weight_streamed_bf16_gb300 import psi
+        X = self.X if X is None else X
+        Y = self.Y if Y is None else Y
+        psi.psi_linear_paged(self.arena.handle, X.data_ptr(), self.cfg.N, self.cfg.K,
+                             self.w.desc(), self.b.data_ptr(), None, Y.data_ptr(), self.cfg.M, 0)
+
+    def io(self):
+        return self.X, self.Y
+
+
+class AttentionWorkload(Workload):
+    timed_alone = True
+
+    def __init__(self, torch, dev):
+        import psi_synth
+        cfg = psi_synth.ATTN
+        self.cfg = cfg
+        self.torch = torch
+        self.Q, self.K, self.V = psi_synth.attn_inputs(cfg, device=dev)
+        self.O = torch.empty_like(self.Q)
+        self._stream = torch.cuda.current_stream(dev)
+        self.flops = float(cfg.flops)
+        self.weight_h2d = 0
+        self.name = (f"partitioned attention: Q,K,V {cfg.heads}x{cfg.N}x{cfg.dh}, scale "
+                     f"1/sqrt({cfg.dh}), 128-key tiles, FP32 online softmax")
+
+    @property
+    def stream(self):
+        return self._stream
+
+    def step(self, X=None, Y=None):
+        from weight_streamed_bf16_gb300 import psi
+        from weight_streamed_bf16_gb300.torch_io import heads_view
+        Q = self.Q if X is None else X
+        O = self.O if Y is None else Y
+        psi.psi_attn_partitioned(heads_view(Q), heads_view(self.K), heads_view(self.V),
+                                 heads_view(O), self.cfg.heads, self.cfg.N, self.cfg.N,
+                                 self.cfg.dh, self.cfg.scale, 128, self._stream.cuda_stream, 0)
+
+    def io(self):
+        return self.Q, self.O
+
+
+def make_workload(torch, dev, args):
+    if args.workload == "block":
+        return BlockWorkload(torch, dev, 1, args.arena_mib, args.resident)
+    if args.workload == "stack":
+        return BlockWorkload(torch, dev, args.blocks, args.arena_mib, args.resident)
+    if args.workload == "ffn":
+        return FfnWorkload(torch, dev)
+    if args.workload == "linear":
+        return LinearWorkload(torch, dev)
+    if args.workload == "attention":
+        return AttentionWorkload(torch, dev)
+    raise SystemExit(f"unknown workload {args.workload}")
+
+
+# ------------------------------------------------------------ CPU oracle --
+class OracleSample:
+    """The CPU oracle on a bounded sample of a workload.  Inputs are drawn
+    once (untimed); ``run(rows)`` times the oracle on `rows` token (query)
+    rows of every operator and returns (algorithmic FLOPs, seconds, text)."""
+
+    def __init__(self, workload: str):
+        import numpy as np
+        import torch
+
+        import psi_synth
+        from oracle import bf16
+
+        def f64(t):
+            return bf16.decode(t.contiguous().view(torch.int16).numpy().view(np.uint16))
+
+        self.workload = workload
+        self.np = np
+        if workload in ("block", "stack"):
+            cfg = psi_synth.BLOCK
+            w = psi_synth.block_weights(cfg, block=0)
+            self.cfg = cfg
+            self.w = {k: f64(v) for k, v in w.items()}
+            self.X = f64(psi_synth.normal_bf16((1024, cfg.d), 1.0, cfg.seed, 90001))
+            self.KV = f64(psi_synth.normal_bf16((2, cfg.N, cfg.dh), 1.0, cfg.seed, 90002))
+        elif workload == "ffn":
+            cfg = psi_synth.FFN
+            self.cfg = cfg
+            self.t = [f64(t) for t in psi_synth.ffn_inputs(cfg)]
+        elif workload == "linear":
+            cfg = psi_synth.LINEAR
+            self.cfg = cfg
+            self.t = [f64(t) for t in psi_synth.linear_inputs(cfg)]
+        else:
+            cfg = psi_synth.ATTN
+            self.cfg = cfg
+            self.t = [f64(t) for t in psi_synth.attn_inputs(cfg)]
+
+    def run(self, rows: int):
+        from oracle import ops
+        np, cfg = self.np, self.cfg
+        fl = 0.0
+        t0 = time.perf_counter()
+        if self.workload in ("block", "stack"):
+            w = self.w
+            rows = min(rows, self.X.shape[0])
+            X = self.X[:rows]
+            h = ops.linear(X, w["Wqkv"], w["bqkv"]).y
+            fl += 2.0 * rows * cfg.d * cfg.qkv_rows
+            att = np.empty((rows, cfg.heads * cfg.dh))
+            for hd in range(cfg.heads):
+                q = h[:, hd * cfg.dh:(hd + 1) * cfg.dh]
+                att[:, hd * cfg.dh:(hd + 1) * cfg.dh] = ops.attention(
+                    q, self.KV[0], self.KV[1], 1 / math.sqrt(cfg.dh)).y
+            fl += 4.0 * rows * cfg.N * cfg.dh * cfg.heads
+            x1 = ops.linear(att, w["Wo"], w["bo"], residual=X).y
+            fl += 2.0 * rows * cfg.d * cfg.d
+            ops.ffn(x1, w["W1"], w["W2"], w["a1"], w["b1"], residual=x1)
+            fl += 4.0 * rows * cfg.d * cfg.hidden
+            desc = (f"oracle on {rows} token rows of every block operator (QKV, attention of "
+                    f"all {cfg.heads} heads against {cfg.N} keys, out-proj, FFN), float64 numpy")
+        elif self.workload == "ffn":
+            X, U, V, a, b = self.t
+            rows = min(rows, X.shape[0])
+            ops.ffn(X[:rows], U, V, a, b)
+            fl = 4.0 * rows * cfg.d * cfg.h
+            desc = f"oracle FFN on {rows} of {cfg.N} token rows"
+        elif self.workload == "linear":
+            X, W, b = self.t
+            n = 0
+            while time.perf_counter() - t0 < 1.0:
+                ops.linear(X, W, b)
+                n += 1
+            fl = float(cfg.flops) * n
+            desc = f"oracle linear, whole configuration, {n} repetitions"
+        else:
+            Q, K, V = self.t
+            rows = min(rows, Q.shape[1])
+            for hd in range(cfg.heads):
+                ops.attention(Q[hd, :rows], K[hd], V[hd], cfg.scale)
+            fl = 4.0 * cfg.heads * rows * cfg.N * cfg.dh
+            desc = f"oracle attention on {rows} of {cfg.N} query rows of all {cfg.heads} heads"
+        return fl, time.perf_counter() - t0, desc
+
+
+def reference_arm(args):
+    """--impl reference: the oracle timed on the host cores (rank 0 only)."""
+    rank, world, _ = env_rank()
+    if rank != 0:
+        return 0
+    rows = {"block": 64, "stack": 64, "ffn": 64, "linear": 0, "attention": 16}[args.workload]
+    sample = OracleSample(args.workload)
+    for _ in range(args.warmup):
+        sample.run(max(1, rows // 8))
+    tot_fl, tot_s, desc = 0.0, 0.0, ""
+    for _ in range(args.steps):
+        fl, sec, desc = sample.run(rows)
+        tot_fl += fl
+        tot_s += sec
+    v = tot_fl / tot_s / 1e12
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": tot_s / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "sample": desc},
+        "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": os.cpu_count(),
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }))
+    return 0
+
+
+# ------------------------------------------------------------------- main --
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="psi", choices=["psi", "reference"])
+    ap.add_argument("--workload", default="block",
+                    choices=["block", "stack", "ffn", "linear", "attention"])
+    ap.add_argument("--blocks", type=int, default=48, help="stack depth (workload stack)")
+    ap.add_argument("--arena-mib", type=int, default=80)
+    ap.add_argument("--resident", action="store_true", help="weights resident (no streaming)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=512)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    if args.impl == "reference":
+        return reference_arm(args)
+
+    import torch
+    rank, world, local = env_rank()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    from weight_streamed_bf16_gb300 import build, psi
+    build.build()
+    psi.load()
+
+    peaks = load_peaks()
+    link_gbs = h2d_probe(torch, dev)
+    wl = make_workload(torch, dev, args)
+    stream = wl.stream
+    arena = getattr(wl, "arena", None)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            wl.step()
+    if arena is not None:
+        arena.sync()
+        psi.psi_arena_reset_stats(arena.handle)
+        psi.psi_arena_set_timing(arena.handle, True)
+    attn0 = getattr(getattr(wl, "runner", None), "attn_launches", 0)
+
+    # ------------------------------------------------ device-timed region --
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = str(local)
+    clocks = ClockSampler(gpu_id)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier()
+    clocks.start()
+    t_wall = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)             # write > L2 between steps (not timed)
+            ev[i][0].record(stream)
+            wl.step()
+            ev[i][1].record(stream)
+    barrier()
+    t_wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = sum(step_ms)
+    if arena is not None:
+        st = psi.psi_arena_stats(arena.handle)
+        psi.psi_arena_set_timing(arena.handle, False)
+        if st["pages_streamed"] or st["resident_pages"]:
+            pass
+    else:
+        st = None
+    gpu_launches = (st["kernels_launched"] if st else 0)
+    if hasattr(wl, "runner"):
+        gpu_launches += wl.runner.attn_launches - attn0
+    elif isinstance(wl, AttentionWorkload):
+        gpu_launches += args.steps
+    if dist is not None:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = wl.flops * world / (total_ms * 1e-3) / 1e12
+
+    # ------------------------------------------------------------ e2e ---
+    Xd, Yd = wl.io()
+    Xh = torch.empty(Xd.shape, dtype=Xd.dtype, pin_memory=True)
+    Xh.copy_(Xd)
+    Yh = torch.empty(Yd.shape, dtype=Yd.dtype, pin_memory=True)
+    Xe = torch.empty_like(Xd)
+    Ye = torch.empty_like(Yd)
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            Xe.copy_(Xh, non_blocking=True)
+            wl.step(Xe, Ye)
+            Yh.copy_(Ye, non_blocking=True)
+    barrier()
+    ee = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            ee[i][0].record(stream)
+            Xe.copy_(Xh, non_blocking=True)
+            wl.step(Xe, Ye)
+            Yh.copy_(Ye, non_blocking=True)
+            ee[i][1].record(stream)
+    barrier()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in ee)
+    if dist is not None:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = wl.flops * world / (e2e_ms * 1e-3) / 1e12
+    in_bytes = Xh.numel() * Xh.element_size()
+    out_bytes = Yh.numel() * Yh.element_size()
+
+    # ------------------------------------------------ roofline (page GEMM) --
+    digest = source_digest("page_gemm.cu", "ptx.cuh")
+    roof = None
+    peak_t = peaks["bf16_tflops"] if wl.timed_alone else peaks["bf16_tflops_sustained"]
+    if st and st["timed_gemms"]:
+        avg_ms = st["gemm_ms"] / st["timed_gemms"]
+        fl_launch = st["gemm_flops"] / st["timed_gemms"]
+        ach = fl_launch / (avg_ms * 1e-3) / 1e12
+        roof = {"kernel": "page_gemm (tcgen05, all epilogues)", "bound": "tensor",
+                "achieved": ach, "peak": peak_t, "unit": "TFLOP/s", "frac": ach / peak_t,
+                "peak_kind": ("burst" if wl.timed_alone else "sustained") + f" bf16, of {peaks['source']}",
+                "launches": st["timed_gemms"], "avg_launch_ms": avg_ms,
+                "flops_per_launch": fl_launch,
+                "traffic": profile_traffic("page_gemm_block_traffic.txt", digest)}
+    elif isinstance(wl, AttentionWorkload):
+        ach = wl.flops / (ms_per_step * 1e-3) / 1e12
+        roof = {"kernel": "attn_partitioned (tcgen05)", "bound": "tensor", "achieved": ach,
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": ach / peaks["bf16_tflops"],
+                "peak_kind": f"burst bf16, of {peaks['source']}",
+                "traffic": profile_traffic("attention_traffic.txt",
+                                           source_digest("attention.cu", "ptx.cuh"))}
+
+    ingest = None
+    if st and st["timed_copies"]:
+        ce = st["copy_bytes"] / (st["copy_ms"] * 1e-3) / 1e9
+        eff = wl.weight_h2d / (ms_per_step * 1e-3) / 1e9
+        ingest = {"unit": "GB/s", "copy_engine_gbs": ce, "effective_gbs": eff,
+                  "link_probe_gbs": link_gbs, "copy_frac_of_link": ce / link_gbs,
+                  "weight_bytes_per_step": wl.weight_h2d,
+                  "pages_per_step": st["pages_streamed"] / args.steps}
+    step_bound_ms = max(wl.flops / (peaks["bf16_tflops_sustained"] * 1e12),
+                        wl.weight_h2d / (link_gbs * 1e9)) * 1e3
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        fl, sec, desc = OracleSample(args.workload).run(args.cpu_rows)
+        cpu = {"value": fl / sec / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
+               "kind": "oracle", "sample": desc, "seconds": sec}
+
+    if rank == 0:
+        out = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic (seeded, N(0,1/fan_in) weights)",
+            "config": {"workload": wl.name, "l2": "flushed between steps (256 MiB write)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "flops_per_step": wl.flops, "wall_s_timed": t_wall,
+                       "step_roofline_ms": step_bound_ms,
+                       "frac_of_step_roofline": step_bound_ms / ms_per_step},
+            "roofline": roof, "ingest": ingest, "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step":
+                    in_bytes + wl.weight_h2d, "d2h_bytes_per_step": out_bytes,
+                    "ms_per_step": e2e_ms / args.steps},
+            "gpu_launches": gpu_launches, "clocks": clk,
+            "peaks": peaks,
+        }
+        print(json.dumps(out))
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

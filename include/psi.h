@@ -1,0 +1,246 @@
+/*
+ * psi.h -- C ABI of the paged BF16 operator library (libpsi).
+ *
+ * Precision-Preserving Subtensor Inference (PSI, arXiv 2611.08023):
+ *  - section II-A: a fixed device arena of reusable weight pages; every
+ *    library device buffer comes from caller memory (the library itself never
+ *    allocates device memory); each page has at most one unreleased slice
+ *    request; reuse follows the copy and consumer dependencies; operators
+ *    declare their BF16 write boundaries.
+ *  - section II-D: page lifecycle free -> filling (H2D copy) -> ready ->
+ *    consuming -> free, enforced by stream order and cross-stream events;
+ *    release records an event after all uses are enqueued and the next copy
+ *    into the page waits for it.
+ *  - section II-B Eq.(2): hidden-partitioned FFN, Eqs.(3)-(4): online-softmax
+ *    attention over disjoint key tiles.
+ *  - section III-A: bias added in FP32 before the only BF16 write; FP32
+ *    attention weights.
+ *
+ * Conventions (all entry points):
+ *  - BF16 tensors are row-major arrays of uint16 bit patterns; "dev" pointers
+ *    are device addresses, "host" pointers are pinned host addresses.
+ *  - Calls enqueue work on the given CUDA streams and return; results are
+ *    valid once the stream has finished.  Asynchronous failures (a CUDA error
+ *    or an error recorded by a kernel) are returned by psi_sync or
+ *    psi_stream_wait.
+ *  - The caller owns every buffer.  The library creates only CUDA events and
+ *    host-side tensor-map descriptors.
+ *  - Errors: a psi_status is returned; psi_last_error() gives a message for
+ *    the last failing call of the calling thread.  An argument error enqueues
+ *    nothing.
+ *  - One arena is used by one host thread at a time.
+ */
+#ifndef PSI_H
+#define PSI_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PSI_OK = 0,
+  PSI_ERR_INVALID_ARG = 1,  /* null pointer, bad shape, stride or alignment */
+  PSI_ERR_CAPACITY = 2,     /* a page or workspace is too small for its tile */
+  PSI_ERR_PAGE_BUSY = 3,    /* a second request on an unreleased page */
+  PSI_ERR_CUDA = 4,         /* a CUDA runtime or driver call failed */
+  PSI_ERR_TIMEOUT = 5,      /* a host wait passed its deadline */
+  PSI_ERR_UNSUPPORTED = 6,  /* a shape or flag this build does not handle */
+  PSI_ERR_DEVICE = 7        /* a kernel recorded an error (bounded wait expired) */
+} psi_status;
+
+/* flags (bitwise or) */
+#define PSI_RESIDENT              0x1u /* weights read from dev_resident: no copies */
+#define PSI_SYNC_COPY             0x2u /* H2D page copies on the compute stream */
+#define PSI_BOUNDARY_PREGELU_BF16 0x4u /* FFN: extra BF16 write of the biased
+                                          pre-activation before GELU (section III-A,
+                                          "both native variants write the biased up
+                                          projection as BF16 before GELU") */
+
+typedef struct psi_arena psi_arena;
+
+/* A page handed out by psi_page_stream: slot index, request sequence number,
+ * device address of the slot and the bytes copied into it. */
+typedef struct {
+  int32_t slot;
+  uint64_t seq;
+  void* dev;
+  size_t bytes;
+} psi_page;
+
+/* Weight of a paged linear layer, W [rows x cols] BF16 row-major (rows =
+ * output features, cols = input features, the U layout of Eq.(2)).  Page p
+ * holds output rows [p*page_rows, min(rows, (p+1)*page_rows)), which are
+ * contiguous in W, so `host` is W itself.  `dev_resident` is a device copy of
+ * the same bytes, read instead of streaming when PSI_RESIDENT is given. */
+typedef struct {
+  const void* host;
+  const void* dev_resident;
+  int64_t rows;
+  int64_t cols;
+  int64_t page_rows;
+} psi_linear_weight;
+
+/* Weight of a paged FFN (Eq.(2)): U [h x d], V [r x h].  The hidden
+ * dimension is cut into slices J of `slice` channels; page J holds U_J
+ * ([slice x d], contiguous in U) followed by V_:,J ([r x slice], gathered).
+ * `host` is the packed image written by psi_ffn_pack (h/slice pages of
+ * psi_ffn_page_bytes each); `dev_resident` is a device copy of that image. */
+typedef struct {
+  const void* host;
+  const void* dev_resident;
+  int64_t d;
+  int64_t h;
+  int64_t r;
+  int64_t slice;
+} psi_ffn_weight;
+
+/* A BF16 tensor with a head dimension: element (head, token, c) is at
+ * ptr[head*ld_head + token*ld_token + c] (strides in elements, c contiguous). */
+typedef struct {
+  void* ptr;
+  int64_t ld_token;
+  int64_t ld_head;
+} psi_heads;
+
+typedef struct {
+  uint64_t pages_streamed;   /* H2D page requests */
+  uint64_t h2d_bytes;        /* bytes copied into pages */
+  uint64_t resident_pages;   /* pages read from dev_resident */
+  uint64_t kernels_launched; /* kernels this arena enqueued */
+  uint64_t timed_gemms;      /* page-GEMM launches bracketed by events */
+  double gemm_ms;            /* their summed device time */
+  double gemm_flops;         /* their summed algorithmic FLOPs (2*M*N*K) */
+  uint64_t timed_copies;     /* H2D copies bracketed by events */
+  double copy_ms;            /* their summed device time */
+  double copy_bytes;
+} psi_stats;
+
+/* ---------------------------------------------------------------- misc -- */
+const char* psi_version(void);
+const char* psi_status_string(psi_status s);
+/* Message of the last failing call on this thread ("" if none). */
+const char* psi_last_error(void);
+
+/* ------------------------------------------------------- page plans ----- */
+/* Output rows per page of a linear weight [rows x cols] for pages of
+ * page_bytes: the largest multiple of 256 (or, below 256 rows, of 16) whose
+ * rows fit, capped at `rows`.  PSI_ERR_CAPACITY if not even 16 rows fit
+ * (the "weight tile exceeds page" outcome of the capacity study, Table V).
+ * The plan depends on the page size only, never on the arena size. */
+psi_status psi_plan_linear(int64_t rows, int64_t cols, size_t page_bytes,
+                           int64_t* page_rows);
+
+/* Bytes of one FFN page: slice*d*2 + r*slice*2. */
+size_t psi_ffn_page_bytes(int64_t d, int64_t r, int64_t slice);
+
+/* Pack U [h x d] and V [r x h] (host BF16) into the page image `dst` (host,
+ * h/slice pages of psi_ffn_page_bytes).  h must be a multiple of slice.
+ * Runs on host threads; no CUDA call. */
+psi_status psi_ffn_pack(const void* U, const void* V, int64_t d, int64_t h,
+                        int64_t r, int64_t slice, void* dst);
+
+/* Workspace of psi_ffn_paged: hidden_bytes = 2*N*slice*2 (two BF16 hidden
+ * slices, so the next slice's up projection never overwrites the slice the
+ * down projection is reading), acc_bytes = N*r*4 (FP32 accumulator). */
+psi_status psi_ffn_workspace(int64_t N, int64_t r, int64_t slice,
+                             size_t* hidden_bytes, size_t* acc_bytes);
+
+/* ------------------------------------------------------------- arena ---- */
+/* Create an arena over caller device memory [dev_base, dev_base+dev_bytes):
+ * floor(dev_bytes / page_bytes) page slots (at least 1).  dev_base must be
+ * 1024-byte aligned and page_bytes a multiple of 1024.  compute_stream and
+ * copy_stream are cudaStream_t handles (they may be equal; NULL is the
+ * legacy default stream).  The arena owns only events. */
+psi_status psi_arena_create(void* dev_base, size_t dev_bytes, size_t page_bytes,
+                            void* compute_stream, void* copy_stream,
+                            psi_arena** out);
+/* Waits for the arena's streams, then frees its events. */
+psi_status psi_arena_destroy(psi_arena* arena);
+int32_t psi_arena_slots(const psi_arena* arena);
+
+/* Request the next slot of the ring and enqueue the H2D copy of
+ * host_src[0..bytes) into it.  The copy stream first waits for the slot's
+ * last release (its previous consumers); the compute stream then waits for
+ * the copy.  With PSI_SYNC_COPY the copy is enqueued on the compute stream
+ * instead.  PSI_ERR_PAGE_BUSY if that slot still has an unreleased request,
+ * PSI_ERR_CAPACITY if bytes > page_bytes. */
+psi_status psi_page_stream(psi_arena* arena, const void* host_src, size_t bytes,
+                           uint32_t flags, psi_page* out);
+/* End a request: records the slot's consumed event on the compute stream
+ * after every use enqueued so far.  PSI_ERR_INVALID_ARG for a stale page. */
+psi_status psi_page_release(psi_arena* arena, psi_page page);
+
+/* Poll the arena's streams until both are idle or timeout_ms passes
+ * (PSI_ERR_TIMEOUT; timeout_ms < 0 waits without limit), then report any
+ * asynchronous CUDA error or kernel-recorded error (PSI_ERR_DEVICE, which
+ * is cleared by the report). */
+psi_status psi_sync(psi_arena* arena, int64_t timeout_ms);
+/* The same for one stream, without an arena. */
+psi_status psi_stream_wait(void* stream, int64_t timeout_ms);
+
+psi_status psi_arena_stats(const psi_arena* arena, psi_stats* out);
+psi_status psi_arena_reset_stats(psi_arena* arena);
+/* enable != 0: bracket every page GEMM (compute stream) and every H2D copy
+ * (copy stream) with CUDA events; psi_arena_stats sums them (it waits for
+ * the events).  Off by default. */
+psi_status psi_arena_set_timing(psi_arena* arena, int32_t enable);
+/* Test hook: the next psi_page_stream call on this arena fails with
+ * PSI_ERR_CUDA before enqueuing anything (host-side fault injection). */
+psi_status psi_arena_fail_next_copy(psi_arena* arena);
+
+/* ---------------------------------------------------------- operators --- */
+/* Paged linear, section IV-B ("projection tiles ... output columns per
+ * group"): for each page p, Y[:, rows_p] = B(X W_p^T + b_p [+ R[:, rows_p]]),
+ * FP32 accumulation over all of K, bias (and residual) added in FP32 before
+ * the single BF16 write.
+ *   X    dev [N x K] BF16, row stride K; 16-byte aligned, K % 8 == 0
+ *   W    weight descriptor; W->cols == K
+ *   bias dev [W->rows] BF16 (required)
+ *   residual  dev [N x W->rows] BF16 with row stride ldy, or NULL
+ *   Y    dev [N x W->rows] BF16 with row stride ldy (ldy >= rows, ldy % 8 == 0)
+ * Weights stream through the arena page by page (or are read in place with
+ * PSI_RESIDENT); kernels run on the arena's compute stream.  The per-element
+ * arithmetic is the same in every mode, so resident and streamed results
+ * are bitwise equal. */
+psi_status psi_linear_paged(psi_arena* arena, const void* X, int64_t N, int64_t K,
+                            const psi_linear_weight* W, const void* bias,
+                            const void* residual, void* Y, int64_t ldy,
+                            uint32_t flags);
+
+/* Paged FFN, Eq.(2) with the reuse schedule of section III-B: for each
+ * hidden slice J = 0..S-1 in order, page J is streamed, then
+ *   H_J  = B(phi(X U_J^T + a_J))            (BF16 write; phi = tanh-GELU;
+ *                                            with PSI_BOUNDARY_PREGELU_BF16
+ *                                            the pre-activation is rounded too)
+ *   Acc  = Acc + H_J V_:,J^T                (FP32, J = 0 stores)
+ * and the last slice writes Y = B(Acc + H_S V_:,S^T + b [+ residual]).
+ *   X [N x d], residual and Y [N x r] (row stride r), a [h], b [r]: dev BF16
+ *   hidden_ws, acc_ws: dev workspace of psi_ffn_workspace sizes (16-byte
+ *   aligned); the full [N x h] hidden tensor is never formed. */
+psi_status psi_ffn_paged(psi_arena* arena, const void* X, int64_t N,
+                         const psi_ffn_weight* W, const void* a, const void* b,
+                         void* hidden_ws, void* acc_ws, const void* residual,
+                         void* Y, uint32_t flags);
+
+/* Partitioned attention, Eqs.(3)-(4): for every head and query row,
+ * s_j = scale * q.k_j in FP32; keys are visited in blocks of key_block and
+ * combined by the online-softmax update in FP32 (m, l, z); O = B(z / l).
+ * Unmasked, noncausal, no dropout; Nk >= 1.
+ *   Q [heads x Nq x dh], K, V [heads x Nk x dh], O [heads x Nq x dh]: dev
+ *   BF16 views (psi_heads strides, 16-byte aligned rows).  dh == 128.
+ *   key_block: 128 or 256.
+ * Enqueued on `stream` (cudaStream_t).  No arena: inputs are resident. */
+psi_status psi_attn_partitioned(const psi_heads* Q, const psi_heads* K,
+                                const psi_heads* V, const psi_heads* O,
+                                int32_t heads, int64_t Nq, int64_t Nk, int32_t dh,
+                                float scale, int32_t key_block, void* stream,
+                                uint32_t flags);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PSI_H */

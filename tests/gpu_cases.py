@@ -1,0 +1,101 @@
+"""Helpers for the GPU parity tests: run an operator through the C ABI and
+hand the same input bytes to the oracle."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from oracle import bf16, grade, ops
+from weight_streamed_bf16_gb300 import build, psi
+from weight_streamed_bf16_gb300.torch_io import (Arena, FfnWeight, LinearWeight,
+                                                 ffn_workspace, heads_view)
+
+_built = False
+
+
+def ensure_lib():
+    global _built
+    if not _built:
+        build.build()
+        psi.load()
+        _built = True
+
+
+def f64(t: torch.Tensor) -> np.ndarray:
+    """BF16 tensor -> float64 values through the oracle's own decoder."""
+    bits = t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    return bf16.decode(bits)
+
+
+def run_linear(X, W, b, page_rows, slots, flags=0, residual=None, arena=None, ldy=None):
+    """X, W, b: CPU bf16.  Returns the GPU output (CPU bf16 tensor)."""
+    N, K = X.shape
+    M = W.shape[0]
+    ldy = ldy or M
+    dev = torch.device("cuda")
+    Xd = X.to(dev)
+    bd = b.to(dev)
+    Y = torch.full((N, ldy), float("nan"), dtype=torch.bfloat16, device=dev)
+    Rd = None
+    if residual is not None:
+        Rd = torch.zeros((N, ldy), dtype=torch.bfloat16, device=dev)
+        Rd[:, :M] = residual.to(dev)
+    page_bytes = page_rows * K * 2
+    page_bytes = (page_bytes + 1023) // 1024 * 1024
+    own = arena is None
+    if own:
+        arena = Arena(page_bytes, slots)
+    w = LinearWeight(W, page_bytes, page_rows=page_rows, resident=bool(flags & psi.PSI_RESIDENT))
+    psi.psi_linear_paged(arena.handle, Xd.data_ptr(), N, K, w.desc(), bd.data_ptr(),
+                         Rd.data_ptr() if Rd is not None else None, Y.data_ptr(), ldy, flags)
+    arena.sync()
+    out = Y[:, :M].cpu()
+    if own:
+        arena.close()
+    return out
+
+
+def run_ffn(X, U, V, a, b, slice_, slots, flags=0, residual=None, return_hidden=False):
+    N, d = X.shape
+    r = V.shape[0]
+    dev = torch.device("cuda")
+    Xd, ad, bd = X.to(dev), a.to(dev), b.to(dev)
+    Rd = residual.to(dev) if residual is not None else None
+    Y = torch.full((N, r), float("nan"), dtype=torch.bfloat16, device=dev)
+    w = FfnWeight(U, V, slice_, resident=bool(flags & psi.PSI_RESIDENT))
+    arena = Arena((w.page_bytes + 1023) // 1024 * 1024, slots)
+    hid, acc = ffn_workspace(N, r, slice_)
+    psi.psi_ffn_paged(arena.handle, Xd.data_ptr(), N, w.desc(), ad.data_ptr(), bd.data_ptr(),
+                      hid.data_ptr(), acc.data_ptr(),
+                      Rd.data_ptr() if Rd is not None else None, Y.data_ptr(), flags)
+    arena.sync()
+    stats = arena.stats()
+    arena.close()
+    S = U.shape[0] // slice_
+    last = hid.view(2, N, slice_)[(S - 1) & 1].cpu()
+    if return_hidden:
+        return Y.cpu(), last, stats
+    return Y.cpu()
+
+
+def run_attention(Q, K, V, scale, key_block=128, O=None):
+    """Q [H x Nq x dh], K, V [H x Nk x dh] (device bf16 views); returns O."""
+    H, Nq, dh = Q.shape
+    Nk = K.shape[1]
+    if O is None:
+        O = torch.full((H, Nq, dh), float("nan"), dtype=torch.bfloat16, device=Q.device)
+    s = torch.cuda.current_stream()
+    psi.psi_attn_partitioned(heads_view(Q), heads_view(K), heads_view(V), heads_view(O), H, Nq,
+                             Nk, dh, scale, key_block, s.cuda_stream)
+    psi.psi_stream_wait(s.cuda_stream, 120000)
+    return O
+
+
+def check(y_gpu: torch.Tensor, res, tol=2.0, what=""):
+    rep = grade.report(f64(y_gpu), res, tol)
+    assert rep["pass"], f"{what}: {rep}"
+    return rep
+
+
+__all__ = ["ensure_lib", "f64", "run_linear", "run_ffn", "run_attention", "check", "ops",
+           "grade", "bf16"]

@@ -1,0 +1,111 @@
+"""The C-ABI library builds, loads and exports every declared entry point;
+host-only entry points (plans, packing, argument checks) work without a GPU.
+"""
+import ctypes as C
+import os
+import re
+
+import pytest
+import torch
+
+from weight_streamed_bf16_gb300 import build, psi
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return psi.load()
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "psi.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(psi_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert len(names) >= 20
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(names) == sorted(psi.EXPORTS)
+
+
+def test_version_and_status_strings(lib):
+    assert "sm_103a" in psi.psi_version()
+    assert psi.psi_status_string(psi.PSI_ERR_PAGE_BUSY) == "PSI_ERR_PAGE_BUSY"
+    assert psi.psi_status_string(99) == "PSI_ERR_UNKNOWN"
+
+
+def test_plan_linear(lib):
+    # 64-row pages of a [512 x 512] weight in 64 KiB pages
+    assert psi.psi_plan_linear(512, 512, 64 * 1024) == 64
+    # 16 MiB pages of [12288 x 4096]: 2048 rows (a multiple of 256)
+    assert psi.psi_plan_linear(12288, 4096, 16 << 20) == 2048
+    # a weight that fits one page is one page
+    assert psi.psi_plan_linear(100, 64, 1 << 20) == 100
+    # the plan depends on the page only
+    assert psi.psi_plan_linear(4096, 4096, 16 << 20) == 2048
+    with pytest.raises(psi.PsiError) as e:
+        psi.psi_plan_linear(4096, 4096, 8 * 4096 * 2)  # 8 rows < 16
+    assert e.value.status == psi.PSI_ERR_CAPACITY
+
+
+def test_ffn_page_bytes_and_workspace(lib):
+    assert psi.psi_ffn_page_bytes(2048, 2048, 1024) == 8 << 20
+    assert psi.psi_ffn_page_bytes(4096, 4096, 1024) == 16 << 20
+    hb, ab = psi.psi_ffn_workspace(1024, 2048, 1024)
+    assert hb == 2 * 1024 * 1024 * 2 and ab == 1024 * 2048 * 4
+
+
+def test_ffn_pack_layout(lib):
+    d, h, r, sl = 24, 64, 40, 16
+    U = torch.arange(h * d, dtype=torch.int32).to(torch.int16).view(h, d)
+    V = (torch.arange(r * h, dtype=torch.int32) * 7).to(torch.int16).view(r, h)
+    pb = psi.psi_ffn_page_bytes(d, r, sl)
+    dst = torch.zeros((h // sl) * pb // 2, dtype=torch.int16)
+    psi.psi_ffn_pack(U.data_ptr(), V.data_ptr(), d, h, r, sl, dst.data_ptr())
+    for J in range(h // sl):
+        page = dst[J * pb // 2:(J + 1) * pb // 2]
+        assert torch.equal(page[:sl * d].view(sl, d), U[J * sl:(J + 1) * sl])
+        assert torch.equal(page[sl * d:].view(r, sl), V[:, J * sl:(J + 1) * sl])
+
+
+def test_ffn_pack_rejects_ragged_hidden(lib):
+    with pytest.raises(psi.PsiError) as e:
+        psi.psi_ffn_pack(1, 1, 8, 100, 8, 64, 1)
+    assert e.value.status == psi.PSI_ERR_INVALID_ARG
+
+
+def test_arena_create_argument_checks(lib):
+    with pytest.raises(psi.PsiError) as e:
+        psi.psi_arena_create(0, 1 << 20, 1 << 16, 0, 0)
+    assert e.value.status == psi.PSI_ERR_INVALID_ARG
+    with pytest.raises(psi.PsiError) as e:
+        psi.psi_arena_create(1024, 1 << 20, 1000, 0, 0)  # page not a multiple of 1024
+    assert e.value.status == psi.PSI_ERR_INVALID_ARG
+    with pytest.raises(psi.PsiError) as e:
+        psi.psi_arena_create(1024, 1 << 10, 1 << 16, 0, 0)  # smaller than one page
+    assert e.value.status == psi.PSI_ERR_CAPACITY
+    assert "aligned" in psi.psi_last_error() or "page" in psi.psi_last_error()
+
+
+def test_operator_argument_checks_need_no_gpu(lib):
+    W = psi.psi_linear_weight(None, None, 64, 64, 64)
+    r = lib.psi_linear_paged(None, None, 1, 64, C.byref(W), None, None, None, 64, 0)
+    assert r == psi.PSI_ERR_INVALID_ARG
+    q = psi.psi_heads(None, 128, 0)
+    r = lib.psi_attn_partitioned(C.byref(q), C.byref(q), C.byref(q), C.byref(q), 1, 1, 0,
+                                 128, 0.1, 128, None, 0)
+    assert r == psi.PSI_ERR_INVALID_ARG
+
+
+def test_header_documents_no_device_allocation():
+    text = open(os.path.join(ROOT, "include", "psi.h")).read()
+    assert "never" in text and "allocat" in text
+    src = os.path.join(ROOT, "weight_streamed_bf16_gb300", "csrc")
+    for f in os.listdir(src):
+        body = open(os.path.join(src, f)).read()
+        assert "cudaMalloc" not in body, f

@@ -1,0 +1,93 @@
+"""Partitioned attention on the GPU against the oracle (PSI section II-B
+Eqs.(3)-(4), FP32 online accumulation of section III-A)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import psi_synth
+from weight_streamed_bf16_gb300 import psi
+
+from gpu_cases import check, ensure_lib, f64, ops, run_attention
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    ensure_lib()
+
+
+def _qkv(H, Nq, Nk, seed, dh=128):
+    g = torch.Generator().manual_seed(seed)
+    Q = torch.randn(H, Nq, dh, generator=g).to(torch.bfloat16)
+    K = torch.randn(H, Nk, dh, generator=g).to(torch.bfloat16)
+    V = torch.randn(H, Nk, dh, generator=g).to(torch.bfloat16)
+    return Q, K, V
+
+
+@pytest.mark.parametrize("H,Nq,Nk", [
+    (1, 128, 128),     # one tile each
+    (2, 200, 300),     # ragged queries and keys (last key tile 44 keys)
+    (3, 64, 1),        # a single key: O = B(v)
+    (1, 130, 129),     # one key past a tile boundary
+    (2, 256, 1024),    # several key tiles (online rescaling)
+])
+def test_attention_shapes(H, Nq, Nk):
+    Q, K, V = _qkv(H, Nq, Nk, H * 7 + Nq + Nk)
+    sc = 1 / math.sqrt(128)
+    O = run_attention(Q.cuda(), K.cuda(), V.cuda(), sc).cpu()
+    res = ops.attention_heads(f64(Q), f64(K), f64(V), sc)
+    rep = check(O, res, what=f"attn {H}x{Nq}x{Nk}")
+    assert rep["all_finite"]
+
+
+def test_attention_single_key_exact():
+    Q, K, V = _qkv(2, 100, 1, 3)
+    O = run_attention(Q.cuda(), K.cuda(), V.cuda(), 0.1).cpu()
+    assert torch.equal(O.view(torch.int16), V.expand(2, 100, 128).contiguous().view(torch.int16))
+
+
+def test_attention_config_sampled_rows():
+    """Q, K, V [32 x 4096 x 128], scale 1/sqrt(128): the GPU runs the full
+    configuration; the oracle checks every head on sampled query rows."""
+    cfg = psi_synth.ATTN
+    Q, K, V = psi_synth.attn_inputs(cfg)
+    O = run_attention(Q.cuda(), K.cuda(), V.cuda(), cfg.scale).cpu()
+    rows = np.array([0, 1, 127, 128, 2047, 2048, 4000, 4095])
+    Of = f64(O)
+    Qf, Kf, Vf = f64(Q), f64(K), f64(V)
+    worst = 0.0
+    for h in range(cfg.heads):
+        res = ops.attention(Qf[h], Kf[h], Vf[h], cfg.scale, rows=rows)
+        rep = check(O[h][rows], res, what=f"head {h}")
+        worst = max(worst, rep["max_rel_err"])
+    assert worst <= 1e-2
+    assert np.isfinite(Of).all()
+
+
+def test_attention_interleaved_layout():
+    """Heads interleaved within a token row (the fused QKV projection output):
+    Q, K, V read in place from [tokens x 3*H*dh], O written to [tokens x H*dh]."""
+    H, N, dh = 4, 300, 128
+    g = torch.Generator().manual_seed(21)
+    qkv = torch.randn(N, 3 * H * dh, generator=g).to(torch.bfloat16).cuda()
+    view = qkv.view(N, 3, H, dh)
+    Q = view[:, 0].permute(1, 0, 2)   # [H x N x dh], strides (dh, 3*H*dh, 1)
+    K = view[:, 1].permute(1, 0, 2)
+    V = view[:, 2].permute(1, 0, 2)
+    Obuf = torch.full((N, H * dh), float("nan"), dtype=torch.bfloat16, device="cuda")
+    O = Obuf.view(N, H, dh).permute(1, 0, 2)
+    run_attention(Q, K, V, 1 / math.sqrt(dh), O=O)
+    ref = run_attention(Q.contiguous(), K.contiguous(), V.contiguous(), 1 / math.sqrt(dh))
+    assert torch.equal(O.contiguous().view(torch.int16), ref.view(torch.int16))
+    res = ops.attention_heads(f64(Q), f64(K), f64(V), 1 / math.sqrt(dh))
+    check(O.contiguous().cpu(), res, what="interleaved")
+
+
+def test_attention_rejects_unsupported():
+    Q, K, V = _qkv(1, 8, 8, 1)
+    with pytest.raises(psi.PsiError) as e:
+        run_attention(Q.cuda(), K.cuda(), V.cuda(), 0.1, key_block=64)
+    assert e.value.status == psi.PSI_ERR_UNSUPPORTED

@@ -1,0 +1,83 @@
+"""Paged linear on the GPU against the oracle (PSI section IV-B projection
+pages; section III-A bias before the single BF16 write)."""
+import math
+
+import pytest
+import torch
+
+import psi_synth
+from weight_streamed_bf16_gb300 import psi
+
+from gpu_cases import check, ensure_lib, f64, ops, run_linear
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    ensure_lib()
+
+
+def test_linear_config_single_paged():
+    """X [64 x 512], W [512 x 512] in 64-row pages, 2-page arena, seed 0."""
+    cfg = psi_synth.LINEAR
+    X, W, b = psi_synth.linear_inputs(cfg)
+    y = run_linear(X, W, b, cfg.page_rows, cfg.slots)
+    res = ops.linear(f64(X), f64(W), f64(b))
+    rep = check(y, res, what="linear config")
+    assert rep["max_raw_ulps"] <= 2
+
+
+@pytest.mark.parametrize("N,K,M,page_rows,slots", [
+    (1, 64, 32, 16, 1),          # one token, one slot (copy waits for every consumer)
+    (77, 200, 130, 48, 2),       # ragged tokens, K tail (200 = 3*64 + 8), ragged last page
+    (300, 520, 272, 256, 3),     # multiple M tiles, N tile tail of a 256-row page
+    (129, 1024, 700, 352, 2),    # page rows not a multiple of the 256 tile
+])
+def test_linear_ragged_shapes(N, K, M, page_rows, slots):
+    g = torch.Generator().manual_seed(N * 1000 + K)
+    X = torch.randn(N, K, generator=g).to(torch.bfloat16)
+    W = (torch.randn(M, K, generator=g) / math.sqrt(K)).to(torch.bfloat16)
+    b = (torch.randn(M, generator=g) * 0.02).to(torch.bfloat16)
+    R = torch.randn(N, M, generator=g).to(torch.bfloat16)
+    y = run_linear(X, W, b, page_rows, slots, residual=R)
+    res = ops.linear(f64(X), f64(W), f64(b), residual=f64(R))
+    check(y, res, what=f"linear {N}x{K}x{M}")
+
+
+def test_linear_strided_output():
+    """Y written into a wider buffer (ldy > rows), as the fused QKV layout does."""
+    g = torch.Generator().manual_seed(5)
+    X = torch.randn(130, 256, generator=g).to(torch.bfloat16)
+    W = (torch.randn(96, 256, generator=g) / 16).to(torch.bfloat16)
+    b = (torch.randn(96, generator=g) * 0.02).to(torch.bfloat16)
+    y = run_linear(X, W, b, 32, 2, ldy=136)
+    check(y, ops.linear(f64(X), f64(W), f64(b)), what="strided")
+
+
+def test_linear_resident_streamed_sync_bitwise():
+    """Transport-only control: resident, streamed (async ring) and streamed on
+    the compute stream give the same bytes (byte-preserving transport)."""
+    g = torch.Generator().manual_seed(7)
+    X = torch.randn(256, 512, generator=g).to(torch.bfloat16)
+    W = (torch.randn(1024, 512, generator=g) / math.sqrt(512)).to(torch.bfloat16)
+    b = (torch.randn(1024, generator=g) * 0.02).to(torch.bfloat16)
+    a = run_linear(X, W, b, 128, 2)
+    r = run_linear(X, W, b, 128, 2, flags=psi.PSI_RESIDENT)
+    s = run_linear(X, W, b, 128, 2, flags=psi.PSI_SYNC_COPY)
+    one = run_linear(X, W, b, 128, 1)
+    many = run_linear(X, W, b, 128, 8)
+    for o in (r, s, one, many):
+        assert torch.equal(a.view(torch.int16), o.view(torch.int16))
+
+
+def test_linear_special_values():
+    """W = I gives B(x + b); an all-zero input gives B(b)."""
+    X = torch.randn(64, 128).to(torch.bfloat16)
+    W = torch.eye(128).to(torch.bfloat16)
+    b = (torch.randn(128) * 0.5).to(torch.bfloat16)
+    y = run_linear(X, W, b, 64, 2)
+    rep = check(y, ops.linear(f64(X), f64(W), f64(b)))
+    assert rep["max_raw_ulps"] <= 1
+    z = run_linear(torch.zeros(3, 128, dtype=torch.bfloat16), W, b, 64, 2)
+    assert torch.equal(z.view(torch.int16), b.expand(3, 128).contiguous().view(torch.int16))

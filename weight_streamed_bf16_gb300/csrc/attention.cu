@@ -1,0 +1,423 @@
+// attention.cu -- partitioned attention with FP32 online softmax on tcgen05.
+//
+// Paper: Precision-Preserving Subtensor Inference, section II-B Eqs.(3)-(4)
+// (online-softmax invariant over disjoint key tiles: m' = max(m, max s_j),
+// eta = e^{m-m'}, l' = eta*l + sum e^{s_j-m'}, z' = eta*z + sum e^{s_j-m'}
+// v_j, output z/l) and section III-A ("FP32 online accumulation" in place of
+// BF16 numerator exponential weights).
+//
+// One CTA per (head, 128-query tile).  Key tiles of 128:
+//   warp 0      TMA producer: Q once, then K_j and V_j into 2-stage rings
+//   warp 1      TMEM owner and MMA issuer:
+//                 S_j = Q K_j^T  (M=128, N=128 keys, K=128) into one of two
+//                                 TMEM S buffers, one tile ahead of softmax
+//                 O  += P_hi V_j + P_lo V_j  (V read MN-major)
+//   warps 2..5  softmax, one query row per thread: scores scaled to log2
+//               units in FP32, running max m and sum l in FP32, weights
+//               p = 2^(s - m) in FP32 split into p_hi = B(p) and p_lo =
+//               B(p - p_hi) (so the tensor-core operand carries ~16 bits of
+//               p, FP32 fidelity within 2^-17), O rescaled by eta in TMEM
+//               when the max moves, and the final O / l written as BF16.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace psi {
+namespace {
+
+constexpr int BQ = 128;
+constexpr int BKEY = 128;
+constexpr int DH = 128;
+constexpr int kThreads = 192;
+constexpr int TILE64 = 128 * 128;  // one [128 rows x 64 cols] BF16 swizzled block, bytes
+
+constexpr int OFF_Q = 0;
+constexpr int OFF_K = OFF_Q + 2 * TILE64;       // 2 stages x 2 column blocks
+constexpr int OFF_V = OFF_K + 2 * 2 * TILE64;
+constexpr int OFF_PHI = OFF_V + 2 * 2 * TILE64;
+constexpr int OFF_PLO = OFF_PHI + 2 * TILE64;
+constexpr int OFF_BAR = OFF_PLO + 2 * TILE64;   // 224 KiB
+constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
+
+constexpr uint32_t TM_S = 0;     // two S buffers: columns 0..127, 128..255
+constexpr uint32_t TM_O = 256;   // O accumulator: columns 256..383
+constexpr uint32_t TM_COLS = 512;
+
+struct __align__(8) ABars {
+  uint64_t q_full;
+  uint64_t k_full[2], k_empty[2];
+  uint64_t v_full[2], v_empty[2];
+  uint64_t s_full[2], s_empty[2];
+  uint64_t p_full;
+  uint64_t pv_done;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+// Coordinates of (head, token) in a 2-D tensor map: x = col + h*hx,
+// y = token + h*hy.
+struct View {
+  int32_t hx;
+  int32_t hy;
+};
+
+__device__ __forceinline__ void record_error(DevError* e, int code, int where, int i0, int i1) {
+  if (atomicCAS(&e->code, 0, code) == 0) {
+    e->where = where;
+    e->info0 = i0;
+    e->info1 = i1;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                const __grid_constant__ CUtensorMap tmV, const View vq, const View vk,
+                const View vv, const AttnArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  ABars* bars = reinterpret_cast<ABars*>(smem + OFF_BAR);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int q_tiles = (args.Nq + BQ - 1) / BQ;
+  const int head = blockIdx.x / q_tiles;
+  const int q0 = (blockIdx.x % q_tiles) * BQ;
+  const int nb = (args.Nk + BKEY - 1) / BKEY;
+  volatile int* abort_flag = &bars->abort_flag;
+  constexpr int kWhere = KID_ATTN * 16;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
+      mbar_init(&bars->s_full[s], 1);
+      mbar_init(&bars->s_empty[s], 128);
+    }
+    mbar_init(&bars->p_full, 128);
+    mbar_init(&bars->pv_done, 1);
+    mbar_init(&bars->drain, 1);
+    bars->abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, TM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer --
+    if (lane == 0) {
+      uint32_t k_armed = 0, v_armed = 0;  // per-stage parity of the last arming
+      int k_cnt[2] = {0, 0}, v_cnt[2] = {0, 0};
+      mbar_arrive_expect_tx(&bars->q_full, 2 * TILE64);
+      tma_load_2d(smem + OFF_Q, &tmQ, &bars->q_full, head * vq.hx, head * vq.hy + q0);
+      tma_load_2d(smem + OFF_Q + TILE64, &tmQ, &bars->q_full, head * vq.hx + 64,
+                  head * vq.hy + q0);
+      bool ok = true;
+      for (int j = 0; j < nb && ok; ++j) {
+        const int s = j & 1;
+        const uint32_t par = ((j >> 1) & 1) ^ 1;
+        const int key0 = j * BKEY;
+        if (!mbar_wait(&bars->k_empty[s], par, abort_flag, args.timeout_ns)) {
+          record_error(args.err, 1, kWhere + 0, j, 0);
+          bars->abort_flag = 1;
+          ok = false;
+          break;
+        }
+        uint8_t* kd = smem + OFF_K + s * 2 * TILE64;
+        mbar_arrive_expect_tx(&bars->k_full[s], 2 * TILE64);
+        tma_load_2d(kd, &tmK, &bars->k_full[s], head * vk.hx, head * vk.hy + key0);
+        tma_load_2d(kd + TILE64, &tmK, &bars->k_full[s], head * vk.hx + 64, head * vk.hy + key0);
+        k_armed = (k_armed & ~(1u << s)) | (static_cast<uint32_t>(k_cnt[s] & 1) << s);
+        ++k_cnt[s];
+        if (!mbar_wait(&bars->v_empty[s], par, abort_flag, args.timeout_ns)) {
+          record_error(args.err, 1, kWhere + 0, j, 1);
+          bars->abort_flag = 1;
+          ok = false;
+          break;
+        }
+        uint8_t* vd = smem + OFF_V + s * 2 * TILE64;
+        mbar_arrive_expect_tx(&bars->v_full[s], 2 * TILE64);
+        tma_load_2d(vd, &tmV, &bars->v_full[s], head * vv.hx, head * vv.hy + key0);
+        tma_load_2d(vd + TILE64, &tmV, &bars->v_full[s], head * vv.hx + 64, head * vv.hy + key0);
+        v_armed = (v_armed & ~(1u << s)) | (static_cast<uint32_t>(v_cnt[s] & 1) << s);
+        ++v_cnt[s];
+      }
+      // drain this thread's copies before the CTA exits
+      int dummy = 0;
+      if (!mbar_wait(&bars->q_full, 0, &dummy, args.timeout_ns))
+        record_error(args.err, 1, kWhere + 4, -1, 0);
+      for (int s = 0; s < 2; ++s) {
+        if (k_cnt[s] && !mbar_wait(&bars->k_full[s], (k_armed >> s) & 1, &dummy, args.timeout_ns))
+          record_error(args.err, 1, kWhere + 4, s, 1);
+        if (v_cnt[s] && !mbar_wait(&bars->v_full[s], (v_armed >> s) & 1, &dummy, args.timeout_ns))
+          record_error(args.err, 1, kWhere + 4, s, 2);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------- MMA issuer --
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(128, 128, 0, 1);  // V is MN-major
+      const uint32_t sQ = smem_u32(smem + OFF_Q);
+      bool ok = true, issued = false;
+      auto fail = [&](int j, int what) {
+        record_error(args.err, 1, kWhere + 1, j, what);
+        bars->abort_flag = 1;
+        ok = false;
+      };
+      auto issue_s = [&](int j) {
+        const int s = j & 1;
+        if (!mbar_wait(&bars->k_full[s], (j >> 1) & 1, abort_flag, args.timeout_ns)) {
+          fail(j, 0);
+          return;
+        }
+        if (!mbar_wait(&bars->s_empty[s], ((j >> 1) & 1) ^ 1, abort_flag, args.timeout_ns)) {
+          fail(j, 1);
+          return;
+        }
+        tc_fence_after();
+        const uint32_t sK = smem_u32(smem + OFF_K + s * 2 * TILE64);
+#pragma unroll
+        for (int kk = 0; kk < DH / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * TILE64 + (kk & 3) * 32;
+          mma_bf16_ss(tmem + TM_S + s * 128, sdesc_sw128(sQ + off, 16, 1024),
+                      sdesc_sw128(sK + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+        }
+        issued = true;
+        mma_commit(&bars->k_empty[s]);
+        mma_commit(&bars->s_full[s]);
+      };
+      if (!mbar_wait(&bars->q_full, 0, abort_flag, args.timeout_ns)) fail(-1, 2);
+      if (ok) issue_s(0);
+      for (int j = 0; j < nb && ok; ++j) {
+        if (j + 1 < nb) {
+          issue_s(j + 1);
+          if (!ok) break;
+        }
+        const int s = j & 1;
+        if (!mbar_wait(&bars->p_full, j & 1, abort_flag, args.timeout_ns)) {
+          fail(j, 3);
+          break;
+        }
+        if (!mbar_wait(&bars->v_full[s], (j >> 1) & 1, abort_flag, args.timeout_ns)) {
+          fail(j, 4);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sV = smem_u32(smem + OFF_V + s * 2 * TILE64);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const uint32_t sP = smem_u32(smem + (half ? OFF_PLO : OFF_PHI));
+#pragma unroll
+          for (int kk = 0; kk < BKEY / 16; ++kk) {
+            const uint32_t aoff = (kk >> 2) * TILE64 + (kk & 3) * 32;
+            // 16 keys = 16 rows of 128 B in each V column block; the two
+            // 64-wide dh blocks are TILE64 bytes apart (LBO)
+            mma_bf16_ss(tmem + TM_O, sdesc_sw128(sP + aoff, 16, 1024),
+                        sdesc_sw128(sV + kk * 2048, TILE64, 1024), idesc_o,
+                        (j | half | kk) != 0 ? 1u : 0u);
+          }
+        }
+        mma_commit(&bars->v_empty[s]);
+        mma_commit(&bars->pv_done);
+      }
+      if (issued) {
+        mma_commit(&bars->drain);
+        int dummy = 0;
+        if (!mbar_wait(&bars->drain, 0, &dummy, args.timeout_ns))
+          record_error(args.err, 1, kWhere + 5, 0, 0);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- softmax --
+    const int q = warp & 3;
+    const int row = q * 32 + lane;  // query row within the tile
+    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    float m2 = -INFINITY;  // running max, log2 units
+    float l = 0.f;         // running sum of weights
+    bool ok = true;
+    uint8_t* phi = smem + OFF_PHI;
+    uint8_t* plo = smem + OFF_PLO;
+    for (int j = 0; j < nb; ++j) {
+      const int b = j & 1;
+      if (!mbar_wait(&bars->s_full[b], (j >> 1) & 1, abort_flag, args.timeout_ns)) {
+        if (lane == 0) record_error(args.err, 1, kWhere + 2, j, q);
+        bars->abort_flag = 1;
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float s[BKEY];
+#pragma unroll
+      for (int c = 0; c < BKEY / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tmem + TM_S + b * 128 + c * 32 + lane_off, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[i]);
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->s_empty[b]);
+
+      const int kvalid = args.Nk - j * BKEY;  // keys of this tile that exist
+      float mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < BKEY; ++i) {
+        const float x = i < kvalid ? s[i] * args.scale_log2 : -INFINITY;
+        s[i] = x;
+        mx = fmaxf(mx, x);
+      }
+      const float m_new = fmaxf(m2, mx);
+      const float eta = exp2f(m2 - m_new);  // 0 on the first tile
+      float rs = 0.f;
+#pragma unroll
+      for (int i = 0; i < BKEY; ++i) {
+        const float p = exp2f(s[i] - m_new);
+        s[i] = p;
+        rs += p;
+      }
+      l = eta * l + rs;
+      m2 = m_new;
+
+      if (j > 0) {
+        // the previous PV has finished: P buffers are free and O is stable
+        if (!mbar_wait(&bars->pv_done, (j - 1) & 1, abort_flag, args.timeout_ns)) {
+          if (lane == 0) record_error(args.err, 1, kWhere + 3, j, q);
+          bars->abort_flag = 1;
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, eta != 1.0f)) {
+#pragma unroll 1
+          for (int c = 0; c < DH / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(tmem + TM_O + c * 32 + lane_off, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * eta);
+            tmem_st_32x32b_x32(tmem + TM_O + c * 32 + lane_off, r);
+          }
+          tmem_wait_st();
+        }
+      }
+      // P_hi / P_lo rows into the 128B-swizzled K-major operand layout
+#pragma unroll
+      for (int ch = 0; ch < BKEY / 8; ++ch) {
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const float p0 = s[ch * 8 + 2 * t];
+          const float p1 = s[ch * 8 + 2 * t + 1];
+          hi[t] = pack_bf16x2(p0, p1);
+          lo[t] = pack_bf16x2(p0 - bf16_lo(hi[t]), p1 - bf16_hi(hi[t]));
+        }
+        const int cb = ch >> 3;        // 64-key column block
+        const int c16 = ch & 7;        // 16-byte chunk within the 128-byte row
+        const uint32_t off = cb * TILE64 + row * 128 + ((c16 ^ (row & 7)) << 4);
+        *reinterpret_cast<uint4*>(phi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(plo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bars->p_full);
+    }
+    if (ok && nb > 0) {
+      if (!mbar_wait(&bars->pv_done, (nb - 1) & 1, abort_flag, args.timeout_ns)) {
+        if (lane == 0) record_error(args.err, 1, kWhere + 3, nb, q);
+        bars->abort_flag = 1;
+      } else {
+        tc_fence_after();
+        const int tok = q0 + row;
+        uint16_t* orow = args.O + head * args.o_ld_head + static_cast<int64_t>(tok) * args.o_ld_token;
+#pragma unroll 1
+        for (int c = 0; c < DH / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tmem + TM_O + c * 32 + lane_off, r);
+          tmem_wait_ld();
+          if (tok < args.Nq) {
+            uint4* o4 = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              float v[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) v[i] = __fdiv_rn(__uint_as_float(r[8 * t + i]), l);
+              o4[t] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                                 pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TM_COLS);
+  }
+}
+
+// Choose the 2-D tensor map of a psi_heads view: head-major rows (ld_head a
+// multiple of ld_token) or heads interleaved along the row.
+psi_status make_view(const psi_heads* h, int heads, int64_t tokens, CUtensorMap* m, View* v) {
+  if (!h || !h->ptr) return set_error(PSI_ERR_INVALID_ARG, "attention: null tensor");
+  if (h->ld_token < DH) return set_error(PSI_ERR_INVALID_ARG, "attention: ld_token < dh");
+  if (h->ld_head >= h->ld_token && h->ld_head % h->ld_token == 0) {
+    const int64_t hy = h->ld_head / h->ld_token;
+    if (hy < tokens && heads > 1)
+      return set_error(PSI_ERR_INVALID_ARG, "attention: heads overlap (ld_head too small)");
+    v->hx = 0;
+    v->hy = static_cast<int32_t>(hy);
+    return make_tmap_2d(m, h->ptr, (heads - 1) * hy + tokens, DH, h->ld_token, 128, 64);
+  }
+  if (h->ld_head >= DH && (heads - 1) * h->ld_head + DH <= h->ld_token && h->ld_head % 8 == 0) {
+    v->hx = static_cast<int32_t>(h->ld_head);
+    v->hy = 0;
+    return make_tmap_2d(m, h->ptr, tokens, (heads - 1) * h->ld_head + DH, h->ld_token, 128, 64);
+  }
+  return set_error(PSI_ERR_UNSUPPORTED, "attention: head layout is neither head-major nor "
+                                        "interleaved within a row");
+}
+
+}  // namespace
+
+psi_status launch_attention(const psi_heads* Q, const psi_heads* K, const psi_heads* V,
+                            const AttnArgs& a, cudaStream_t stream) {
+  CUtensorMap mq, mk, mv;
+  View vq, vk, vv;
+  psi_status st = make_view(Q, a.heads, a.Nq, &mq, &vq);
+  if (st != PSI_OK) return st;
+  if ((st = make_view(K, a.heads, a.Nk, &mk, &vk)) != PSI_OK) return st;
+  if ((st = make_view(V, a.heads, a.Nk, &mv, &vv)) != PSI_OK) return st;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e =
+        cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute(attn)");
+    attr_set = true;
+  }
+  const int q_tiles = (a.Nq + BQ - 1) / BQ;
+  const long long grid = static_cast<long long>(q_tiles) * a.heads;
+  if (grid <= 0) return PSI_OK;
+  if (grid > 0x7FFFFFFFLL) return set_error(PSI_ERR_UNSUPPORTED, "attention: grid too large");
+  attn_kernel<<<static_cast<unsigned>(grid), kThreads, SMEM_BYTES, stream>>>(mq, mk, mv, vq, vk,
+                                                                             vv, a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_error(e, "attention launch");
+  return PSI_OK;
+}
+
+}  // namespace psi

@@ -1,0 +1,112 @@
+// common.cu -- error reporting, the device error record, tensor-map
+// encoding and device queries shared by the kernels and the runtime.
+#include <cstdio>
+#include <mutex>
+#include <string>
+#include <cudaTypedefs.h>
+#include "internal.h"
+
+namespace psi {
+
+// Kernel-side error record (see DevError).  A module-scope device variable:
+// it is part of the library's loaded image, not a device allocation.
+__device__ DevError g_dev_error;
+
+namespace {
+thread_local std::string t_last_error;
+
+constexpr int kMaxDevices = 64;
+DevError* g_err_ptr[kMaxDevices] = {};
+std::mutex g_err_mu;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+cudaError_t g_encode_status = cudaSuccess;
+
+int g_sms[kMaxDevices] = {};
+}  // namespace
+
+psi_status set_error(psi_status s, const std::string& msg) {
+  t_last_error = msg;
+  return s;
+}
+
+psi_status cuda_error(cudaError_t e, const char* what) {
+  return set_error(PSI_ERR_CUDA, std::string(what) + ": " + cudaGetErrorName(e) + " (" +
+                                     cudaGetErrorString(e) + ")");
+}
+
+const char* last_error_cstr() { return t_last_error.c_str(); }
+
+DevError* dev_error_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_err_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_dev_error) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<DevError*>(p);
+  }
+  return g_err_ptr[dev];
+}
+
+cudaError_t dev_error_take(DevError* out) {
+  DevError zero = {0, 0, 0, 0};
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_dev_error, sizeof(DevError));
+  if (e != cudaSuccess) return e;
+  if (out->code != 0) e = cudaMemcpyToSymbol(g_dev_error, &zero, sizeof(DevError));
+  return e;
+}
+
+int num_sms() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= kMaxDevices) dev = 0;
+  if (g_sms[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    g_sms[dev] = n > 0 ? n : 1;
+  }
+  return g_sms[dev];
+}
+
+static psi_status get_encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    g_encode_status = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                       cudaEnableDefault, &q);
+    if (g_encode_status == cudaSuccess && q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode) {
+    return set_error(PSI_ERR_CUDA, "cuTensorMapEncodeTiled entry point not available");
+  }
+  return PSI_OK;
+}
+
+psi_status make_tmap_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                        uint64_t ld, uint32_t box_rows, uint32_t box_cols) {
+  psi_status st = get_encoder();
+  if (st != PSI_OK) return st;
+  if ((reinterpret_cast<uintptr_t>(base) & 15) || ((ld * 2) & 15))
+    return set_error(PSI_ERR_INVALID_ARG, "tensor map: base or row stride not 16-byte aligned");
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {ld * 2};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char buf[160];
+    snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled(2d) failed: %d (rows %llu cols %llu)",
+             static_cast<int>(r), static_cast<unsigned long long>(rows),
+             static_cast<unsigned long long>(cols));
+    return set_error(PSI_ERR_CUDA, buf);
+  }
+  return PSI_OK;
+}
+
+}  // namespace psi

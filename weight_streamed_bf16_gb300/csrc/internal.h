@@ -1,0 +1,90 @@
+// internal.h -- declarations shared by the translation units of libpsi.
+#pragma once
+#include <cstdint>
+#include <cstddef>
+#include <string>
+#include <cuda_runtime.h>
+#include <cuda.h>
+#include "../../include/psi.h"
+
+namespace psi {
+
+// Error record written by kernels (first error wins); lives in device
+// memory of the library module (a __device__ variable, not an allocation).
+struct DevError {
+  int code;   // 0 = none; 1 = bounded wait expired; 2 = bad range
+  int where;  // kernel id * 16 + role
+  int info0;
+  int info1;
+};
+
+enum KernelId : int { KID_GEMM = 1, KID_ATTN = 2 };
+
+// Returns the device address of the error record on the current device.
+DevError* dev_error_ptr();
+// Copies the record to the host and clears it (synchronous, current device).
+cudaError_t dev_error_take(DevError* out);
+
+// thread-local last-error message
+psi_status set_error(psi_status s, const std::string& msg);
+psi_status cuda_error(cudaError_t e, const char* what);
+
+// Tensor maps (driver entry point obtained through the runtime).
+// 2-D BF16 tensor [rows x cols] with row stride ld (elements), box
+// {box_cols, box_rows}, 128-byte swizzle.
+psi_status make_tmap_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                        uint64_t ld, uint32_t box_rows, uint32_t box_cols);
+int num_sms();
+
+// ------------------------------------------------------------ page GEMM --
+enum Epilogue : int {
+  EPI_LINEAR = 0,     // out = B(acc + bias [+ resid])
+  EPI_GELU = 1,       // out = B(phi(acc + bias)), optional pre-GELU rounding
+  EPI_ACC_STORE = 2,  // accf = acc
+  EPI_ACC_ADD = 3,    // accf += acc
+  EPI_ACC_FINAL = 4   // out = B(accf + acc + bias [+ resid])
+};
+
+struct GemmArgs {
+  int32_t M;  // output rows (tokens)
+  int32_t N;  // output columns (page rows)
+  int32_t K;
+  int32_t epi;
+  int32_t pregelu;
+  int32_t pad_;
+  const uint16_t* bias;   // [N]
+  const uint16_t* resid;  // [M x ldo] or null
+  uint16_t* out;          // [M x ldo]
+  float* accf;            // [M x ldacc]
+  int64_t ldo;
+  int64_t ldacc;
+  DevError* err;
+  uint64_t timeout_ns;
+};
+
+// D[M x N] = X[M x K] * P[N x K]^T with the chosen epilogue, on `stream`.
+// X and P are BF16 row-major with row strides ldx and ldp (elements).
+psi_status launch_page_gemm(const void* X, int64_t ldx, const void* P, int64_t ldp,
+                            const GemmArgs& args, cudaStream_t stream);
+
+// ------------------------------------------------------------ attention --
+struct AttnArgs {
+  int32_t heads;
+  int32_t Nq;
+  int32_t Nk;
+  int32_t key_block;
+  float scale_log2;  // scale * log2(e)
+  int32_t pad_;
+  uint16_t* O;
+  int64_t o_ld_token;
+  int64_t o_ld_head;
+  DevError* err;
+  uint64_t timeout_ns;
+};
+
+psi_status launch_attention(const psi_heads* Q, const psi_heads* K, const psi_heads* V,
+                            const AttnArgs& args, cudaStream_t stream);
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per in-kernel wait
+
+}  // namespace psi

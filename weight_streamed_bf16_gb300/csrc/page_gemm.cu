@@ -1,0 +1,405 @@
+// page_gemm.cu -- the page GEMM: D = X * P^T for one weight page, on the
+// 5th-generation tensor cores (tcgen05.mma kind::f16, BF16 in, FP32
+// accumulator in tensor memory), operands staged by TMA, with the bias /
+// GELU / FP32-accumulate / BF16-cast epilogues fused.
+//
+// Paper: Precision-Preserving Subtensor Inference, section II-B Eq.(2) (each
+// output entry receives its complete dot product; output bias added once),
+// section III-A (bias added in FP32 before the single BF16 write) and
+// section III-B (hidden slice computed once, written as BF16, reused by the
+// down projection; ordered down-projection accumulation).
+//
+// Structure (one CTA per SM, persistent over output tiles of 128 x BN):
+//   warp 0      TMA producer: X tile [128 x 64] and page tile [BN x 64] per
+//               stage into a STAGES-deep shared-memory ring (128B swizzle)
+//   warp 1      TMEM allocation and the MMA issuer: 4 MMAs of K = 16 per
+//               stage into one of two TMEM accumulators (2 x BN columns)
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator rows, fused
+//               epilogue, global stores; frees the accumulator so the next
+//               tile's MMAs overlap this tile's epilogue
+// Every wait is bounded; on expiry the kernel records an error, drains its
+// own copies and MMAs, frees TMEM and returns.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace psi {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;  // one 128-byte swizzle row of BF16
+constexpr int kThreads = 192;
+
+template <int BN>
+struct Cfg {
+  static constexpr int STAGES = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int BAR_OFFSET = STAGES * STAGE_BYTES;
+  static constexpr int SMEM_BYTES = BAR_OFFSET + 256 + 1024;  // + barriers + align slack
+};
+
+struct __align__(8) Bars {
+  uint64_t full[8];
+  uint64_t empty[8];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+__device__ __forceinline__ void record_error(DevError* e, int code, int where, int i0, int i1) {
+  if (atomicCAS(&e->code, 0, code) == 0) {
+    e->where = where;
+    e->info0 = i0;
+    e->info1 = i1;
+  }
+}
+
+__device__ __forceinline__ float gelu_tanh(float x) {
+  // tanh form of GELU: x/2 (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3)))
+  const float k0 = 0.7978845608028654f;
+  const float k1 = 0.044715f;
+  const float u = k0 * fmaf(k1 * x * x, x, x);
+  return 0.5f * x * (1.0f + tanhf(u));
+}
+
+__device__ __forceinline__ float round_bf16_f(float x) {
+  return bf16_lo(pack_bf16x2(x, 0.f));
+}
+
+// Epilogue of 32 consecutive columns of one row.  v[] are the FP32
+// accumulator values; col0 is the first column; ncol <= 32 valid columns.
+__device__ __forceinline__ void epilogue_row32(const GemmArgs& a, int row, int col0, int ncol,
+                                               float (&v)[32]) {
+  const bool full = (ncol == 32);
+  if (a.epi == EPI_ACC_STORE || a.epi == EPI_ACC_ADD) {
+    float* p = a.accf + static_cast<int64_t>(row) * a.ldacc + col0;
+    if (full) {
+      float4* p4 = reinterpret_cast<float4*>(p);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        float4 o = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        if (a.epi == EPI_ACC_ADD) {
+          const float4 q = p4[j];
+          o.x = q.x + o.x;
+          o.y = q.y + o.y;
+          o.z = q.z + o.z;
+          o.w = q.w + o.w;
+        }
+        p4[j] = o;
+      }
+    } else {
+      for (int j = 0; j < ncol; ++j) p[j] = (a.epi == EPI_ACC_ADD) ? p[j] + v[j] : v[j];
+    }
+    return;
+  }
+  // BF16 outputs: gather bias (and accumulator / residual) into v
+  float bia[32];
+  if (full) {
+    const uint4* b4 = reinterpret_cast<const uint4*>(a.bias + col0);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint4 q = __ldg(b4 + j);
+      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        bia[8 * j + 2 * t] = bf16_lo(w[t]);
+        bia[8 * j + 2 * t + 1] = bf16_hi(w[t]);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      bia[j] = j < ncol ? __uint_as_float(static_cast<uint32_t>(a.bias[col0 + j]) << 16) : 0.f;
+  }
+  if (a.epi == EPI_ACC_FINAL) {
+    const float* p = a.accf + static_cast<int64_t>(row) * a.ldacc + col0;
+    if (full) {
+      const float4* p4 = reinterpret_cast<const float4*>(p);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float4 q = p4[j];
+        v[4 * j] = q.x + v[4 * j];
+        v[4 * j + 1] = q.y + v[4 * j + 1];
+        v[4 * j + 2] = q.z + v[4 * j + 2];
+        v[4 * j + 3] = q.w + v[4 * j + 3];
+      }
+    } else {
+      for (int j = 0; j < ncol; ++j) v[j] = p[j] + v[j];
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = v[j] + bia[j];
+  if (a.epi == EPI_GELU) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      float t = v[j];
+      if (a.pregelu) t = round_bf16_f(t);
+      v[j] = gelu_tanh(t);
+    }
+  }
+  uint16_t* out = a.out + static_cast<int64_t>(row) * a.ldo + col0;
+  const uint16_t* res = a.resid ? a.resid + static_cast<int64_t>(row) * a.ldo + col0 : nullptr;
+  if (full) {
+    if (res) {
+      const uint4* r4 = reinterpret_cast<const uint4*>(res);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint4 q = r4[j];
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          v[8 * j + 2 * t] += bf16_lo(w[t]);
+          v[8 * j + 2 * t + 1] += bf16_hi(w[t]);
+        }
+      }
+    }
+    uint4* o4 = reinterpret_cast<uint4*>(out);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint4 q;
+      q.x = pack_bf16x2(v[8 * j + 0], v[8 * j + 1]);
+      q.y = pack_bf16x2(v[8 * j + 2], v[8 * j + 3]);
+      q.z = pack_bf16x2(v[8 * j + 4], v[8 * j + 5]);
+      q.w = pack_bf16x2(v[8 * j + 6], v[8 * j + 7]);
+      o4[j] = q;
+    }
+  } else {
+    for (int j = 0; j < ncol; ++j) {
+      float t = v[j];
+      if (res) t += __uint_as_float(static_cast<uint32_t>(res[j]) << 16);
+      out[j] = static_cast<uint16_t>(pack_bf16x2(t, 0.f) & 0xFFFFu);
+    }
+  }
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    page_gemm_kernel(const __grid_constant__ CUtensorMap tmX,
+                     const __grid_constant__ CUtensorMap tmP, const GemmArgs args) {
+  using C = Cfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;                              // STAGES x [128 x 64] bf16
+  uint8_t* sB = smem + C::STAGES * C::A_BYTES;     // STAGES x [BN x 64] bf16
+  Bars* bars = reinterpret_cast<Bars*>(smem + C::BAR_OFFSET);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int m_tiles = (args.M + BM - 1) / BM;
+  const int n_tiles = (args.N + BN - 1) / BN;
+  const int tiles = m_tiles * n_tiles;
+  const int kblocks = (args.K + BK - 1) / BK;
+  volatile int* abort_flag = &bars->abort_flag;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&bars->tfull[a], 1);
+      mbar_init(&bars->tempty[a], 4);
+    }
+    mbar_init(&bars->drain, 1);
+    bars->abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmX);
+    tma_prefetch_desc(&tmP);
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer --
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0;  // bit s: stage s has been armed at least once
+      uint32_t last_parity = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+        const int m0 = (t % m_tiles) * BM;
+        const int n0 = (t / m_tiles) * BN;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(&bars->empty[stage], phase ^ 1, abort_flag, args.timeout_ns)) {
+            record_error(args.err, 1, KID_GEMM * 16 + 0, t, kb);
+            bars->abort_flag = 1;
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bars->full[stage], C::STAGE_BYTES);
+          tma_load_2d(sA + stage * C::A_BYTES, &tmX, &bars->full[stage], kb * BK, m0);
+          tma_load_2d(sB + stage * C::B_BYTES, &tmP, &bars->full[stage], kb * BK, n0);
+          armed |= 1u << stage;
+          last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // drain: every armed stage's last load has landed before exit
+      for (int s = 0; s < C::STAGES; ++s) {
+        if (armed & (1u << s)) {
+          int dummy = 0;
+          if (!mbar_wait(&bars->full[s], (last_parity >> s) & 1, &dummy, args.timeout_ns))
+            record_error(args.err, 1, KID_GEMM * 16 + 4, s, 0);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------- MMA issuer --
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, 0, 0);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      bool issued = false;
+      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+        if (!mbar_wait(&bars->tempty[acc], acc_phase ^ 1, abort_flag, args.timeout_ns)) {
+          record_error(args.err, 1, KID_GEMM * 16 + 1, t, -1);
+          bars->abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + acc * BN;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(&bars->full[stage], phase, abort_flag, args.timeout_ns)) {
+            record_error(args.err, 1, KID_GEMM * 16 + 1, t, kb);
+            bars->abort_flag = 1;
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(sA + stage * C::A_BYTES);
+          const uint32_t b_base = smem_u32(sB + stage * C::B_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = sdesc_sw128(a_base + kk * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(b_base + kk * 32, 16, 1024);
+            mma_bf16_ss(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          issued = true;
+          mma_commit(&bars->empty[stage]);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&bars->tfull[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
+      }
+      if (issued) {  // all MMAs complete before TMEM is released
+        mma_commit(&bars->drain);
+        int dummy = 0;
+        if (!mbar_wait(&bars->drain, 0, &dummy, args.timeout_ns))
+          record_error(args.err, 1, KID_GEMM * 16 + 5, 0, 0);
+      }
+    }
+  } else {
+    // --------------------------------------------------------- epilogue --
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
+      const int m0 = (t % m_tiles) * BM;
+      const int n0 = (t / m_tiles) * BN;
+      if (!mbar_wait(&bars->tfull[acc], acc_phase, abort_flag, args.timeout_ns)) {
+        if (lane == 0) record_error(args.err, 1, KID_GEMM * 16 + 2, t, q);
+        bars->abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const int row = m0 + q * 32 + lane;
+      const uint32_t tbase = tmem + static_cast<uint32_t>(acc * BN) +
+                             (static_cast<uint32_t>(q * 32) << 16);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tbase + c * 32, r);
+        tmem_wait_ld();
+        const int col0 = n0 + c * 32;
+        if (col0 < args.N && row < args.M) {
+          float v[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+          const int ncol = min(32, args.N - col0);
+          epilogue_row32(args, row, col0, ncol, v);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->tempty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <int BN>
+psi_status launch_bn(const CUtensorMap& tx, const CUtensorMap& tp, const GemmArgs& a,
+                     cudaStream_t s) {
+  using C = Cfg<BN>;
+  static bool attr_set = false;  // per process; one device per process
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(page_gemm_kernel<BN>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_BYTES);
+    if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute(page_gemm)");
+    attr_set = true;
+  }
+  const int tiles = ((a.M + BM - 1) / BM) * ((a.N + BN - 1) / BN);
+  const int grid = tiles < num_sms() ? tiles : num_sms();
+  page_gemm_kernel<BN><<<grid, kThreads, C::SMEM_BYTES, s>>>(tx, tp, a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_error(e, "page_gemm launch");
+  return PSI_OK;
+}
+
+}  // namespace
+
+int gemm_bn_for(int64_t N) { return N > 128 ? 256 : (N > 64 ? 128 : 64); }
+
+psi_status launch_page_gemm(const void* X, int64_t ldx, const void* P, int64_t ldp,
+                            const GemmArgs& a, cudaStream_t stream) {
+  if (a.M <= 0 || a.N <= 0 || a.K <= 0) return PSI_OK;
+  const int bn = gemm_bn_for(a.N);
+  CUtensorMap tx, tp;
+  psi_status st = make_tmap_2d(&tx, X, a.M, a.K, ldx, BM, BK);
+  if (st != PSI_OK) return st;
+  st = make_tmap_2d(&tp, P, a.N, a.K, ldp, bn, BK);
+  if (st != PSI_OK) return st;
+  switch (bn) {
+    case 256: return launch_bn<256>(tx, tp, a, stream);
+    case 128: return launch_bn<128>(tx, tp, a, stream);
+    default: return launch_bn<64>(tx, tp, a, stream);
+  }
+}
+
+}  // namespace psi

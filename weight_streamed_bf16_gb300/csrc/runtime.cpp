@@ -1,0 +1,576 @@
+// runtime.cpp -- the fixed arena of weight pages, the page ring with its
+// copy/consumer events, and the paged operators (C ABI of include/psi.h).
+//
+// Paper: Precision-Preserving Subtensor Inference, section II-A (managed
+// working set M <= S_live + W + 2P + eps; the four arena rules), section
+// II-D (page lifecycle free -> filling -> ready -> consuming; release
+// records an event after all uses, the next copy waits on it), section III-B
+// (weight prefetch into alternating pages; FFN reuse schedule).
+#include <algorithm>
+#include <chrono>
+#include <cmath>
+#include <cstring>
+#include <string>
+#include <thread>
+#include <utility>
+#include <vector>
+#include "internal.h"
+
+namespace psi {
+const char* last_error_cstr();
+int gemm_bn_for(int64_t N);
+}  // namespace psi
+
+using namespace psi;
+
+namespace {
+
+enum SlotState : int { SLOT_FREE = 0, SLOT_REQUESTED = 1 };
+
+struct TimedLaunch {
+  cudaEvent_t start;
+  cudaEvent_t stop;
+  double work;  // FLOPs for a GEMM, bytes for a copy
+};
+
+}  // namespace
+
+struct psi_arena {
+  int device = 0;
+  char* base = nullptr;
+  size_t bytes = 0;
+  size_t page_bytes = 0;
+  int nslots = 0;
+  cudaStream_t compute = nullptr;
+  cudaStream_t copy = nullptr;
+  std::vector<cudaEvent_t> ready;      // copy into the slot complete
+  std::vector<cudaEvent_t> consumed;   // last consumer of the slot complete
+  std::vector<uint8_t> has_consumed;   // consumed[s] has been recorded
+  std::vector<int> state;              // host shadow of the request state
+  std::vector<uint64_t> slot_seq;      // sequence number of the open request
+  int next = 0;
+  uint64_t seq = 0;
+  psi_stats stats{};
+  bool timing = false;
+  bool fail_next_copy = false;
+  std::vector<TimedLaunch> gemm_t, copy_t;
+  std::vector<cudaEvent_t> pool;
+};
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+cudaEvent_t pool_get(psi_arena* a) {
+  if (!a->pool.empty()) {
+    cudaEvent_t e = a->pool.back();
+    a->pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+psi_status timed_begin(psi_arena* a, cudaStream_t s, TimedLaunch* t) {
+  t->start = pool_get(a);
+  t->stop = pool_get(a);
+  if (!t->start || !t->stop) return set_error(PSI_ERR_CUDA, "cudaEventCreate failed");
+  cudaError_t e = cudaEventRecord(t->start, s);
+  return e == cudaSuccess ? PSI_OK : cuda_error(e, "cudaEventRecord");
+}
+
+psi_status timed_end(psi_arena* a, cudaStream_t s, TimedLaunch t, std::vector<TimedLaunch>* v) {
+  cudaError_t e = cudaEventRecord(t.stop, s);
+  if (e != cudaSuccess) return cuda_error(e, "cudaEventRecord");
+  v->push_back(t);
+  (void)a;
+  return PSI_OK;
+}
+
+// Launch one page GEMM on the arena's compute stream (timed if enabled).
+psi_status arena_gemm(psi_arena* a, const void* X, int64_t ldx, const void* P, int64_t ldp,
+                      const GemmArgs& g) {
+  TimedLaunch t{};
+  psi_status st;
+  if (a->timing && (st = timed_begin(a, a->compute, &t)) != PSI_OK) return st;
+  st = launch_page_gemm(X, ldx, P, ldp, g, a->compute);
+  if (st != PSI_OK) return st;
+  a->stats.kernels_launched++;
+  if (a->timing) {
+    t.work = 2.0 * g.M * static_cast<double>(g.N) * g.K;
+    return timed_end(a, a->compute, t, &a->gemm_t);
+  }
+  return PSI_OK;
+}
+
+psi_status wait_stream(cudaStream_t s, std::chrono::steady_clock::time_point deadline,
+                       bool bounded) {
+  while (true) {
+    cudaError_t e = cudaStreamQuery(s);
+    if (e == cudaSuccess) return PSI_OK;
+    if (e != cudaErrorNotReady) return cuda_error(e, "stream");
+    if (bounded && std::chrono::steady_clock::now() > deadline)
+      return set_error(PSI_ERR_TIMEOUT, "stream did not finish before the deadline");
+    std::this_thread::sleep_for(std::chrono::microseconds(50));
+  }
+}
+
+psi_status report_device_errors() {
+  DevError d{};
+  cudaError_t e = dev_error_take(&d);
+  if (e != cudaSuccess) return cuda_error(e, "reading the kernel error record");
+  if (d.code != 0) {
+    char buf[200];
+    snprintf(buf, sizeof buf,
+             "kernel error %d (%s) in kernel %d role %d, info %d %d", d.code,
+             d.code == 1 ? "bounded wait expired" : "range", d.where / 16, d.where % 16, d.info0,
+             d.info1);
+    return set_error(PSI_ERR_DEVICE, buf);
+  }
+  return PSI_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* psi_version(void) { return "psi-gb300 0.1 (sm_103a, tcgen05)"; }
+
+const char* psi_status_string(psi_status s) {
+  switch (s) {
+    case PSI_OK: return "PSI_OK";
+    case PSI_ERR_INVALID_ARG: return "PSI_ERR_INVALID_ARG";
+    case PSI_ERR_CAPACITY: return "PSI_ERR_CAPACITY";
+    case PSI_ERR_PAGE_BUSY: return "PSI_ERR_PAGE_BUSY";
+    case PSI_ERR_CUDA: return "PSI_ERR_CUDA";
+    case PSI_ERR_TIMEOUT: return "PSI_ERR_TIMEOUT";
+    case PSI_ERR_UNSUPPORTED: return "PSI_ERR_UNSUPPORTED";
+    case PSI_ERR_DEVICE: return "PSI_ERR_DEVICE";
+  }
+  return "PSI_ERR_UNKNOWN";
+}
+
+const char* psi_last_error(void) { return last_error_cstr(); }
+
+psi_status psi_plan_linear(int64_t rows, int64_t cols, size_t page_bytes, int64_t* page_rows) {
+  if (!page_rows || rows <= 0 || cols <= 0)
+    return set_error(PSI_ERR_INVALID_ARG, "plan_linear: bad arguments");
+  const int64_t fit = static_cast<int64_t>(page_bytes / (static_cast<size_t>(cols) * 2));
+  if (fit >= rows) {
+    *page_rows = rows;
+    return PSI_OK;
+  }
+  int64_t pr = fit >= 256 ? (fit / 256) * 256 : (fit / 16) * 16;
+  if (pr < 16)
+    return set_error(PSI_ERR_CAPACITY, "plan_linear: weight tile exceeds page (16 rows do not fit)");
+  *page_rows = pr;
+  return PSI_OK;
+}
+
+size_t psi_ffn_page_bytes(int64_t d, int64_t r, int64_t slice) {
+  if (d <= 0 || r <= 0 || slice <= 0) return 0;
+  return static_cast<size_t>(slice) * static_cast<size_t>(d) * 2 +
+         static_cast<size_t>(r) * static_cast<size_t>(slice) * 2;
+}
+
+psi_status psi_ffn_pack(const void* U, const void* V, int64_t d, int64_t h, int64_t r,
+                        int64_t slice, void* dst) {
+  if (!U || !V || !dst || d <= 0 || h <= 0 || r <= 0 || slice <= 0 || h % slice)
+    return set_error(PSI_ERR_INVALID_ARG, "ffn_pack: bad arguments (h must be a multiple of slice)");
+  const int64_t S = h / slice;
+  const size_t pb = psi_ffn_page_bytes(d, r, slice);
+  const uint16_t* u = static_cast<const uint16_t*>(U);
+  const uint16_t* v = static_cast<const uint16_t*>(V);
+  char* out = static_cast<char*>(dst);
+  auto pack_one = [&](int64_t J) {
+    char* page = out + J * pb;
+    std::memcpy(page, u + J * slice * d, static_cast<size_t>(slice * d) * 2);
+    uint16_t* vj = reinterpret_cast<uint16_t*>(page + static_cast<size_t>(slice * d) * 2);
+    for (int64_t o = 0; o < r; ++o)
+      std::memcpy(vj + o * slice, v + o * h + J * slice, static_cast<size_t>(slice) * 2);
+  };
+  unsigned nt = std::max(1u, std::min<unsigned>(std::thread::hardware_concurrency(), 32u));
+  nt = static_cast<unsigned>(std::min<int64_t>(nt, S));
+  std::vector<std::thread> th;
+  for (unsigned t = 0; t < nt; ++t)
+    th.emplace_back([&, t] {
+      for (int64_t J = t; J < S; J += nt) pack_one(J);
+    });
+  for (auto& x : th) x.join();
+  return PSI_OK;
+}
+
+psi_status psi_ffn_workspace(int64_t N, int64_t r, int64_t slice, size_t* hidden_bytes,
+                             size_t* acc_bytes) {
+  if (N < 0 || r <= 0 || slice <= 0 || !hidden_bytes || !acc_bytes)
+    return set_error(PSI_ERR_INVALID_ARG, "ffn_workspace: bad arguments");
+  *hidden_bytes = 2 * static_cast<size_t>(N) * static_cast<size_t>(slice) * 2;
+  *acc_bytes = static_cast<size_t>(N) * static_cast<size_t>(r) * 4;
+  return PSI_OK;
+}
+
+psi_status psi_arena_create(void* dev_base, size_t dev_bytes, size_t page_bytes,
+                            void* compute_stream, void* copy_stream, psi_arena** out) {
+  if (!out) return set_error(PSI_ERR_INVALID_ARG, "arena_create: out is null");
+  *out = nullptr;
+  if (!dev_base || page_bytes == 0 || (page_bytes % 1024) ||
+      (reinterpret_cast<uintptr_t>(dev_base) % 1024))
+    return set_error(PSI_ERR_INVALID_ARG,
+                     "arena_create: base must be 1024-byte aligned, page_bytes a multiple of 1024");
+  if (dev_bytes < page_bytes)
+    return set_error(PSI_ERR_CAPACITY, "arena_create: arena smaller than one page");
+  psi_arena* a = new psi_arena();
+  cudaGetDevice(&a->device);
+  a->base = static_cast<char*>(dev_base);
+  a->bytes = dev_bytes;
+  a->page_bytes = page_bytes;
+  a->nslots = static_cast<int>(dev_bytes / page_bytes);
+  a->compute = static_cast<cudaStream_t>(compute_stream);
+  a->copy = static_cast<cudaStream_t>(copy_stream);
+  a->ready.resize(a->nslots);
+  a->consumed.resize(a->nslots);
+  a->has_consumed.assign(a->nslots, 0);
+  a->state.assign(a->nslots, SLOT_FREE);
+  a->slot_seq.assign(a->nslots, 0);
+  for (int s = 0; s < a->nslots; ++s) {
+    cudaError_t e1 = cudaEventCreateWithFlags(&a->ready[s], cudaEventDisableTiming);
+    cudaError_t e2 = cudaEventCreateWithFlags(&a->consumed[s], cudaEventDisableTiming);
+    if (e1 != cudaSuccess || e2 != cudaSuccess) {
+      psi_arena_destroy(a);
+      return cuda_error(e1 != cudaSuccess ? e1 : e2, "arena_create: cudaEventCreate");
+    }
+  }
+  if (!dev_error_ptr()) {
+    psi_arena_destroy(a);
+    return set_error(PSI_ERR_CUDA, "arena_create: kernel error record not reachable");
+  }
+  *out = a;
+  return PSI_OK;
+}
+
+psi_status psi_arena_destroy(psi_arena* a) {
+  if (!a) return PSI_OK;
+  cudaStreamSynchronize(a->compute);
+  if (a->copy != a->compute) cudaStreamSynchronize(a->copy);
+  for (auto e : a->ready)
+    if (e) cudaEventDestroy(e);
+  for (auto e : a->consumed)
+    if (e) cudaEventDestroy(e);
+  for (auto& t : a->gemm_t) {
+    cudaEventDestroy(t.start);
+    cudaEventDestroy(t.stop);
+  }
+  for (auto& t : a->copy_t) {
+    cudaEventDestroy(t.start);
+    cudaEventDestroy(t.stop);
+  }
+  for (auto e : a->pool) cudaEventDestroy(e);
+  delete a;
+  return PSI_OK;
+}
+
+int32_t psi_arena_slots(const psi_arena* a) { return a ? a->nslots : 0; }
+
+psi_status psi_page_stream(psi_arena* a, const void* host_src, size_t bytes, uint32_t flags,
+                           psi_page* out) {
+  if (!a || !host_src || !out) return set_error(PSI_ERR_INVALID_ARG, "page_stream: null argument");
+  if (bytes > a->page_bytes)
+    return set_error(PSI_ERR_CAPACITY, "page_stream: slice larger than the page");
+  const int s = a->next;
+  if (a->state[s] != SLOT_FREE)
+    return set_error(PSI_ERR_PAGE_BUSY, "page_stream: slot " + std::to_string(s) +
+                                            " still has an unreleased request");
+  if (a->fail_next_copy) {
+    a->fail_next_copy = false;
+    return set_error(PSI_ERR_CUDA, "page_stream: injected copy failure (test hook)");
+  }
+  void* dst = a->base + static_cast<size_t>(s) * a->page_bytes;
+  cudaError_t e;
+  const bool sync_copy = (flags & PSI_SYNC_COPY) || a->copy == a->compute;
+  TimedLaunch t{};
+  psi_status st;
+  if (sync_copy) {
+    // the copy follows every earlier consumer on the compute stream
+    if (a->timing && (st = timed_begin(a, a->compute, &t)) != PSI_OK) return st;
+    e = cudaMemcpyAsync(dst, host_src, bytes, cudaMemcpyHostToDevice, a->compute);
+    if (e != cudaSuccess) return cuda_error(e, "page_stream: cudaMemcpyAsync");
+  } else {
+    if (a->has_consumed[s]) {
+      e = cudaStreamWaitEvent(a->copy, a->consumed[s], 0);  // previous consumers done
+      if (e != cudaSuccess) return cuda_error(e, "page_stream: wait consumed");
+    }
+    if (a->timing && (st = timed_begin(a, a->copy, &t)) != PSI_OK) return st;
+    e = cudaMemcpyAsync(dst, host_src, bytes, cudaMemcpyHostToDevice, a->copy);
+    if (e != cudaSuccess) return cuda_error(e, "page_stream: cudaMemcpyAsync");
+    e = cudaEventRecord(a->ready[s], a->copy);
+    if (e != cudaSuccess) return cuda_error(e, "page_stream: record ready");
+    e = cudaStreamWaitEvent(a->compute, a->ready[s], 0);  // consumers wait for the copy
+    if (e != cudaSuccess) return cuda_error(e, "page_stream: wait ready");
+  }
+  if (a->timing) {
+    t.work = static_cast<double>(bytes);
+    if ((st = timed_end(a, sync_copy ? a->compute : a->copy, t, &a->copy_t)) != PSI_OK) return st;
+  }
+  a->state[s] = SLOT_REQUESTED;
+  a->slot_seq[s] = ++a->seq;
+  a->next = (s + 1) % a->nslots;
+  a->stats.pages_streamed++;
+  a->stats.h2d_bytes += bytes;
+  out->slot = s;
+  out->seq = a->slot_seq[s];
+  out->dev = dst;
+  out->bytes = bytes;
+  return PSI_OK;
+}
+
+psi_status psi_page_release(psi_arena* a, psi_page p) {
+  if (!a || p.slot < 0 || p.slot >= a->nslots)
+    return set_error(PSI_ERR_INVALID_ARG, "page_release: bad page");
+  if (a->state[p.slot] != SLOT_REQUESTED || a->slot_seq[p.slot] != p.seq)
+    return set_error(PSI_ERR_INVALID_ARG, "page_release: stale or already released page");
+  cudaError_t e = cudaEventRecord(a->consumed[p.slot], a->compute);
+  if (e != cudaSuccess) return cuda_error(e, "page_release: record consumed");
+  a->has_consumed[p.slot] = 1;
+  a->state[p.slot] = SLOT_FREE;
+  return PSI_OK;
+}
+
+psi_status psi_sync(psi_arena* a, int64_t timeout_ms) {
+  if (!a) return set_error(PSI_ERR_INVALID_ARG, "sync: null arena");
+  const bool bounded = timeout_ms >= 0;
+  const auto dl = std::chrono::steady_clock::now() + std::chrono::milliseconds(bounded ? timeout_ms : 0);
+  psi_status st = wait_stream(a->compute, dl, bounded);
+  if (st != PSI_OK) return st;
+  if (a->copy != a->compute && (st = wait_stream(a->copy, dl, bounded)) != PSI_OK) return st;
+  return report_device_errors();
+}
+
+psi_status psi_stream_wait(void* stream, int64_t timeout_ms) {
+  const bool bounded = timeout_ms >= 0;
+  const auto dl = std::chrono::steady_clock::now() + std::chrono::milliseconds(bounded ? timeout_ms : 0);
+  psi_status st = wait_stream(static_cast<cudaStream_t>(stream), dl, bounded);
+  if (st != PSI_OK) return st;
+  return report_device_errors();
+}
+
+psi_status psi_arena_stats(const psi_arena* ca, psi_stats* out) {
+  if (!ca || !out) return set_error(PSI_ERR_INVALID_ARG, "arena_stats: null argument");
+  psi_arena* a = const_cast<psi_arena*>(ca);
+  auto fold = [&](std::vector<TimedLaunch>& v, uint64_t* n, double* ms, double* work) -> psi_status {
+    for (auto& t : v) {
+      cudaError_t e = cudaEventSynchronize(t.stop);
+      if (e != cudaSuccess) return cuda_error(e, "arena_stats: event");
+      float f = 0.f;
+      e = cudaEventElapsedTime(&f, t.start, t.stop);
+      if (e != cudaSuccess) return cuda_error(e, "arena_stats: elapsed");
+      *n += 1;
+      *ms += f;
+      *work += t.work;
+      a->pool.push_back(t.start);
+      a->pool.push_back(t.stop);
+    }
+    v.clear();
+    return PSI_OK;
+  };
+  psi_status st = fold(a->gemm_t, &a->stats.timed_gemms, &a->stats.gemm_ms, &a->stats.gemm_flops);
+  if (st != PSI_OK) return st;
+  st = fold(a->copy_t, &a->stats.timed_copies, &a->stats.copy_ms, &a->stats.copy_bytes);
+  if (st != PSI_OK) return st;
+  *out = a->stats;
+  return PSI_OK;
+}
+
+psi_status psi_arena_reset_stats(psi_arena* a) {
+  if (!a) return set_error(PSI_ERR_INVALID_ARG, "arena_reset_stats: null arena");
+  psi_stats tmp;
+  psi_status st = psi_arena_stats(a, &tmp);  // folds and recycles pending events
+  a->stats = psi_stats{};
+  return st;
+}
+
+psi_status psi_arena_set_timing(psi_arena* a, int32_t enable) {
+  if (!a) return set_error(PSI_ERR_INVALID_ARG, "arena_set_timing: null arena");
+  a->timing = enable != 0;
+  return PSI_OK;
+}
+
+psi_status psi_arena_fail_next_copy(psi_arena* a) {
+  if (!a) return set_error(PSI_ERR_INVALID_ARG, "arena_fail_next_copy: null arena");
+  a->fail_next_copy = true;
+  return PSI_OK;
+}
+
+// --------------------------------------------------------------------------
+psi_status psi_linear_paged(psi_arena* a, const void* X, int64_t N, int64_t K,
+                            const psi_linear_weight* W, const void* bias, const void* residual,
+                            void* Y, int64_t ldy, uint32_t flags) {
+  if (!a || !X || !W || !bias || !Y)
+    return set_error(PSI_ERR_INVALID_ARG, "linear_paged: null argument");
+  if (N < 0 || K <= 0 || W->cols != K || W->rows <= 0 || W->page_rows <= 0)
+    return set_error(PSI_ERR_INVALID_ARG, "linear_paged: bad shape (W->cols must equal K)");
+  if (K % 8 || ldy < W->rows || ldy % 8)
+    return set_error(PSI_ERR_INVALID_ARG, "linear_paged: K and ldy must be multiples of 8, ldy >= rows");
+  if (W->page_rows < W->rows && W->page_rows % 16)
+    return set_error(PSI_ERR_INVALID_ARG, "linear_paged: page_rows must be a multiple of 16");
+  if (!aligned16(X) || !aligned16(Y) || !aligned16(bias) || (residual && !aligned16(residual)))
+    return set_error(PSI_ERR_INVALID_ARG, "linear_paged: pointers must be 16-byte aligned");
+  if (N > 0x7FFFFFFF || K > 0x7FFFFFFF || W->rows > 0x7FFFFFFF)
+    return set_error(PSI_ERR_UNSUPPORTED, "linear_paged: dimension above 2^31");
+  const bool resident = flags & PSI_RESIDENT;
+  const char* src = static_cast<const char*>(resident ? W->dev_resident : W->host);
+  if (!src)
+    return set_error(PSI_ERR_INVALID_ARG, resident ? "linear_paged: dev_resident is null"
+                                                   : "linear_paged: host is null");
+  const size_t max_page = static_cast<size_t>(std::min(W->page_rows, W->rows)) * K * 2;
+  if (!resident && max_page > a->page_bytes)
+    return set_error(PSI_ERR_CAPACITY, "linear_paged: weight tile exceeds page");
+  const int64_t npages = (W->rows + W->page_rows - 1) / W->page_rows;
+  DevError* err = dev_error_ptr();
+  for (int64_t p = 0; p < npages; ++p) {
+    const int64_t r0 = p * W->page_rows;
+    const int64_t rows_p = std::min(W->page_rows, W->rows - r0);
+    const size_t off = static_cast<size_t>(r0) * K * 2;
+    const size_t nbytes = static_cast<size_t>(rows_p) * K * 2;
+    psi_page pg{};
+    const void* dev;
+    if (resident) {
+      dev = src + off;
+      a->stats.resident_pages++;
+    } else {
+      psi_status st = psi_page_stream(a, src + off, nbytes, flags, &pg);
+      if (st != PSI_OK) return st;
+      dev = pg.dev;
+    }
+    GemmArgs g{};
+    g.M = static_cast<int32_t>(N);
+    g.N = static_cast<int32_t>(rows_p);
+    g.K = static_cast<int32_t>(K);
+    g.epi = EPI_LINEAR;
+    g.bias = static_cast<const uint16_t*>(bias) + r0;
+    g.resid = residual ? static_cast<const uint16_t*>(residual) + r0 : nullptr;
+    g.out = static_cast<uint16_t*>(Y) + r0;
+    g.ldo = ldy;
+    g.err = err;
+    g.timeout_ns = kWaitLimitNs;
+    psi_status st = arena_gemm(a, X, K, dev, K, g);
+    if (st != PSI_OK) return st;
+    if (!resident && (st = psi_page_release(a, pg)) != PSI_OK) return st;
+  }
+  return PSI_OK;
+}
+
+psi_status psi_ffn_paged(psi_arena* a, const void* X, int64_t N, const psi_ffn_weight* W,
+                         const void* av, const void* bv, void* hidden_ws, void* acc_ws,
+                         const void* residual, void* Y, uint32_t flags) {
+  if (!a || !X || !W || !av || !bv || !hidden_ws || !acc_ws || !Y)
+    return set_error(PSI_ERR_INVALID_ARG, "ffn_paged: null argument");
+  const int64_t d = W->d, h = W->h, r = W->r, sl = W->slice;
+  if (N < 0 || d <= 0 || h <= 0 || r <= 0 || sl <= 0 || h % sl)
+    return set_error(PSI_ERR_INVALID_ARG, "ffn_paged: bad shape (h must be a multiple of slice)");
+  if (d % 8 || r % 8 || sl % 16)
+    return set_error(PSI_ERR_INVALID_ARG, "ffn_paged: d, r must be multiples of 8, slice of 16");
+  if (!aligned16(X) || !aligned16(Y) || !aligned16(av) || !aligned16(bv) ||
+      !aligned16(hidden_ws) || !aligned16(acc_ws) || (residual && !aligned16(residual)))
+    return set_error(PSI_ERR_INVALID_ARG, "ffn_paged: pointers must be 16-byte aligned");
+  if (N > 0x7FFFFFFF || d > 0x7FFFFFFF || h > 0x7FFFFFFF || r > 0x7FFFFFFF)
+    return set_error(PSI_ERR_UNSUPPORTED, "ffn_paged: dimension above 2^31");
+  const bool resident = flags & PSI_RESIDENT;
+  const char* src = static_cast<const char*>(resident ? W->dev_resident : W->host);
+  if (!src)
+    return set_error(PSI_ERR_INVALID_ARG, resident ? "ffn_paged: dev_resident is null"
+                                                   : "ffn_paged: host is null");
+  const size_t pb = psi_ffn_page_bytes(d, r, sl);
+  if (!resident && pb > a->page_bytes)
+    return set_error(PSI_ERR_CAPACITY, "ffn_paged: FFN weight tile exceeds page");
+  const int64_t S = h / sl;
+  DevError* err = dev_error_ptr();
+  const uint16_t* a16 = static_cast<const uint16_t*>(av);
+  uint16_t* hid = static_cast<uint16_t*>(hidden_ws);
+  for (int64_t J = 0; J < S; ++J) {
+    psi_page pg{};
+    const char* dev;
+    if (resident) {
+      dev = src + static_cast<size_t>(J) * pb;
+      a->stats.resident_pages++;
+    } else {
+      psi_status st = psi_page_stream(a, src + static_cast<size_t>(J) * pb, pb, flags, &pg);
+      if (st != PSI_OK) return st;
+      dev = static_cast<const char*>(pg.dev);
+    }
+    const void* UJ = dev;
+    const void* VJ = dev + static_cast<size_t>(sl) * d * 2;
+    uint16_t* HJ = hid + static_cast<size_t>(J & 1) * N * sl;
+    // up projection slice: H_J = B(phi(X U_J^T + a_J))
+    GemmArgs up{};
+    up.M = static_cast<int32_t>(N);
+    up.N = static_cast<int32_t>(sl);
+    up.K = static_cast<int32_t>(d);
+    up.epi = EPI_GELU;
+    up.pregelu = (flags & PSI_BOUNDARY_PREGELU_BF16) ? 1 : 0;
+    up.bias = a16 + J * sl;
+    up.out = HJ;
+    up.ldo = sl;
+    up.err = err;
+    up.timeout_ns = kWaitLimitNs;
+    psi_status st = arena_gemm(a, X, d, UJ, d, up);
+    if (st != PSI_OK) return st;
+    // down projection slice, ordered FP32 accumulation; bias once at the end
+    GemmArgs dn{};
+    dn.M = static_cast<int32_t>(N);
+    dn.N = static_cast<int32_t>(r);
+    dn.K = static_cast<int32_t>(sl);
+    dn.accf = static_cast<float*>(acc_ws);
+    dn.ldacc = r;
+    dn.err = err;
+    dn.timeout_ns = kWaitLimitNs;
+    if (J == S - 1) {
+      dn.epi = S == 1 ? EPI_LINEAR : EPI_ACC_FINAL;
+      dn.bias = static_cast<const uint16_t*>(bv);
+      dn.resid = static_cast<const uint16_t*>(residual);
+      dn.out = static_cast<uint16_t*>(Y);
+      dn.ldo = r;
+    } else {
+      dn.epi = J == 0 ? EPI_ACC_STORE : EPI_ACC_ADD;
+    }
+    st = arena_gemm(a, HJ, sl, VJ, sl, dn);
+    if (st != PSI_OK) return st;
+    if (!resident && (st = psi_page_release(a, pg)) != PSI_OK) return st;
+  }
+  return PSI_OK;
+}
+
+psi_status psi_attn_partitioned(const psi_heads* Q, const psi_heads* K, const psi_heads* V,
+                                const psi_heads* O, int32_t heads, int64_t Nq, int64_t Nk,
+                                int32_t dh, float scale, int32_t key_block, void* stream,
+                                uint32_t flags) {
+  (void)flags;
+  if (!Q || !K || !V || !O || !O->ptr)
+    return set_error(PSI_ERR_INVALID_ARG, "attn: null argument");
+  if (heads <= 0 || Nq < 0 || Nk < 1)
+    return set_error(PSI_ERR_INVALID_ARG, "attn: need heads >= 1, Nq >= 0 and at least one key");
+  if (dh != 128) return set_error(PSI_ERR_UNSUPPORTED, "attn: this build handles dh = 128");
+  if (key_block != 128)
+    return set_error(PSI_ERR_UNSUPPORTED, "attn: key_block must be 128 in this build");
+  if (!std::isfinite(scale)) return set_error(PSI_ERR_INVALID_ARG, "attn: scale not finite");
+  if (!aligned16(O->ptr) || O->ld_token % 8 || O->ld_head % 8 || O->ld_token < dh)
+    return set_error(PSI_ERR_INVALID_ARG, "attn: O rows must be 16-byte aligned");
+  if (Nq > 0x7FFFFFFF || Nk > 0x7FFFFFFF)
+    return set_error(PSI_ERR_UNSUPPORTED, "attn: token count above 2^31");
+  if (Nq == 0) return PSI_OK;
+  AttnArgs g{};
+  g.heads = heads;
+  g.Nq = static_cast<int32_t>(Nq);
+  g.Nk = static_cast<int32_t>(Nk);
+  g.key_block = key_block;
+  g.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+  g.O = static_cast<uint16_t*>(O->ptr);
+  g.o_ld_token = O->ld_token;
+  g.o_ld_head = O->ld_head;
+  g.err = dev_error_ptr();
+  if (!g.err) return set_error(PSI_ERR_CUDA, "attn: kernel error record not reachable");
+  g.timeout_ns = kWaitLimitNs;
+  return launch_attention(Q, K, V, g, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

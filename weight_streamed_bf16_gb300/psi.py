@@ -1,0 +1,240 @@
+"""ctypes binding of libpsi (include/psi.h): the same entry points, argument
+marshalling only.  Every step of the operators runs in the library's CUDA
+kernels; there is no Python or CPU fallback.  Loading fails loudly when the
+library has not been built.
+
+Pointers are passed as Python ints (device or pinned-host addresses, e.g.
+``tensor.data_ptr()``); streams as ints (``torch.cuda.Stream.cuda_stream``).
+Each wrapper raises ``PsiError`` when the library returns a non-OK status.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libpsi.so")
+
+PSI_OK = 0
+PSI_ERR_INVALID_ARG = 1
+PSI_ERR_CAPACITY = 2
+PSI_ERR_PAGE_BUSY = 3
+PSI_ERR_CUDA = 4
+PSI_ERR_TIMEOUT = 5
+PSI_ERR_UNSUPPORTED = 6
+PSI_ERR_DEVICE = 7
+
+PSI_RESIDENT = 0x1
+PSI_SYNC_COPY = 0x2
+PSI_BOUNDARY_PREGELU_BF16 = 0x4
+
+# every entry point include/psi.h declares
+EXPORTS = [
+    "psi_version", "psi_status_string", "psi_last_error",
+    "psi_plan_linear", "psi_ffn_page_bytes", "psi_ffn_pack", "psi_ffn_workspace",
+    "psi_arena_create", "psi_arena_destroy", "psi_arena_slots",
+    "psi_page_stream", "psi_page_release", "psi_sync", "psi_stream_wait",
+    "psi_arena_stats", "psi_arena_reset_stats", "psi_arena_set_timing",
+    "psi_arena_fail_next_copy",
+    "psi_linear_paged", "psi_ffn_paged", "psi_attn_partitioned",
+]
+
+
+class PsiError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{_status_name(status)}: {msg}")
+        self.status = status
+
+
+class psi_page(C.Structure):
+    _fields_ = [("slot", C.c_int32), ("seq", C.c_uint64), ("dev", C.c_void_p),
+                ("bytes", C.c_size_t)]
+
+
+class psi_linear_weight(C.Structure):
+    _fields_ = [("host", C.c_void_p), ("dev_resident", C.c_void_p), ("rows", C.c_int64),
+                ("cols", C.c_int64), ("page_rows", C.c_int64)]
+
+
+class psi_ffn_weight(C.Structure):
+    _fields_ = [("host", C.c_void_p), ("dev_resident", C.c_void_p), ("d", C.c_int64),
+                ("h", C.c_int64), ("r", C.c_int64), ("slice", C.c_int64)]
+
+
+class psi_heads(C.Structure):
+    _fields_ = [("ptr", C.c_void_p), ("ld_token", C.c_int64), ("ld_head", C.c_int64)]
+
+
+class psi_stats(C.Structure):
+    _fields_ = [("pages_streamed", C.c_uint64), ("h2d_bytes", C.c_uint64),
+                ("resident_pages", C.c_uint64), ("kernels_launched", C.c_uint64),
+                ("timed_gemms", C.c_uint64), ("gemm_ms", C.c_double),
+                ("gemm_flops", C.c_double), ("timed_copies", C.c_uint64),
+                ("copy_ms", C.c_double), ("copy_bytes", C.c_double)]
+
+    def as_dict(self):
+        return {k: getattr(self, k) for k, _ in self._fields_}
+
+
+_lib = None
+
+
+def _status_name(s):
+    names = {0: "PSI_OK", 1: "PSI_ERR_INVALID_ARG", 2: "PSI_ERR_CAPACITY",
+             3: "PSI_ERR_PAGE_BUSY", 4: "PSI_ERR_CUDA", 5: "PSI_ERR_TIMEOUT",
+             6: "PSI_ERR_UNSUPPORTED", 7: "PSI_ERR_DEVICE"}
+    return names.get(s, f"status {s}")
+
+
+def load(path: str = LIB_PATH) -> C.CDLL:
+    """Load libpsi.so (raises if it is missing: build it with build.build())."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"libpsi.so not found at {path}; run "
+                           "weight_streamed_bf16_gb300.build.build() (needs nvcc)")
+    lib = C.CDLL(path)
+    vp, i32, i64, u32, sz = C.c_void_p, C.c_int32, C.c_int64, C.c_uint32, C.c_size_t
+    st = C.c_int
+    sig = {
+        "psi_version": (C.c_char_p, []),
+        "psi_status_string": (C.c_char_p, [st]),
+        "psi_last_error": (C.c_char_p, []),
+        "psi_plan_linear": (st, [i64, i64, sz, C.POINTER(i64)]),
+        "psi_ffn_page_bytes": (sz, [i64, i64, i64]),
+        "psi_ffn_pack": (st, [vp, vp, i64, i64, i64, i64, vp]),
+        "psi_ffn_workspace": (st, [i64, i64, i64, C.POINTER(sz), C.POINTER(sz)]),
+        "psi_arena_create": (st, [vp, sz, sz, vp, vp, C.POINTER(vp)]),
+        "psi_arena_destroy": (st, [vp]),
+        "psi_arena_slots": (i32, [vp]),
+        "psi_page_stream": (st, [vp, vp, sz, u32, C.POINTER(psi_page)]),
+        "psi_page_release": (st, [vp, psi_page]),
+        "psi_sync": (st, [vp, i64]),
+        "psi_stream_wait": (st, [vp, i64]),
+        "psi_arena_stats": (st, [vp, C.POINTER(psi_stats)]),
+        "psi_arena_reset_stats": (st, [vp]),
+        "psi_arena_set_timing": (st, [vp, i32]),
+        "psi_arena_fail_next_copy": (st, [vp]),
+        "psi_linear_paged": (st, [vp, vp, i64, i64, C.POINTER(psi_linear_weight), vp, vp,
+                                  vp, i64, u32]),
+        "psi_ffn_paged": (st, [vp, vp, i64, C.POINTER(psi_ffn_weight), vp, vp, vp, vp, vp,
+                               vp, u32]),
+        "psi_attn_partitioned": (st, [C.POINTER(psi_heads)] * 4 +
+                                 [i32, i64, i64, i32, C.c_float, i32, vp, u32]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(status: int):
+    if status != PSI_OK:
+        raise PsiError(status, load().psi_last_error().decode())
+
+
+# ------------------------------------------------------------- wrappers --
+def psi_version() -> str:
+    return load().psi_version().decode()
+
+
+def psi_status_string(s: int) -> str:
+    return load().psi_status_string(s).decode()
+
+
+def psi_last_error() -> str:
+    return load().psi_last_error().decode()
+
+
+def psi_plan_linear(rows: int, cols: int, page_bytes: int) -> int:
+    out = C.c_int64()
+    _check(load().psi_plan_linear(rows, cols, page_bytes, C.byref(out)))
+    return out.value
+
+
+def psi_ffn_page_bytes(d: int, r: int, slice_: int) -> int:
+    return load().psi_ffn_page_bytes(d, r, slice_)
+
+
+def psi_ffn_pack(U: int, V: int, d: int, h: int, r: int, slice_: int, dst: int):
+    _check(load().psi_ffn_pack(U, V, d, h, r, slice_, dst))
+
+
+def psi_ffn_workspace(N: int, r: int, slice_: int):
+    hb, ab = C.c_size_t(), C.c_size_t()
+    _check(load().psi_ffn_workspace(N, r, slice_, C.byref(hb), C.byref(ab)))
+    return hb.value, ab.value
+
+
+def psi_arena_create(dev_base: int, dev_bytes: int, page_bytes: int,
+                     compute_stream: int, copy_stream: int) -> int:
+    out = C.c_void_p()
+    _check(load().psi_arena_create(dev_base, dev_bytes, page_bytes, compute_stream,
+                                   copy_stream, C.byref(out)))
+    return out.value
+
+
+def psi_arena_destroy(arena: int):
+    _check(load().psi_arena_destroy(arena))
+
+
+def psi_arena_slots(arena: int) -> int:
+    return load().psi_arena_slots(arena)
+
+
+def psi_page_stream(arena: int, host_src: int, nbytes: int, flags: int = 0) -> psi_page:
+    pg = psi_page()
+    _check(load().psi_page_stream(arena, host_src, nbytes, flags, C.byref(pg)))
+    return pg
+
+
+def psi_page_release(arena: int, page: psi_page):
+    _check(load().psi_page_release(arena, page))
+
+
+def psi_sync(arena: int, timeout_ms: int = 60000):
+    _check(load().psi_sync(arena, timeout_ms))
+
+
+def psi_stream_wait(stream: int, timeout_ms: int = 60000):
+    _check(load().psi_stream_wait(stream, timeout_ms))
+
+
+def psi_arena_stats(arena: int) -> dict:
+    s = psi_stats()
+    _check(load().psi_arena_stats(arena, C.byref(s)))
+    return s.as_dict()
+
+
+def psi_arena_reset_stats(arena: int):
+    _check(load().psi_arena_reset_stats(arena))
+
+
+def psi_arena_set_timing(arena: int, enable: bool):
+    _check(load().psi_arena_set_timing(arena, 1 if enable else 0))
+
+
+def psi_arena_fail_next_copy(arena: int):
+    _check(load().psi_arena_fail_next_copy(arena))
+
+
+def psi_linear_paged(arena: int, X: int, N: int, K: int, W: psi_linear_weight, bias: int,
+                     residual: int | None, Y: int, ldy: int, flags: int = 0):
+    _check(load().psi_linear_paged(arena, X, N, K, C.byref(W), bias, residual or None, Y,
+                                   ldy, flags))
+
+
+def psi_ffn_paged(arena: int, X: int, N: int, W: psi_ffn_weight, a: int, b: int,
+                  hidden_ws: int, acc_ws: int, residual: int | None, Y: int, flags: int = 0):
+    _check(load().psi_ffn_paged(arena, X, N, C.byref(W), a, b, hidden_ws, acc_ws,
+                                residual or None, Y, flags))
+
+
+def psi_attn_partitioned(Q: psi_heads, K: psi_heads, V: psi_heads, O: psi_heads, heads: int,
+                         Nq: int, Nk: int, dh: int, scale: float, key_block: int, stream: int,
+                         flags: int = 0):
+    _check(load().psi_attn_partitioned(C.byref(Q), C.byref(K), C.byref(V), C.byref(O), heads,
+                                       Nq, Nk, dh, scale, key_block, stream, flags))
