@@ -97,7 +97,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -536,7 +536,7 @@ def main():
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_ms = float(t.item())
     ms_per_step = total_ms / args.steps
-    value = wl.flops * world / (total_ms * 1e-3) / 1e12
+    value = wl.flops * world / (ms_per_step * 1e-3) / 1e12
 
     # ------------------------------------------------------------ e2e ---
     Xd, Yd = wl.io()
@@ -567,7 +567,7 @@ def main():
         t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_ms = float(t.item())
-    e2e_value = wl.flops * world / (e2e_ms * 1e-3) / 1e12
+    e2e_value = wl.flops * world / (e2e_ms / args.steps * 1e-3) / 1e12
     in_bytes = Xh.numel() * Xh.element_size()
     out_bytes = Yh.numel() * Yh.element_size()
 

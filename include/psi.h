@@ -55,9 +55,9 @@ typedef enum {
 #define PSI_RESIDENT              0x1u /* weights read from dev_resident: no copies */
 #define PSI_SYNC_COPY             0x2u /* H2D page copies on the compute stream */
 #define PSI_BOUNDARY_PREGELU_BF16 0x4u /* FFN: extra BF16 write of the biased
-                                          pre-activation before GELU (section III-A,
-                                          "both native variants write the biased up
-                                          projection as BF16 before GELU") */
+                                          pre-activation before GELU, the rounding
+                                          order of the paper's native prototype
+                                          (section III-A) */
 
 typedef struct psi_arena psi_arena;
 
@@ -190,6 +190,12 @@ psi_status psi_arena_set_timing(psi_arena* arena, int32_t enable);
 /* Test hook: the next psi_page_stream call on this arena fails with
  * PSI_ERR_CUDA before enqueuing anything (host-side fault injection). */
 psi_status psi_arena_fail_next_copy(psi_arena* arena);
+/* Test hook: the next page GEMM this process launches gets a producer that
+ * issues no copies and in-kernel waits bounded by timeout_ns, so its
+ * consumers' waits expire; the kernel records the error, frees its tensor
+ * memory and returns (no fault, no hang).  The following psi_sync reports
+ * PSI_ERR_DEVICE and the context stays usable.  timeout_ns in (0, 1e10]. */
+psi_status psi_debug_stall_next_gemm(uint64_t timeout_ns);
 
 /* ---------------------------------------------------------- operators --- */
 /* Paged linear, section IV-B ("projection tiles ... output columns per

@@ -12,6 +12,12 @@ Two measures are reported for every element:
   nearly cancels (|y64| much smaller than A) cannot be expected within 2 raw
   ulp; the floor 2**-8 * A keeps the criterion a forward-error bound there.
 
+Where the operator has an inner BF16 write boundary (the FFN hidden slice),
+a correct FP32 evaluation may round an inner value the other way when the
+exact value lies within the FP32 error bound of a rounding boundary; the
+oracle's ``slack`` is the largest effect such flips can have on each output
+and is subtracted from |y - y_oracle| before grading.
+
 The tolerance is ``graded <= 2`` for every element; raw violations are listed
 with their condition number A / |y64|.  Normwise errors: max|dy| / max|y| and
 relative L2, the measure used in section IV-B of the paper.
@@ -34,9 +40,19 @@ def raw_ulps(y, y_ref) -> np.ndarray:
     return np.abs(_ordered(encode(y)) - _ordered(encode(y_ref)))
 
 
-def graded_ulps(y, y_ref, y64, A) -> np.ndarray:
+def graded_ulps(y, y_ref, y64, A, slack=None) -> np.ndarray:
     scale = np.maximum(np.abs(np.asarray(y64)), np.ldexp(np.asarray(A, np.float64), -8))
-    return np.abs(np.asarray(y, np.float64) - np.asarray(y_ref, np.float64)) / ulp(scale)
+    d = np.abs(np.asarray(y, np.float64) - np.asarray(y_ref, np.float64))
+    if slack is not None:
+        d = np.maximum(d - np.asarray(slack, np.float64), 0.0)
+    return d / ulp(scale)
+
+
+def _slack_used(y, ref, res) -> int:
+    slack = getattr(res, "slack", None)
+    if slack is None:
+        return 0
+    return int(np.count_nonzero((np.abs(y - ref) > 0) & (slack > 0)))
 
 
 def report(y, res, tol_ulps: float = 2.0) -> dict:
@@ -46,7 +62,7 @@ def report(y, res, tol_ulps: float = 2.0) -> dict:
     if y.shape != ref.shape:
         raise ValueError(f"shape mismatch {y.shape} vs {ref.shape}")
     finite = np.isfinite(y)
-    g = graded_ulps(y, ref, res.y64, res.A)
+    g = graded_ulps(y, ref, res.y64, res.A, getattr(res, "slack", None))
     r = raw_ulps(np.where(finite, y, 0.0), ref)
     diff = np.abs(y - ref)
     denom = max(float(np.max(np.abs(ref))), 1e-300)
@@ -58,6 +74,7 @@ def report(y, res, tol_ulps: float = 2.0) -> dict:
         "n": int(y.size),
         "all_finite": bool(finite.all()),
         "max_graded_ulps": float(g.max()) if g.size else 0.0,
+        "n_slack_used": _slack_used(y, ref, res),
         "max_raw_ulps": int(r.max()) if r.size else 0,
         "n_raw_gt_tol": int(len(bad)),
         "n_differing": int(np.count_nonzero(r)),

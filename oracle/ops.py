@@ -6,8 +6,8 @@ them with ``oracle.bf16.decode``).  Products of two BF16 values are exact in
 float64; sums are float64 and carry the usual error bound
 |fl(sum) - sum| <= gamma_n * sum|terms|, gamma_n = n*u/(1-n*u), u = 2**-53.
 Where that bound straddles a BF16 rounding decision, ``linear`` and ``ffn``
-recompute the element exactly with rational arithmetic and round the exact
-sum once (section IV-B, Eq.(6): "rounding the exact real sum once").
+recompute the element exactly with rational arithmetic and round that exact
+sum a single time (the exact evaluation of section IV-B, Eq.(6)).
 
 Each result carries ``y`` (BF16 values as float64), ``y64`` (the unrounded
 float64 value) and ``A`` (the sum of the magnitudes of the terms, or for
@@ -34,6 +34,8 @@ class Result:
     A: np.ndarray     # magnitude scale of the element (see module docstring)
     H: np.ndarray | None = None   # FFN hidden activations (BF16 values)
     exact_fixed: int = 0          # elements re-rounded from an exact sum
+    slack: np.ndarray | None = None  # extra |dy| allowed by ambiguous BF16
+                                     # roundings at an inner write boundary
 
 
 def _gamma(n: int) -> float:
@@ -55,8 +57,8 @@ def _fix_ties(y, y64, A, nterms, exact_elem):
 def gelu_tanh(x):
     """phi(x) = x/2 * (1 + tanh(sqrt(2/pi) * (x + 0.044715 x^3))), float64.
 
-    The pages name only "tanh-GELU" (section II-B); this is the textbook
-    tanh form of the Gaussian error linear unit.
+    Section II-B names a tanh-based GELU without constants; this is the
+    textbook tanh approximation of the Gaussian error linear unit.
     """
     x = np.asarray(x, dtype=np.float64)
     return 0.5 * x * (1.0 + np.tanh(GELU_K0 * (x + GELU_K1 * x * x * x)))
@@ -110,8 +112,9 @@ def ffn(X, U, V, a, b, residual=None, pregelu_bf16=False,
     a = np.asarray(a, np.float64)
     b = np.asarray(b, np.float64)
     t = X @ U.T + a[None, :]
+    At = np.abs(X) @ np.abs(U).T + np.abs(a)[None, :]
+    t_exact = t
     if pregelu_bf16:
-        At = np.abs(X) @ np.abs(U).T + np.abs(a)[None, :]
         tb = round_bf16(t)
         if exact_ties:
             def exact_t(ij):
@@ -122,6 +125,8 @@ def ffn(X, U, V, a, b, residual=None, pregelu_bf16=False,
             _fix_ties(tb, t, At, X.shape[1] + 2, exact_t)
         t = tb
     H = round_bf16(gelu_tanh(t))
+    jump = hidden_rounding_jump(t_exact, At, H, pregelu_bf16)
+    slack = jump @ np.abs(V).T
     y64 = H @ V.T + b[None, :]
     A = np.abs(H) @ np.abs(V).T + np.abs(b)[None, :]
     if residual is not None:
@@ -140,7 +145,38 @@ def ffn(X, U, V, a, b, residual=None, pregelu_bf16=False,
                 s += Fraction(float(residual[i, j]))
             return s
         fixed = _fix_ties(y, y64, A, H.shape[1] + 2, exact)
-    return Result(y=y, y64=y64, A=A, H=H, exact_fixed=fixed)
+    return Result(y=y, y64=y64, A=A, H=H, exact_fixed=fixed, slack=slack)
+
+
+# FP32 evaluation bound used to decide whether a BF16 rounding at the hidden
+# write boundary is ambiguous: pre-activation error <= 2**-22 * sum|terms|
+# (a few units of FP32 roundoff relative to the term magnitudes, far above
+# the ~2**-24 / sqrt(K) typical relative error of a K-term FP32 dot
+# product), GELU evaluated in FP32 to within 2**-21 * (|t| + |phi(t)|).
+T_REL = 2.0 ** -22
+PHI_REL = 2.0 ** -21
+
+
+def hidden_rounding_jump(t, At, H, pregelu_bf16=False):
+    """For each hidden element, how far B(phi(t')) can move from H when t'
+    and phi are evaluated in FP32 instead of exactly (0 where the rounding is
+    unambiguous).  Two correct evaluations of Eq.(2) with a BF16 write of H
+    may differ there by this much; the output tolerance adds the effect of
+    those differences on the down projection."""
+    d = T_REL * At
+    lo, hi = t - d, t + d
+    if pregelu_bf16:
+        lo, hi = round_bf16(lo), round_bf16(hi)
+    cands = []
+    for x in (lo, hi):
+        p = gelu_tanh(x)
+        e = PHI_REL * (np.abs(x) + np.abs(p))
+        cands.append(round_bf16(p - e))
+        cands.append(round_bf16(p + e))
+    jump = np.zeros_like(H)
+    for c in cands:
+        jump = np.maximum(jump, np.abs(c - H))
+    return jump
 
 
 def ffn_partitioned_exact(X, U, V, a, b, slices):

@@ -31,7 +31,7 @@ def run_linear(X, W, b, page_rows, slots, flags=0, residual=None, arena=None, ld
     """X, W, b: CPU bf16.  Returns the GPU output (CPU bf16 tensor)."""
     N, K = X.shape
     M = W.shape[0]
-    ldy = ldy or M
+    ldy = ldy or (M + 7) // 8 * 8   # row stride: a multiple of 8 elements
     dev = torch.device("cuda")
     Xd = X.to(dev)
     bd = b.to(dev)

@@ -247,3 +247,60 @@ def test_attention_rows_subset():
 def test_attention_needs_a_key():
     with pytest.raises(ValueError):
         ops.attention(np.zeros((1, 4)), np.zeros((0, 4)), np.zeros((0, 4)), 1.0)
+
+
+def test_ffn_hidden_rounding_slack():
+    """A hidden pre-activation placed within 2^-26 of the value whose GELU is
+    the midpoint between the BF16 neighbours 1 and 1 + 2^-7: an FP32
+    evaluation may round H either way.  The output nearly cancels, so the
+    other rounding moves y by ~60 graded ulps; the oracle's slack covers it,
+    and without the slack the same output would fail."""
+    from oracle import grade
+    mid = 1.0 + 2.0 ** -8
+    t = 1.1
+    for _ in range(80):                    # Newton on phi(t) = mid, float64
+        eps = 1e-7
+        d = (ops.gelu_tanh(t + eps) - ops.gelu_tanh(t - eps)) / (2 * eps)
+        t -= (float(ops.gelu_tanh(t)) - mid) / d
+    u = []
+    rest = t
+    for _ in range(3):                     # t as a sum of three BF16 values
+        u.append(float(bf16.round_bf16(rest)))
+        rest -= u[-1]
+    assert abs(rest) < 2.0 ** -26
+    X = np.array([[1.0, 1.0, 1.0]])
+    U = np.array([u, [2.0, 0.0, 0.0]])
+    h2 = float(bf16.round_bf16(ops.gelu_tanh(2.0)))
+    V = np.array([[1.0, float(bf16.round_bf16(-1.0 / h2))]])
+    r = ops.ffn(X, U, V, np.zeros(2), np.zeros(1))
+    h1 = r.H[0, 0]
+    assert h1 in (1.0, 1.0078125)
+    assert r.slack[0, 0] == 2.0 ** -7      # one BF16 ulp at 1, times |v| = 1
+    other = 1.0078125 if h1 == 1.0 else 1.0
+    y_alt = bf16.round_bf16(np.array([[other * V[0, 0] + r.H[0, 1] * V[0, 1]]]))
+    assert grade.report(y_alt, r)["pass"]
+    r.slack = None
+    assert not grade.report(y_alt, r)["pass"]
+    g = json.load(open(os.path.join(GOLD, "ffn_hand.json")))
+    r0 = ops.ffn(np.array(g["X"]), np.array(g["U"]), np.array(g["V"]),
+                 np.array(g["a"]), np.array(g["b"]))
+    # t = 8 has an unambiguous rounding; t = 0 = 1 - 1 only a tiny one
+    t0 = np.array(g["X"]) @ np.array(g["U"]).T
+    jump = ops.hidden_rounding_jump(t0, np.abs(np.array(g["X"])) @ np.abs(np.array(g["U"])).T,
+                                    r0.H)
+    assert jump[0, 1] == 0 and jump[0, 0] < 2.0 ** -20
+
+
+def test_ffn_slack_is_small_on_random_inputs():
+    """The slack is a small correction: a fraction of a percent of the hidden
+    values are ambiguous, and it never exceeds 2^-7 of the output scale."""
+    rng = np.random.default_rng(12)
+    X = _rand_bf16(rng, (16, 256))
+    U = _rand_bf16(rng, (512, 256), 1 / 16)
+    V = _rand_bf16(rng, (64, 512), 1 / math.sqrt(512))
+    r = ops.ffn(X, U, V, np.zeros(512), np.zeros(64))
+    t = X @ U.T
+    At = np.abs(X) @ np.abs(U).T
+    jump = ops.hidden_rounding_jump(t, At, r.H)
+    assert np.count_nonzero(jump) < 0.02 * jump.size
+    assert np.all(r.slack <= 2.0 ** -7 * r.A)

@@ -51,7 +51,8 @@ struct GemmArgs {
   int32_t K;
   int32_t epi;
   int32_t pregelu;
-  int32_t pad_;
+  int32_t debug_stall;  // test hook: the producer issues no loads, so the
+                        // consumers' bounded waits expire (see timeout_ns)
   const uint16_t* bias;   // [N]
   const uint16_t* resid;  // [M x ldo] or null
   uint16_t* out;          // [M x ldo]

@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t armed = 0;  // bit s: stage s has been armed at least once
       uint32_t last_parity = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+      for (int t = blockIdx.x; t < tiles && ok && !args.debug_stall; t += gridDim.x) {
         const int m0 = (t % m_tiles) * BM;
         const int n0 = (t / m_tiles) * BN;
         for (int kb = 0; kb < kblocks; ++kb) {

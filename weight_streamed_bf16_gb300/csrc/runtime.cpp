@@ -88,9 +88,17 @@ psi_status timed_end(psi_arena* a, cudaStream_t s, TimedLaunch t, std::vector<Ti
   return PSI_OK;
 }
 
+uint64_t g_stall_next_ns = 0;  // test hook, see psi_debug_stall_next_gemm
+
 // Launch one page GEMM on the arena's compute stream (timed if enabled).
 psi_status arena_gemm(psi_arena* a, const void* X, int64_t ldx, const void* P, int64_t ldp,
-                      const GemmArgs& g) {
+                      const GemmArgs& g0) {
+  GemmArgs g = g0;
+  if (g_stall_next_ns) {
+    g.debug_stall = 1;
+    g.timeout_ns = g_stall_next_ns;
+    g_stall_next_ns = 0;
+  }
   TimedLaunch t{};
   psi_status st;
   if (a->timing && (st = timed_begin(a, a->compute, &t)) != PSI_OK) return st;
@@ -392,6 +400,13 @@ psi_status psi_arena_reset_stats(psi_arena* a) {
 psi_status psi_arena_set_timing(psi_arena* a, int32_t enable) {
   if (!a) return set_error(PSI_ERR_INVALID_ARG, "arena_set_timing: null arena");
   a->timing = enable != 0;
+  return PSI_OK;
+}
+
+psi_status psi_debug_stall_next_gemm(uint64_t timeout_ns) {
+  if (timeout_ns == 0 || timeout_ns > 10000000000ull)
+    return set_error(PSI_ERR_INVALID_ARG, "debug_stall_next_gemm: timeout must be in (0, 10 s]");
+  g_stall_next_ns = timeout_ns;
   return PSI_OK;
 }
 

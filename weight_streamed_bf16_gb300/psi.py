@@ -35,7 +35,7 @@ EXPORTS = [
     "psi_arena_create", "psi_arena_destroy", "psi_arena_slots",
     "psi_page_stream", "psi_page_release", "psi_sync", "psi_stream_wait",
     "psi_arena_stats", "psi_arena_reset_stats", "psi_arena_set_timing",
-    "psi_arena_fail_next_copy",
+    "psi_arena_fail_next_copy", "psi_debug_stall_next_gemm",
     "psi_linear_paged", "psi_ffn_paged", "psi_attn_partitioned",
 ]
 
@@ -116,6 +116,7 @@ def load(path: str = LIB_PATH) -> C.CDLL:
         "psi_arena_reset_stats": (st, [vp]),
         "psi_arena_set_timing": (st, [vp, i32]),
         "psi_arena_fail_next_copy": (st, [vp]),
+        "psi_debug_stall_next_gemm": (st, [C.c_uint64]),
         "psi_linear_paged": (st, [vp, vp, i64, i64, C.POINTER(psi_linear_weight), vp, vp,
                                   vp, i64, u32]),
         "psi_ffn_paged": (st, [vp, vp, i64, C.POINTER(psi_ffn_weight), vp, vp, vp, vp, vp,
@@ -219,6 +220,10 @@ def psi_arena_set_timing(arena: int, enable: bool):
 
 def psi_arena_fail_next_copy(arena: int):
     _check(load().psi_arena_fail_next_copy(arena))
+
+
+def psi_debug_stall_next_gemm(timeout_ns: int):
+    _check(load().psi_debug_stall_next_gemm(timeout_ns))
 
 
 def psi_linear_paged(arena: int, X: int, N: int, K: int, W: psi_linear_weight, bias: int,
