@@ -23,8 +23,8 @@
  *    valid once the stream has finished.  Asynchronous failures (a CUDA error
  *    or an error recorded by a kernel) are returned by psi_sync or
  *    psi_stream_wait.
- *  - The caller owns every buffer.  The library creates only CUDA events and
- *    host-side tensor-map descriptors.
+ *  - The caller owns every buffer.  The library creates only CUDA events, one
+ *    auxiliary stream per arena and host-side tensor-map descriptors.
  *  - Errors: a psi_status is returned; psi_last_error() gives a message for
  *    the last failing call of the calling thread.  An argument error enqueues
  *    nothing.
@@ -142,9 +142,10 @@ size_t psi_ffn_page_bytes(int64_t d, int64_t r, int64_t slice);
 psi_status psi_ffn_pack(const void* U, const void* V, int64_t d, int64_t h,
                         int64_t r, int64_t slice, void* dst);
 
-/* Workspace of psi_ffn_paged: hidden_bytes = 2*N*slice*2 (two BF16 hidden
- * slices, so the next slice's up projection never overwrites the slice the
- * down projection is reading), acc_bytes = N*r*4 (FP32 accumulator). */
+/* Workspace of psi_ffn_paged: hidden_bytes = 2*2*N*slice*2 (two groups of
+ * two BF16 hidden slices, so the next group's up projections never
+ * overwrite the group the down projection is reading), acc_bytes = N*r*4
+ * (FP32 accumulator). */
 psi_status psi_ffn_workspace(int64_t N, int64_t r, int64_t slice,
                              size_t* hidden_bytes, size_t* acc_bytes);
 
@@ -153,7 +154,11 @@ psi_status psi_ffn_workspace(int64_t N, int64_t r, int64_t slice,
  * floor(dev_bytes / page_bytes) page slots (at least 1).  dev_base must be
  * 1024-byte aligned and page_bytes a multiple of 1024.  compute_stream and
  * copy_stream are cudaStream_t handles (they may be equal; NULL is the
- * legacy default stream).  The arena owns only events. */
+ * legacy default stream).  The arena owns events and one auxiliary stream:
+ * an operator forks it from the compute stream when it starts, runs some of
+ * its page GEMMs on it, and joins it back into the compute stream before it
+ * returns, so each operator's work is complete when the compute stream
+ * reaches the point after the call. */
 psi_status psi_arena_create(void* dev_base, size_t dev_bytes, size_t page_bytes,
                             void* compute_stream, void* copy_stream,
                             psi_arena** out);
@@ -208,21 +213,26 @@ psi_status psi_debug_stall_next_gemm(uint64_t timeout_ns);
  *   residual  dev [N x W->rows] BF16 with row stride ldy, or NULL
  *   Y    dev [N x W->rows] BF16 with row stride ldy (ldy >= rows, ldy % 8 == 0)
  * Weights stream through the arena page by page (or are read in place with
- * PSI_RESIDENT); kernels run on the arena's compute stream.  The per-element
- * arithmetic is the same in every mode, so resident and streamed results
- * are bitwise equal. */
+ * PSI_RESIDENT); page GEMMs alternate between the compute stream and the
+ * arena's auxiliary stream (disjoint output columns), so one page's tail
+ * overlaps the next page's start.  The per-element arithmetic is the same in
+ * every mode, so resident and streamed results are bitwise equal. */
 psi_status psi_linear_paged(psi_arena* arena, const void* X, int64_t N, int64_t K,
                             const psi_linear_weight* W, const void* bias,
                             const void* residual, void* Y, int64_t ldy,
                             uint32_t flags);
 
-/* Paged FFN, Eq.(2) with the reuse schedule of section III-B: for each
- * hidden slice J = 0..S-1 in order, page J is streamed, then
+/* Paged FFN, Eq.(2) with the reuse schedule of section III-B.  Hidden
+ * slices are taken in order in groups of G (G = 2 when there are at least
+ * two slices and slice % 64 == 0, else 1; fixed by the shape): for each
+ * slice J of a group, page J is streamed and
  *   H_J  = B(phi(X U_J^T + a_J))            (BF16 write; phi = tanh-GELU;
  *                                            with PSI_BOUNDARY_PREGELU_BF16
  *                                            the pre-activation is rounded too)
- *   Acc  = Acc + H_J V_:,J^T                (FP32, J = 0 stores)
- * and the last slice writes Y = B(Acc + H_S V_:,S^T + b [+ residual]).
+ * then one down projection covers the group:
+ *   Acc  = Acc + sum_{J in group} H_J V_:,J^T   (FP32, the first group stores)
+ * and the last group writes Y = B(Acc + its partial + b [+ residual]).
+ * A streamed FFN needs an arena of at least G slots (PSI_ERR_CAPACITY).
  *   X [N x d], residual and Y [N x r] (row stride r), a [h], b [r]: dev BF16
  *   hidden_ws, acc_ws: dev workspace of psi_ffn_workspace sizes (16-byte
  *   aligned); the full [N x h] hidden tensor is never formed. */

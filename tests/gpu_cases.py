@@ -72,7 +72,9 @@ def run_ffn(X, U, V, a, b, slice_, slots, flags=0, residual=None, return_hidden=
     stats = arena.stats()
     arena.close()
     S = U.shape[0] // slice_
-    last = hid.view(2, N, slice_)[(S - 1) & 1].cpu()
+    G = 2 if (S >= 2 and slice_ % 64 == 0) else 1   # slices per down pass (psi.h)
+    g, u = (S - 1) // G, (S - 1) % G
+    last = hid.view(2, N, 2 * slice_)[g & 1][:, u * slice_:(u + 1) * slice_].cpu()
     if return_hidden:
         return Y.cpu(), last, stats
     return Y.cpu()

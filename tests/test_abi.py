@@ -57,7 +57,7 @@ def test_ffn_page_bytes_and_workspace(lib):
     assert psi.psi_ffn_page_bytes(2048, 2048, 1024) == 8 << 20
     assert psi.psi_ffn_page_bytes(4096, 4096, 1024) == 16 << 20
     hb, ab = psi.psi_ffn_workspace(1024, 2048, 1024)
-    assert hb == 2 * 1024 * 1024 * 2 and ab == 1024 * 2048 * 4
+    assert hb == 2 * 2 * 1024 * 1024 * 2 and ab == 1024 * 2048 * 4
 
 
 def test_ffn_pack_layout(lib):

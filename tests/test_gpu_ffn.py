@@ -80,6 +80,17 @@ def test_ffn_resident_streamed_bitwise():
     s = run_ffn(X, U, V, a, b, 256, 2)
     r = run_ffn(X, U, V, a, b, 256, 2, flags=psi.PSI_RESIDENT)
     c = run_ffn(X, U, V, a, b, 256, 4, flags=psi.PSI_SYNC_COPY)
-    one = run_ffn(X, U, V, a, b, 256, 1)
-    for o in (r, c, one):
+    five = run_ffn(X, U, V, a, b, 256, 5)
+    for o in (r, c, five):
         assert torch.equal(s.view(torch.int16), o.view(torch.int16))
+    # a slice group needs two slots: a one-slot arena is refused up front
+    with pytest.raises(psi.PsiError) as e:
+        run_ffn(X, U, V, a, b, 256, 1)
+    assert e.value.status == psi.PSI_ERR_CAPACITY
+
+
+def test_ffn_odd_slice_count():
+    """Five slices: two groups of two and a last group of one."""
+    X, U, V, a, b = _case(130, 128, 320, 96, 17)
+    y = run_ffn(X, U, V, a, b, 64, 3)
+    check(y, ops.ffn(f64(X), f64(U), f64(V), f64(a), f64(b)), what="odd slices")

@@ -3,52 +3,58 @@
 // Paper: Precision-Preserving Subtensor Inference, section II-B Eqs.(3)-(4)
 // (online-softmax invariant over disjoint key tiles: m' = max(m, max s_j),
 // eta = e^{m-m'}, l' = eta*l + sum e^{s_j-m'}, z' = eta*z + sum e^{s_j-m'}
-// v_j, output z/l) and section III-A ("FP32 online accumulation" in place of
+// v_j, output z/l) and section III-A (FP32 online accumulation in place of
 // BF16 numerator exponential weights).
 //
-// One CTA per (head, 128-query tile).  Key tiles of 128:
-//   warp 0      TMA producer: Q once, then K_j and V_j into 2-stage rings
-//   warp 1      TMEM owner and MMA issuer:
-//                 S_j = Q K_j^T  (M=128, N=128 keys, K=128) into one of two
-//                                 TMEM S buffers, one tile ahead of softmax
-//                 O  += P_hi V_j + P_lo V_j  (V read MN-major)
-//   warps 2..5  softmax, one query row per thread: scores scaled to log2
-//               units in FP32, running max m and sum l in FP32, weights
-//               p = 2^(s - m) in FP32 split into p_hi = B(p) and p_lo =
-//               B(p - p_hi) (so the tensor-core operand carries ~16 bits of
-//               p, FP32 fidelity within 2^-17), O rescaled by eta in TMEM
-//               when the max moves, and the final O / l written as BF16.
+// One CTA per (head, 256 queries) = two 128-query tiles that share every K
+// and V tile.  Key tiles of 128:
+//   warp 0      TMA producer: Q (both tiles) once, then K_j and V_j into
+//               2-stage rings
+//   warp 1      TMEM owner and MMA issuer, ping-ponging the two query tiles:
+//                 S_t = Q_t K_j^T          (M=128, N=128 keys, K=128) into
+//                                          the S/P columns of tile t
+//                 O_t += P_t,hi V_j + P_t,lo V_j   (P read from tensor memory,
+//                                          V read MN-major from shared memory)
+//   warps 2..5  softmax of tile 0, warps 6..9 softmax of tile 1, one query
+//               row per thread: scores scaled to log2 units in FP32, running
+//               max m and sum l in FP32, weights p = 2^(s - m) in FP32 split
+//               into p_hi = B(p) and p_lo = B(p - p_hi) (the tensor-core
+//               operand then carries p to within 2^-17 relative) and written
+//               over the row's S columns; O rescaled by eta in tensor memory
+//               when the max moves; O / l written as BF16 at the end.
+// While one softmax warpgroup works on its tile, the tensor core runs the
+// other tile's MMAs.
 #include "internal.h"
 #include "ptx.cuh"
 
 namespace psi {
 namespace {
 
-constexpr int BQ = 128;
-constexpr int BKEY = 128;
+constexpr int BQ = 128;      // queries per tile
+constexpr int NT = 2;        // query tiles per CTA
+constexpr int BKEY = 128;    // keys per tile
 constexpr int DH = 128;
-constexpr int kThreads = 192;
+constexpr int kThreads = 64 + NT * 128;
 constexpr int TILE64 = 128 * 128;  // one [128 rows x 64 cols] BF16 swizzled block, bytes
 
-constexpr int OFF_Q = 0;
-constexpr int OFF_K = OFF_Q + 2 * TILE64;       // 2 stages x 2 column blocks
+constexpr int OFF_Q = 0;                              // NT tiles x 2 column blocks
+constexpr int OFF_K = OFF_Q + NT * 2 * TILE64;        // 2 stages x 2 column blocks
 constexpr int OFF_V = OFF_K + 2 * 2 * TILE64;
-constexpr int OFF_PHI = OFF_V + 2 * 2 * TILE64;
-constexpr int OFF_PLO = OFF_PHI + 2 * TILE64;
-constexpr int OFF_BAR = OFF_PLO + 2 * TILE64;   // 224 KiB
+constexpr int OFF_BAR = OFF_V + 2 * 2 * TILE64;       // 192 KiB
 constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
 
-constexpr uint32_t TM_S = 0;     // two S buffers: columns 0..127, 128..255
-constexpr uint32_t TM_O = 256;   // O accumulator: columns 256..383
+// tensor memory: tile t uses columns [256 t, 256 t + 128) for S (and P over
+// it: P_hi in the first 64 columns, P_lo in the next 64) and [256 t + 128,
+// 256 t + 256) for O
 constexpr uint32_t TM_COLS = 512;
+__device__ __forceinline__ uint32_t tm_s(int t) { return 256u * t; }
+__device__ __forceinline__ uint32_t tm_o(int t) { return 256u * t + 128u; }
 
 struct __align__(8) ABars {
   uint64_t q_full;
   uint64_t k_full[2], k_empty[2];
   uint64_t v_full[2], v_empty[2];
-  uint64_t s_full[2], s_empty[2];
-  uint64_t p_full;
-  uint64_t pv_done;
+  uint64_t s_full[NT], p_full[NT], pv_done[NT];
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -79,9 +85,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   ABars* bars = reinterpret_cast<ABars*>(smem + OFF_BAR);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int q_tiles = (args.Nq + BQ - 1) / BQ;
-  const int head = blockIdx.x / q_tiles;
-  const int q0 = (blockIdx.x % q_tiles) * BQ;
+  const int q_blocks = (args.Nq + NT * BQ - 1) / (NT * BQ);
+  const int head = blockIdx.x / q_blocks;
+  const int q0 = (blockIdx.x % q_blocks) * (NT * BQ);
   const int nb = (args.Nk + BKEY - 1) / BKEY;
   volatile int* abort_flag = &bars->abort_flag;
   constexpr int kWhere = KID_ATTN * 16;
@@ -93,11 +99,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->k_empty[s], 1);
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->v_empty[s], 1);
-      mbar_init(&bars->s_full[s], 1);
-      mbar_init(&bars->s_empty[s], 128);
     }
-    mbar_init(&bars->p_full, 128);
-    mbar_init(&bars->pv_done, 1);
+    for (int t = 0; t < NT; ++t) {
+      mbar_init(&bars->s_full[t], 1);
+      mbar_init(&bars->p_full[t], 128);
+      mbar_init(&bars->pv_done[t], 1);
+    }
     mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
     fence_mbar_init();
@@ -119,19 +126,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t k_armed = 0, v_armed = 0;  // per-stage parity of the last arming
       int k_cnt[2] = {0, 0}, v_cnt[2] = {0, 0};
-      mbar_arrive_expect_tx(&bars->q_full, 2 * TILE64);
-      tma_load_2d(smem + OFF_Q, &tmQ, &bars->q_full, head * vq.hx, head * vq.hy + q0);
-      tma_load_2d(smem + OFF_Q + TILE64, &tmQ, &bars->q_full, head * vq.hx + 64,
-                  head * vq.hy + q0);
-      bool ok = true;
-      for (int j = 0; j < nb && ok; ++j) {
+      mbar_arrive_expect_tx(&bars->q_full, NT * 2 * TILE64);
+      for (int t = 0; t < NT; ++t)
+        for (int cb = 0; cb < 2; ++cb)
+          tma_load_2d(smem + OFF_Q + (t * 2 + cb) * TILE64, &tmQ, &bars->q_full,
+                      head * vq.hx + cb * 64, head * vq.hy + q0 + t * BQ);
+      for (int j = 0; j < nb; ++j) {
         const int s = j & 1;
         const uint32_t par = ((j >> 1) & 1) ^ 1;
         const int key0 = j * BKEY;
         if (!mbar_wait(&bars->k_empty[s], par, abort_flag, args.timeout_ns)) {
           record_error(args.err, 1, kWhere + 0, j, 0);
           bars->abort_flag = 1;
-          ok = false;
           break;
         }
         uint8_t* kd = smem + OFF_K + s * 2 * TILE64;
@@ -143,7 +149,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&bars->v_empty[s], par, abort_flag, args.timeout_ns)) {
           record_error(args.err, 1, kWhere + 0, j, 1);
           bars->abort_flag = 1;
-          ok = false;
           break;
         }
         uint8_t* vd = smem + OFF_V + s * 2 * TILE64;
@@ -169,68 +174,67 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, 128, 0, 1);  // V is MN-major
-      const uint32_t sQ = smem_u32(smem + OFF_Q);
       bool ok = true, issued = false;
       auto fail = [&](int j, int what) {
         record_error(args.err, 1, kWhere + 1, j, what);
         bars->abort_flag = 1;
         ok = false;
       };
-      auto issue_s = [&](int j) {
+      // S_t = Q_t K_j^T into tile t's S/P columns
+      auto issue_s = [&](int j, int t) {
         const int s = j & 1;
-        if (!mbar_wait(&bars->k_full[s], (j >> 1) & 1, abort_flag, args.timeout_ns)) {
-          fail(j, 0);
-          return;
+        if (t == 0) {
+          if (!mbar_wait(&bars->k_full[s], (j >> 1) & 1, abort_flag, args.timeout_ns)) {
+            fail(j, 0);
+            return;
+          }
+          tc_fence_after();
         }
-        if (!mbar_wait(&bars->s_empty[s], ((j >> 1) & 1) ^ 1, abort_flag, args.timeout_ns)) {
-          fail(j, 1);
-          return;
-        }
-        tc_fence_after();
         const uint32_t sK = smem_u32(smem + OFF_K + s * 2 * TILE64);
+        const uint32_t sQ = smem_u32(smem + OFF_Q + t * 2 * TILE64);
 #pragma unroll
         for (int kk = 0; kk < DH / 16; ++kk) {
           const uint32_t off = (kk >> 2) * TILE64 + (kk & 3) * 32;
-          mma_bf16_ss(tmem + TM_S + s * 128, sdesc_sw128(sQ + off, 16, 1024),
+          mma_bf16_ss(tmem + tm_s(t), sdesc_sw128(sQ + off, 16, 1024),
                       sdesc_sw128(sK + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
         }
+        mma_commit(&bars->s_full[t]);
+        if (t == NT - 1) mma_commit(&bars->k_empty[s]);  // both tiles have read K_j
         issued = true;
-        mma_commit(&bars->k_empty[s]);
-        mma_commit(&bars->s_full[s]);
       };
       if (!mbar_wait(&bars->q_full, 0, abort_flag, args.timeout_ns)) fail(-1, 2);
-      if (ok) issue_s(0);
+      for (int t = 0; t < NT && ok; ++t) issue_s(0, t);
       for (int j = 0; j < nb && ok; ++j) {
-        if (j + 1 < nb) {
-          issue_s(j + 1);
-          if (!ok) break;
-        }
         const int s = j & 1;
-        if (!mbar_wait(&bars->p_full, j & 1, abort_flag, args.timeout_ns)) {
-          fail(j, 3);
-          break;
-        }
         if (!mbar_wait(&bars->v_full[s], (j >> 1) & 1, abort_flag, args.timeout_ns)) {
           fail(j, 4);
           break;
         }
-        tc_fence_after();
         const uint32_t sV = smem_u32(smem + OFF_V + s * 2 * TILE64);
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const uint32_t sP = smem_u32(smem + (half ? OFF_PLO : OFF_PHI));
-#pragma unroll
-          for (int kk = 0; kk < BKEY / 16; ++kk) {
-            const uint32_t aoff = (kk >> 2) * TILE64 + (kk & 3) * 32;
-            // 16 keys = 16 rows of 128 B in each V column block; the two
-            // 64-wide dh blocks are TILE64 bytes apart (LBO)
-            mma_bf16_ss(tmem + TM_O, sdesc_sw128(sP + aoff, 16, 1024),
-                        sdesc_sw128(sV + kk * 2048, TILE64, 1024), idesc_o,
-                        (j | half | kk) != 0 ? 1u : 0u);
+        for (int t = 0; t < NT && ok; ++t) {
+          if (!mbar_wait(&bars->p_full[t], j & 1, abort_flag, args.timeout_ns)) {
+            fail(j, 3);
+            break;
           }
+          tc_fence_after();
+          // O_t += P_hi V_j + P_lo V_j: P from tensor memory (8 columns per
+          // 16 keys), V rows kk*16.. of both 64-wide dh blocks (LBO apart)
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+#pragma unroll
+            for (int kk = 0; kk < BKEY / 16; ++kk) {
+              mma_bf16_ts(tmem + tm_o(t), tmem + tm_s(t) + half * 64 + kk * 8,
+                          sdesc_sw128(sV + kk * 2048, TILE64, 1024), idesc_o,
+                          (j | half | kk) != 0 ? 1u : 0u);
+            }
+          }
+          mma_commit(&bars->pv_done[t]);
+          // tile t's next scores overwrite its P: issued after its PV MMAs,
+          // which the tensor core executes first
+          if (j + 1 < nb) issue_s(j + 1, t);
         }
+        if (!ok) break;
         mma_commit(&bars->v_empty[s]);
-        mma_commit(&bars->pv_done);
       }
       if (issued) {
         mma_commit(&bars->drain);
@@ -241,18 +245,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------------------------------------------------- softmax --
-    const int q = warp & 3;
-    const int row = q * 32 + lane;  // query row within the tile
+    const int t = (warp - 2) >> 2;   // query tile of this warpgroup
+    const int q = warp & 3;          // TMEM lane quarter
+    const int row = q * 32 + lane;   // query row within the tile
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    const uint32_t tS = tmem + tm_s(t) + lane_off;
+    const uint32_t tO = tmem + tm_o(t) + lane_off;
     float m2 = -INFINITY;  // running max, log2 units
     float l = 0.f;         // running sum of weights
     bool ok = true;
-    uint8_t* phi = smem + OFF_PHI;
-    uint8_t* plo = smem + OFF_PLO;
     for (int j = 0; j < nb; ++j) {
-      const int b = j & 1;
-      if (!mbar_wait(&bars->s_full[b], (j >> 1) & 1, abort_flag, args.timeout_ns)) {
-        if (lane == 0) record_error(args.err, 1, kWhere + 2, j, q);
+      if (!mbar_wait(&bars->s_full[t], j & 1, abort_flag, args.timeout_ns)) {
+        if (lane == 0) record_error(args.err, 1, kWhere + 2, j, t * 4 + q);
         bars->abort_flag = 1;
         ok = false;
         break;
@@ -262,14 +266,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < BKEY / 32; ++c) {
         uint32_t r[32];
-        tmem_ld_32x32b_x32(tmem + TM_S + b * 128 + c * 32 + lane_off, r);
+        tmem_ld_32x32b_x32(tS + c * 32, r);
         tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[i]);
       }
-      tc_fence_before();
-      mbar_arrive(&bars->s_empty[b]);
-
       const int kvalid = args.Nk - j * BKEY;  // keys of this tile that exist
       float mx = -INFINITY;
 #pragma unroll
@@ -289,11 +290,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       l = eta * l + rs;
       m2 = m_new;
-
+      // P over the S columns (all of S is in registers): 64 columns of p_hi
+      // pairs, then 64 of p_lo pairs; keys 2i and 2i+1 share column i
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t hi[16], lo[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float p0 = s[c * 32 + 2 * i];
+          const float p1 = s[c * 32 + 2 * i + 1];
+          hi[i] = pack_bf16x2(p0, p1);
+          lo[i] = pack_bf16x2(p0 - bf16_lo(hi[i]), p1 - bf16_hi(hi[i]));
+        }
+        tmem_st_32x32b_x16(tS + c * 16, hi);
+        tmem_st_32x32b_x16(tS + 64 + c * 16, lo);
+      }
       if (j > 0) {
-        // the previous PV has finished: P buffers are free and O is stable
-        if (!mbar_wait(&bars->pv_done, (j - 1) & 1, abort_flag, args.timeout_ns)) {
-          if (lane == 0) record_error(args.err, 1, kWhere + 3, j, q);
+        // the previous PV of this tile has finished: O is stable
+        if (!mbar_wait(&bars->pv_done[t], (j - 1) & 1, abort_flag, args.timeout_ns)) {
+          if (lane == 0) record_error(args.err, 1, kWhere + 3, j, t * 4 + q);
           bars->abort_flag = 1;
           ok = false;
           break;
@@ -303,57 +318,40 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
           for (int c = 0; c < DH / 32; ++c) {
             uint32_t r[32];
-            tmem_ld_32x32b_x32(tmem + TM_O + c * 32 + lane_off, r);
+            tmem_ld_32x32b_x32(tO + c * 32, r);
             tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * eta);
-            tmem_st_32x32b_x32(tmem + TM_O + c * 32 + lane_off, r);
+            tmem_st_32x32b_x32(tO + c * 32, r);
           }
-          tmem_wait_st();
         }
       }
-      // P_hi / P_lo rows into the 128B-swizzled K-major operand layout
-#pragma unroll
-      for (int ch = 0; ch < BKEY / 8; ++ch) {
-        uint32_t hi[4], lo[4];
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const float p0 = s[ch * 8 + 2 * t];
-          const float p1 = s[ch * 8 + 2 * t + 1];
-          hi[t] = pack_bf16x2(p0, p1);
-          lo[t] = pack_bf16x2(p0 - bf16_lo(hi[t]), p1 - bf16_hi(hi[t]));
-        }
-        const int cb = ch >> 3;        // 64-key column block
-        const int c16 = ch & 7;        // 16-byte chunk within the 128-byte row
-        const uint32_t off = cb * TILE64 + row * 128 + ((c16 ^ (row & 7)) << 4);
-        *reinterpret_cast<uint4*>(phi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(plo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-      }
-      fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&bars->p_full);
+      mbar_arrive(&bars->p_full[t]);
     }
     if (ok && nb > 0) {
-      if (!mbar_wait(&bars->pv_done, (nb - 1) & 1, abort_flag, args.timeout_ns)) {
-        if (lane == 0) record_error(args.err, 1, kWhere + 3, nb, q);
+      if (!mbar_wait(&bars->pv_done[t], (nb - 1) & 1, abort_flag, args.timeout_ns)) {
+        if (lane == 0) record_error(args.err, 1, kWhere + 3, nb, t * 4 + q);
         bars->abort_flag = 1;
       } else {
         tc_fence_after();
-        const int tok = q0 + row;
-        uint16_t* orow = args.O + head * args.o_ld_head + static_cast<int64_t>(tok) * args.o_ld_token;
+        const int tok = q0 + t * BQ + row;
+        uint16_t* orow =
+            args.O + head * args.o_ld_head + static_cast<int64_t>(tok) * args.o_ld_token;
 #pragma unroll 1
         for (int c = 0; c < DH / 32; ++c) {
           uint32_t r[32];
-          tmem_ld_32x32b_x32(tmem + TM_O + c * 32 + lane_off, r);
+          tmem_ld_32x32b_x32(tO + c * 32, r);
           tmem_wait_ld();
           if (tok < args.Nq) {
             uint4* o4 = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
+            for (int u = 0; u < 4; ++u) {
               float v[8];
 #pragma unroll
-              for (int i = 0; i < 8; ++i) v[i] = __fdiv_rn(__uint_as_float(r[8 * t + i]), l);
-              o4[t] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+              for (int i = 0; i < 8; ++i) v[i] = __fdiv_rn(__uint_as_float(r[8 * u + i]), l);
+              o4[u] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
                                  pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
             }
           }
@@ -409,8 +407,8 @@ psi_status launch_attention(const psi_heads* Q, const psi_heads* K, const psi_he
     if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute(attn)");
     attr_set = true;
   }
-  const int q_tiles = (a.Nq + BQ - 1) / BQ;
-  const long long grid = static_cast<long long>(q_tiles) * a.heads;
+  const int q_blocks = (a.Nq + NT * BQ - 1) / (NT * BQ);
+  const long long grid = static_cast<long long>(q_blocks) * a.heads;
   if (grid <= 0) return PSI_OK;
   if (grid > 0x7FFFFFFFLL) return set_error(PSI_ERR_UNSUPPORTED, "attention: grid too large");
   attn_kernel<<<static_cast<unsigned>(grid), kThreads, SMEM_BYTES, stream>>>(mq, mk, mv, vq, vk,

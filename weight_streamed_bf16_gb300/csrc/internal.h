@@ -53,6 +53,9 @@ struct GemmArgs {
   int32_t pregelu;
   int32_t debug_stall;  // test hook: the producer issues no loads, so the
                         // consumers' bounded waits expire (see timeout_ns)
+  int32_t k_split;      // k-blocks (of 64) read from the first page; the rest
+                        // come from the second page (0: one page)
+  int32_t pad_;
   const uint16_t* bias;   // [N]
   const uint16_t* resid;  // [M x ldo] or null
   uint16_t* out;          // [M x ldo]
@@ -64,9 +67,12 @@ struct GemmArgs {
 };
 
 // D[M x N] = X[M x K] * P[N x K]^T with the chosen epilogue, on `stream`.
-// X and P are BF16 row-major with row strides ldx and ldp (elements).
+// X and P are BF16 row-major with row strides ldx and ldp (elements).  With
+// args.k_split > 0 the K range is split over two pages: columns
+// [0, 64*k_split) of P come from P, the rest from P2 (same row stride).
 psi_status launch_page_gemm(const void* X, int64_t ldx, const void* P, int64_t ldp,
-                            const GemmArgs& args, cudaStream_t stream);
+                            const GemmArgs& args, cudaStream_t stream,
+                            const void* P2 = nullptr);
 
 // ------------------------------------------------------------ attention --
 struct AttnArgs {

@@ -11,12 +11,15 @@
 //
 // Structure (one CTA per SM, persistent over output tiles of 128 x BN):
 //   warp 0      TMA producer: X tile [128 x 64] and page tile [BN x 64] per
-//               stage into a STAGES-deep shared-memory ring (128B swizzle)
+//               stage into a STAGES-deep shared-memory ring (128B swizzle);
+//               the K range may span two pages (grouped FFN down slices)
 //   warp 1      TMEM allocation and the MMA issuer: 4 MMAs of K = 16 per
 //               stage into one of two TMEM accumulators (2 x BN columns)
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator rows, fused
-//               epilogue, global stores; frees the accumulator so the next
-//               tile's MMAs overlap this tile's epilogue
+//   warps 2..9  epilogue, two warps per TMEM lane quarter (one per column
+//               half): tcgen05.ld of the accumulator rows, fused epilogue,
+//               global stores, FP32 accumulator loads issued ahead of use;
+//               frees the accumulator so the next tile's MMAs overlap this
+//               tile's epilogue
 // Every wait is bounded; on expiry the kernel records an error, drains its
 // own copies and MMAs, frees TMEM and returns.
 #include "internal.h"
@@ -27,7 +30,8 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;  // one 128-byte swizzle row of BF16
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;  // producer, MMA, 8 epilogue warps
+constexpr int kEpiWarps = 8;
 
 template <int BN>
 struct Cfg {
@@ -70,10 +74,24 @@ __device__ __forceinline__ float round_bf16_f(float x) {
   return bf16_lo(pack_bf16x2(x, 0.f));
 }
 
+__device__ __forceinline__ bool epi_reads_acc(int epi) {
+  return epi == EPI_ACC_ADD || epi == EPI_ACC_FINAL;
+}
+
+// The 32 FP32 accumulator values of one row chunk (full chunks only).
+__device__ __forceinline__ void load_acc32(const GemmArgs& a, int row, int col0,
+                                           float4 (&q)[8]) {
+  const float4* p4 =
+      reinterpret_cast<const float4*>(a.accf + static_cast<int64_t>(row) * a.ldacc + col0);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) q[j] = p4[j];
+}
+
 // Epilogue of 32 consecutive columns of one row.  v[] are the FP32
-// accumulator values; col0 is the first column; ncol <= 32 valid columns.
+// accumulator values; col0 is the first column; ncol <= 32 valid columns;
+// wq[] holds the FP32 workspace values of a full chunk (loaded ahead).
 __device__ __forceinline__ void epilogue_row32(const GemmArgs& a, int row, int col0, int ncol,
-                                               float (&v)[32]) {
+                                               float (&v)[32], const float4 (&wq)[8]) {
   const bool full = (ncol == 32);
   if (a.epi == EPI_ACC_STORE || a.epi == EPI_ACC_ADD) {
     float* p = a.accf + static_cast<int64_t>(row) * a.ldacc + col0;
@@ -83,11 +101,10 @@ __device__ __forceinline__ void epilogue_row32(const GemmArgs& a, int row, int c
       for (int j = 0; j < 8; ++j) {
         float4 o = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
         if (a.epi == EPI_ACC_ADD) {
-          const float4 q = p4[j];
-          o.x = q.x + o.x;
-          o.y = q.y + o.y;
-          o.z = q.z + o.z;
-          o.w = q.w + o.w;
+          o.x = wq[j].x + o.x;
+          o.y = wq[j].y + o.y;
+          o.z = wq[j].z + o.z;
+          o.w = wq[j].w + o.w;
         }
         p4[j] = o;
       }
@@ -118,14 +135,12 @@ __device__ __forceinline__ void epilogue_row32(const GemmArgs& a, int row, int c
   if (a.epi == EPI_ACC_FINAL) {
     const float* p = a.accf + static_cast<int64_t>(row) * a.ldacc + col0;
     if (full) {
-      const float4* p4 = reinterpret_cast<const float4*>(p);
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const float4 q = p4[j];
-        v[4 * j] = q.x + v[4 * j];
-        v[4 * j + 1] = q.y + v[4 * j + 1];
-        v[4 * j + 2] = q.z + v[4 * j + 2];
-        v[4 * j + 3] = q.w + v[4 * j + 3];
+        v[4 * j] = wq[j].x + v[4 * j];
+        v[4 * j + 1] = wq[j].y + v[4 * j + 1];
+        v[4 * j + 2] = wq[j].z + v[4 * j + 2];
+        v[4 * j + 3] = wq[j].w + v[4 * j + 3];
       }
     } else {
       for (int j = 0; j < ncol; ++j) v[j] = p[j] + v[j];
@@ -179,7 +194,8 @@ __device__ __forceinline__ void epilogue_row32(const GemmArgs& a, int row, int c
 template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     page_gemm_kernel(const __grid_constant__ CUtensorMap tmX,
-                     const __grid_constant__ CUtensorMap tmP, const GemmArgs args) {
+                     const __grid_constant__ CUtensorMap tmP,
+                     const __grid_constant__ CUtensorMap tmP2, const GemmArgs args) {
   using C = Cfg<BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -203,13 +219,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&bars->tfull[a], 1);
-      mbar_init(&bars->tempty[a], 4);
+      mbar_init(&bars->tempty[a], kEpiWarps);
     }
     mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmX);
     tma_prefetch_desc(&tmP);
+    if (args.k_split) tma_prefetch_desc(&tmP2);
   }
   if (warp == 1) {
     tmem_alloc(&bars->tmem_base, C::TMEM_COLS);
@@ -240,7 +257,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mbar_arrive_expect_tx(&bars->full[stage], C::STAGE_BYTES);
           tma_load_2d(sA + stage * C::A_BYTES, &tmX, &bars->full[stage], kb * BK, m0);
-          tma_load_2d(sB + stage * C::B_BYTES, &tmP, &bars->full[stage], kb * BK, n0);
+          if (args.k_split == 0 || kb < args.k_split)
+            tma_load_2d(sB + stage * C::B_BYTES, &tmP, &bars->full[stage], kb * BK, n0);
+          else
+            tma_load_2d(sB + stage * C::B_BYTES, &tmP2, &bars->full[stage],
+                        (kb - args.k_split) * BK, n0);
           armed |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == C::STAGES) {
@@ -315,33 +336,47 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // --------------------------------------------------------- epilogue --
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int q = warp & 3;                 // TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;       // column half of the tile
+    constexpr int CH = BN / 64;             // 32-column chunks per half
+    const bool pre = epi_reads_acc(args.epi);
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
       const int m0 = (t % m_tiles) * BM;
-      const int n0 = (t / m_tiles) * BN;
+      const int n0 = (t / m_tiles) * BN + half * (BN / 2);
+      const int row = m0 + q * 32 + lane;
+      const bool row_ok = row < args.M;
+      // the FP32 workspace does not depend on this tile's MMAs: start its
+      // loads before waiting for the accumulator
+      float4 nxt[8];
+      if (pre && row_ok && n0 + 32 <= args.N) load_acc32(args, row, n0, nxt);
       if (!mbar_wait(&bars->tfull[acc], acc_phase, abort_flag, args.timeout_ns)) {
         if (lane == 0) record_error(args.err, 1, KID_GEMM * 16 + 2, t, q);
         bars->abort_flag = 1;
         break;
       }
       tc_fence_after();
-      const int row = m0 + q * 32 + lane;
-      const uint32_t tbase = tmem + static_cast<uint32_t>(acc * BN) +
+      const uint32_t tbase = tmem + static_cast<uint32_t>(acc * BN + half * (BN / 2)) +
                              (static_cast<uint32_t>(q * 32) << 16);
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = 0; c < CH; ++c) {
+        float4 cur[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) cur[j] = nxt[j];
+        const int col0 = n0 + c * 32;
+        if (pre && c + 1 < CH && row_ok && col0 + 64 <= args.N)
+          load_acc32(args, row, col0 + 32, nxt);
+        __syncwarp();
         uint32_t r[32];
         tmem_ld_32x32b_x32(tbase + c * 32, r);
         tmem_wait_ld();
-        const int col0 = n0 + c * 32;
-        if (col0 < args.N && row < args.M) {
+        if (col0 < args.N && row_ok) {
           float v[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
           const int ncol = min(32, args.N - col0);
-          epilogue_row32(args, row, col0, ncol, v);
+          epilogue_row32(args, row, col0, ncol, v, cur);
         }
       }
       tc_fence_before();
@@ -363,8 +398,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int BN>
-psi_status launch_bn(const CUtensorMap& tx, const CUtensorMap& tp, const GemmArgs& a,
-                     cudaStream_t s) {
+psi_status launch_bn(const CUtensorMap& tx, const CUtensorMap& tp, const CUtensorMap& tp2,
+                     const GemmArgs& a, cudaStream_t s) {
   using C = Cfg<BN>;
   static bool attr_set = false;  // per process; one device per process
   if (!attr_set) {
@@ -376,7 +411,7 @@ psi_status launch_bn(const CUtensorMap& tx, const CUtensorMap& tp, const GemmArg
   }
   const int tiles = ((a.M + BM - 1) / BM) * ((a.N + BN - 1) / BN);
   const int grid = tiles < num_sms() ? tiles : num_sms();
-  page_gemm_kernel<BN><<<grid, kThreads, C::SMEM_BYTES, s>>>(tx, tp, a);
+  page_gemm_kernel<BN><<<grid, kThreads, C::SMEM_BYTES, s>>>(tx, tp, tp2, a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_error(e, "page_gemm launch");
   return PSI_OK;
@@ -387,18 +422,27 @@ psi_status launch_bn(const CUtensorMap& tx, const CUtensorMap& tp, const GemmArg
 int gemm_bn_for(int64_t N) { return N > 128 ? 256 : (N > 64 ? 128 : 64); }
 
 psi_status launch_page_gemm(const void* X, int64_t ldx, const void* P, int64_t ldp,
-                            const GemmArgs& a, cudaStream_t stream) {
+                            const GemmArgs& a, cudaStream_t stream, const void* P2) {
   if (a.M <= 0 || a.N <= 0 || a.K <= 0) return PSI_OK;
   const int bn = gemm_bn_for(a.N);
-  CUtensorMap tx, tp;
+  CUtensorMap tx, tp, tp2;
   psi_status st = make_tmap_2d(&tx, X, a.M, a.K, ldx, BM, BK);
   if (st != PSI_OK) return st;
-  st = make_tmap_2d(&tp, P, a.N, a.K, ldp, bn, BK);
+  if (a.k_split > 0) {
+    const int64_t k1 = static_cast<int64_t>(a.k_split) * BK;
+    if (!P2 || k1 >= a.K) return set_error(PSI_ERR_INVALID_ARG, "page_gemm: bad K split");
+    st = make_tmap_2d(&tp, P, a.N, k1, ldp, bn, BK);
+    if (st != PSI_OK) return st;
+    st = make_tmap_2d(&tp2, P2, a.N, a.K - k1, ldp, bn, BK);
+  } else {
+    st = make_tmap_2d(&tp, P, a.N, a.K, ldp, bn, BK);
+    tp2 = tp;
+  }
   if (st != PSI_OK) return st;
   switch (bn) {
-    case 256: return launch_bn<256>(tx, tp, a, stream);
-    case 128: return launch_bn<128>(tx, tp, a, stream);
-    default: return launch_bn<64>(tx, tp, a, stream);
+    case 256: return launch_bn<256>(tx, tp, tp2, a, stream);
+    case 128: return launch_bn<128>(tx, tp, tp2, a, stream);
+    default: return launch_bn<64>(tx, tp, tp2, a, stream);
   }
 }
 

@@ -43,6 +43,11 @@ struct psi_arena {
   int nslots = 0;
   cudaStream_t compute = nullptr;
   cudaStream_t copy = nullptr;
+  // second consumer stream owned by the arena: consecutive page GEMMs run on
+  // alternating streams so one kernel's tail overlaps the next one's start
+  cudaStream_t aux = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  cudaEvent_t ev_up[2] = {nullptr, nullptr}, ev_down[2] = {nullptr, nullptr};
   std::vector<cudaEvent_t> ready;      // copy into the slot complete
   std::vector<cudaEvent_t> consumed;   // last consumer of the slot complete
   std::vector<uint8_t> has_consumed;   // consumed[s] has been recorded
@@ -60,6 +65,12 @@ struct psi_arena {
 namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// Hidden slices per down-projection pass.  Two slices share one FP32
+// accumulator read-modify-write (half the accumulator traffic of one slice
+// per pass); the group depends on the slice shape only, never on the arena.
+constexpr int64_t kFfnGroupMax = 2;
+int64_t ffn_group(int64_t S, int64_t sl) { return (S >= 2 && sl % 64 == 0) ? 2 : 1; }
 
 cudaEvent_t pool_get(psi_arena* a) {
   if (!a->pool.empty()) {
@@ -91,8 +102,8 @@ psi_status timed_end(psi_arena* a, cudaStream_t s, TimedLaunch t, std::vector<Ti
 uint64_t g_stall_next_ns = 0;  // test hook, see psi_debug_stall_next_gemm
 
 // Launch one page GEMM on the arena's compute stream (timed if enabled).
-psi_status arena_gemm(psi_arena* a, const void* X, int64_t ldx, const void* P, int64_t ldp,
-                      const GemmArgs& g0) {
+psi_status arena_gemm(psi_arena* a, cudaStream_t sm, const void* X, int64_t ldx, const void* P,
+                      int64_t ldp, const GemmArgs& g0, const void* P2 = nullptr) {
   GemmArgs g = g0;
   if (g_stall_next_ns) {
     g.debug_stall = 1;
@@ -101,13 +112,13 @@ psi_status arena_gemm(psi_arena* a, const void* X, int64_t ldx, const void* P, i
   }
   TimedLaunch t{};
   psi_status st;
-  if (a->timing && (st = timed_begin(a, a->compute, &t)) != PSI_OK) return st;
-  st = launch_page_gemm(X, ldx, P, ldp, g, a->compute);
+  if (a->timing && (st = timed_begin(a, sm, &t)) != PSI_OK) return st;
+  st = launch_page_gemm(X, ldx, P, ldp, g, sm, P2);
   if (st != PSI_OK) return st;
   a->stats.kernels_launched++;
   if (a->timing) {
     t.work = 2.0 * g.M * static_cast<double>(g.N) * g.K;
-    return timed_end(a, a->compute, t, &a->gemm_t);
+    return timed_end(a, sm, t, &a->gemm_t);
   }
   return PSI_OK;
 }
@@ -213,7 +224,8 @@ psi_status psi_ffn_workspace(int64_t N, int64_t r, int64_t slice, size_t* hidden
                              size_t* acc_bytes) {
   if (N < 0 || r <= 0 || slice <= 0 || !hidden_bytes || !acc_bytes)
     return set_error(PSI_ERR_INVALID_ARG, "ffn_workspace: bad arguments");
-  *hidden_bytes = 2 * static_cast<size_t>(N) * static_cast<size_t>(slice) * 2;
+  *hidden_bytes = 2 * static_cast<size_t>(kFfnGroupMax) * static_cast<size_t>(N) *
+                  static_cast<size_t>(slice) * 2;
   *acc_bytes = static_cast<size_t>(N) * static_cast<size_t>(r) * 4;
   return PSI_OK;
 }
@@ -249,6 +261,17 @@ psi_status psi_arena_create(void* dev_base, size_t dev_bytes, size_t page_bytes,
       return cuda_error(e1 != cudaSuccess ? e1 : e2, "arena_create: cudaEventCreate");
     }
   }
+  {
+    cudaError_t e = cudaStreamCreateWithFlags(&a->aux, cudaStreamNonBlocking);
+    cudaEvent_t* evs[] = {&a->ev_fork, &a->ev_join, &a->ev_up[0], &a->ev_up[1], &a->ev_down[0],
+                          &a->ev_down[1]};
+    for (auto* ev : evs)
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      psi_arena_destroy(a);
+      return cuda_error(e, "arena_create: auxiliary stream or events");
+    }
+  }
   if (!dev_error_ptr()) {
     psi_arena_destroy(a);
     return set_error(PSI_ERR_CUDA, "arena_create: kernel error record not reachable");
@@ -261,6 +284,13 @@ psi_status psi_arena_destroy(psi_arena* a) {
   if (!a) return PSI_OK;
   cudaStreamSynchronize(a->compute);
   if (a->copy != a->compute) cudaStreamSynchronize(a->copy);
+  if (a->aux) {
+    cudaStreamSynchronize(a->aux);
+    cudaStreamDestroy(a->aux);
+  }
+  for (cudaEvent_t e : {a->ev_fork, a->ev_join, a->ev_up[0], a->ev_up[1], a->ev_down[0],
+                        a->ev_down[1]})
+    if (e) cudaEventDestroy(e);
   for (auto e : a->ready)
     if (e) cudaEventDestroy(e);
   for (auto e : a->consumed)
@@ -280,8 +310,12 @@ psi_status psi_arena_destroy(psi_arena* a) {
 
 int32_t psi_arena_slots(const psi_arena* a) { return a ? a->nslots : 0; }
 
-psi_status psi_page_stream(psi_arena* a, const void* host_src, size_t bytes, uint32_t flags,
-                           psi_page* out) {
+}  // extern "C"
+
+namespace {
+// Request the next slot for a consumer on stream `cs` (see psi_page_stream).
+psi_status page_stream_to(psi_arena* a, const void* host_src, size_t bytes, uint32_t flags,
+                          cudaStream_t cs, psi_page* out) {
   if (!a || !host_src || !out) return set_error(PSI_ERR_INVALID_ARG, "page_stream: null argument");
   if (bytes > a->page_bytes)
     return set_error(PSI_ERR_CAPACITY, "page_stream: slice larger than the page");
@@ -299,9 +333,13 @@ psi_status psi_page_stream(psi_arena* a, const void* host_src, size_t bytes, uin
   TimedLaunch t{};
   psi_status st;
   if (sync_copy) {
-    // the copy follows every earlier consumer on the compute stream
-    if (a->timing && (st = timed_begin(a, a->compute, &t)) != PSI_OK) return st;
-    e = cudaMemcpyAsync(dst, host_src, bytes, cudaMemcpyHostToDevice, a->compute);
+    // the copy runs on the consumer's stream, after the slot's last consumer
+    if (a->has_consumed[s]) {
+      e = cudaStreamWaitEvent(cs, a->consumed[s], 0);
+      if (e != cudaSuccess) return cuda_error(e, "page_stream: wait consumed");
+    }
+    if (a->timing && (st = timed_begin(a, cs, &t)) != PSI_OK) return st;
+    e = cudaMemcpyAsync(dst, host_src, bytes, cudaMemcpyHostToDevice, cs);
     if (e != cudaSuccess) return cuda_error(e, "page_stream: cudaMemcpyAsync");
   } else {
     if (a->has_consumed[s]) {
@@ -313,12 +351,12 @@ psi_status psi_page_stream(psi_arena* a, const void* host_src, size_t bytes, uin
     if (e != cudaSuccess) return cuda_error(e, "page_stream: cudaMemcpyAsync");
     e = cudaEventRecord(a->ready[s], a->copy);
     if (e != cudaSuccess) return cuda_error(e, "page_stream: record ready");
-    e = cudaStreamWaitEvent(a->compute, a->ready[s], 0);  // consumers wait for the copy
+    e = cudaStreamWaitEvent(cs, a->ready[s], 0);  // consumers wait for the copy
     if (e != cudaSuccess) return cuda_error(e, "page_stream: wait ready");
   }
   if (a->timing) {
     t.work = static_cast<double>(bytes);
-    if ((st = timed_end(a, sync_copy ? a->compute : a->copy, t, &a->copy_t)) != PSI_OK) return st;
+    if ((st = timed_end(a, sync_copy ? cs : a->copy, t, &a->copy_t)) != PSI_OK) return st;
   }
   a->state[s] = SLOT_REQUESTED;
   a->slot_seq[s] = ++a->seq;
@@ -332,16 +370,38 @@ psi_status psi_page_stream(psi_arena* a, const void* host_src, size_t bytes, uin
   return PSI_OK;
 }
 
-psi_status psi_page_release(psi_arena* a, psi_page p) {
+// End a request whose last consumer was enqueued on stream `cs`.
+psi_status page_release_on(psi_arena* a, psi_page p, cudaStream_t cs) {
   if (!a || p.slot < 0 || p.slot >= a->nslots)
     return set_error(PSI_ERR_INVALID_ARG, "page_release: bad page");
   if (a->state[p.slot] != SLOT_REQUESTED || a->slot_seq[p.slot] != p.seq)
     return set_error(PSI_ERR_INVALID_ARG, "page_release: stale or already released page");
-  cudaError_t e = cudaEventRecord(a->consumed[p.slot], a->compute);
+  cudaError_t e = cudaEventRecord(a->consumed[p.slot], cs);
   if (e != cudaSuccess) return cuda_error(e, "page_release: record consumed");
   a->has_consumed[p.slot] = 1;
   a->state[p.slot] = SLOT_FREE;
   return PSI_OK;
+}
+
+// aux (or compute) waits for everything enqueued so far on `from`.
+psi_status stream_after(cudaEvent_t ev, cudaStream_t from, cudaStream_t to) {
+  cudaError_t e = cudaEventRecord(ev, from);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(to, ev, 0);
+  return e == cudaSuccess ? PSI_OK : cuda_error(e, "fork/join event");
+}
+}  // namespace
+
+extern "C" {
+
+psi_status psi_page_stream(psi_arena* a, const void* host_src, size_t bytes, uint32_t flags,
+                           psi_page* out) {
+  if (!a) return set_error(PSI_ERR_INVALID_ARG, "page_stream: null arena");
+  return page_stream_to(a, host_src, bytes, flags, a->compute, out);
+}
+
+psi_status psi_page_release(psi_arena* a, psi_page p) {
+  if (!a) return set_error(PSI_ERR_INVALID_ARG, "page_release: null arena");
+  return page_release_on(a, p, a->compute);
 }
 
 psi_status psi_sync(psi_arena* a, int64_t timeout_ms) {
@@ -351,6 +411,7 @@ psi_status psi_sync(psi_arena* a, int64_t timeout_ms) {
   psi_status st = wait_stream(a->compute, dl, bounded);
   if (st != PSI_OK) return st;
   if (a->copy != a->compute && (st = wait_stream(a->copy, dl, bounded)) != PSI_OK) return st;
+  if ((st = wait_stream(a->aux, dl, bounded)) != PSI_OK) return st;
   return report_device_errors();
 }
 
@@ -442,7 +503,12 @@ psi_status psi_linear_paged(psi_arena* a, const void* X, int64_t N, int64_t K,
     return set_error(PSI_ERR_CAPACITY, "linear_paged: weight tile exceeds page");
   const int64_t npages = (W->rows + W->page_rows - 1) / W->page_rows;
   DevError* err = dev_error_ptr();
+  // pages alternate between the compute and the auxiliary stream (outputs are
+  // disjoint column blocks); aux first catches up with the compute stream
+  psi_status fst = stream_after(a->ev_fork, a->compute, a->aux);
+  if (fst != PSI_OK) return fst;
   for (int64_t p = 0; p < npages; ++p) {
+    cudaStream_t cs = (p & 1) ? a->aux : a->compute;
     const int64_t r0 = p * W->page_rows;
     const int64_t rows_p = std::min(W->page_rows, W->rows - r0);
     const size_t off = static_cast<size_t>(r0) * K * 2;
@@ -453,7 +519,7 @@ psi_status psi_linear_paged(psi_arena* a, const void* X, int64_t N, int64_t K,
       dev = src + off;
       a->stats.resident_pages++;
     } else {
-      psi_status st = psi_page_stream(a, src + off, nbytes, flags, &pg);
+      psi_status st = page_stream_to(a, src + off, nbytes, flags, cs, &pg);
       if (st != PSI_OK) return st;
       dev = pg.dev;
     }
@@ -468,11 +534,11 @@ psi_status psi_linear_paged(psi_arena* a, const void* X, int64_t N, int64_t K,
     g.ldo = ldy;
     g.err = err;
     g.timeout_ns = kWaitLimitNs;
-    psi_status st = arena_gemm(a, X, K, dev, K, g);
+    psi_status st = arena_gemm(a, cs, X, K, dev, K, g);
     if (st != PSI_OK) return st;
-    if (!resident && (st = psi_page_release(a, pg)) != PSI_OK) return st;
+    if (!resident && (st = page_release_on(a, pg, cs)) != PSI_OK) return st;
   }
-  return PSI_OK;
+  return stream_after(a->ev_join, a->aux, a->compute);
 }
 
 psi_status psi_ffn_paged(psi_arena* a, const void* X, int64_t N, const psi_ffn_weight* W,
@@ -499,60 +565,90 @@ psi_status psi_ffn_paged(psi_arena* a, const void* X, int64_t N, const psi_ffn_w
   if (!resident && pb > a->page_bytes)
     return set_error(PSI_ERR_CAPACITY, "ffn_paged: FFN weight tile exceeds page");
   const int64_t S = h / sl;
+  const int64_t G = ffn_group(S, sl);
+  if (!resident && G > a->nslots)
+    return set_error(PSI_ERR_CAPACITY, "ffn_paged: a slice group needs " + std::to_string(G) +
+                                           " page slots, the arena has " +
+                                           std::to_string(a->nslots));
   DevError* err = dev_error_ptr();
   const uint16_t* a16 = static_cast<const uint16_t*>(av);
   uint16_t* hid = static_cast<uint16_t*>(hidden_ws);
-  for (int64_t J = 0; J < S; ++J) {
-    psi_page pg{};
-    const char* dev;
-    if (resident) {
-      dev = src + static_cast<size_t>(J) * pb;
-      a->stats.resident_pages++;
-    } else {
-      psi_status st = psi_page_stream(a, src + static_cast<size_t>(J) * pb, pb, flags, &pg);
-      if (st != PSI_OK) return st;
-      dev = static_cast<const char*>(pg.dev);
+  // up projections run on the auxiliary stream, one group ahead of the down
+  // projections on the compute stream; hidden buffer g&1 is rewritten only
+  // after the down projection of group g-2 has read it
+  psi_status fst = stream_after(a->ev_fork, a->compute, a->aux);
+  if (fst != PSI_OK) return fst;
+  for (int64_t J0 = 0, g = 0; J0 < S; J0 += G, ++g) {
+    const int64_t gs = std::min(G, S - J0);
+    uint16_t* Hg = hid + static_cast<size_t>(g & 1) * N * G * sl;
+    if (g >= 2) {
+      cudaError_t e = cudaStreamWaitEvent(a->aux, a->ev_down[g & 1], 0);
+      if (e != cudaSuccess) return cuda_error(e, "ffn_paged: wait down projection");
     }
-    const void* UJ = dev;
-    const void* VJ = dev + static_cast<size_t>(sl) * d * 2;
-    uint16_t* HJ = hid + static_cast<size_t>(J & 1) * N * sl;
-    // up projection slice: H_J = B(phi(X U_J^T + a_J))
-    GemmArgs up{};
-    up.M = static_cast<int32_t>(N);
-    up.N = static_cast<int32_t>(sl);
-    up.K = static_cast<int32_t>(d);
-    up.epi = EPI_GELU;
-    up.pregelu = (flags & PSI_BOUNDARY_PREGELU_BF16) ? 1 : 0;
-    up.bias = a16 + J * sl;
-    up.out = HJ;
-    up.ldo = sl;
-    up.err = err;
-    up.timeout_ns = kWaitLimitNs;
-    psi_status st = arena_gemm(a, X, d, UJ, d, up);
-    if (st != PSI_OK) return st;
-    // down projection slice, ordered FP32 accumulation; bias once at the end
+    psi_page pg[kFfnGroupMax]{};
+    const char* dev[kFfnGroupMax];
+    for (int64_t u = 0; u < gs; ++u) {
+      const int64_t J = J0 + u;
+      if (resident) {
+        dev[u] = src + static_cast<size_t>(J) * pb;
+        a->stats.resident_pages++;
+      } else {
+        psi_status st =
+            page_stream_to(a, src + static_cast<size_t>(J) * pb, pb, flags, a->aux, &pg[u]);
+        if (st != PSI_OK) return st;
+        dev[u] = static_cast<const char*>(pg[u].dev);
+      }
+      // up projection slice: H_J = B(phi(X U_J^T + a_J)), columns u*sl of the group
+      GemmArgs up{};
+      up.M = static_cast<int32_t>(N);
+      up.N = static_cast<int32_t>(sl);
+      up.K = static_cast<int32_t>(d);
+      up.epi = EPI_GELU;
+      up.pregelu = (flags & PSI_BOUNDARY_PREGELU_BF16) ? 1 : 0;
+      up.bias = a16 + J * sl;
+      up.out = Hg + u * sl;
+      up.ldo = G * sl;
+      up.err = err;
+      up.timeout_ns = kWaitLimitNs;
+      psi_status st = arena_gemm(a, a->aux, X, d, dev[u], d, up);
+      if (st != PSI_OK) return st;
+    }
+    {
+      psi_status st = stream_after(a->ev_up[g & 1], a->aux, a->compute);
+      if (st != PSI_OK) return st;
+    }
+    // down projection of the group: Acc (+)= [H_J0 .. H_J0+gs-1] [V_:,J0 .. ]^T,
+    // ordered FP32 accumulation over groups; output bias once, at the end
     GemmArgs dn{};
     dn.M = static_cast<int32_t>(N);
     dn.N = static_cast<int32_t>(r);
-    dn.K = static_cast<int32_t>(sl);
+    dn.K = static_cast<int32_t>(gs * sl);
+    dn.k_split = gs > 1 ? static_cast<int32_t>(sl / 64) : 0;
     dn.accf = static_cast<float*>(acc_ws);
     dn.ldacc = r;
     dn.err = err;
     dn.timeout_ns = kWaitLimitNs;
-    if (J == S - 1) {
-      dn.epi = S == 1 ? EPI_LINEAR : EPI_ACC_FINAL;
+    const bool first = J0 == 0, last = J0 + gs >= S;
+    if (last) {
+      dn.epi = first ? EPI_LINEAR : EPI_ACC_FINAL;
       dn.bias = static_cast<const uint16_t*>(bv);
       dn.resid = static_cast<const uint16_t*>(residual);
       dn.out = static_cast<uint16_t*>(Y);
       dn.ldo = r;
     } else {
-      dn.epi = J == 0 ? EPI_ACC_STORE : EPI_ACC_ADD;
+      dn.epi = first ? EPI_ACC_STORE : EPI_ACC_ADD;
     }
-    st = arena_gemm(a, HJ, sl, VJ, sl, dn);
+    const size_t voff = static_cast<size_t>(sl) * d * 2;
+    psi_status st = arena_gemm(a, a->compute, Hg, G * sl, dev[0] + voff, sl, dn,
+                               gs > 1 ? dev[1] + voff : nullptr);
     if (st != PSI_OK) return st;
-    if (!resident && (st = psi_page_release(a, pg)) != PSI_OK) return st;
+    cudaError_t e = cudaEventRecord(a->ev_down[g & 1], a->compute);
+    if (e != cudaSuccess) return cuda_error(e, "ffn_paged: record down projection");
+    if (!resident)
+      for (int64_t u = 0; u < gs; ++u)
+        if ((st = page_release_on(a, pg[u], a->compute)) != PSI_OK) return st;
   }
-  return PSI_OK;
+  return stream_after(a->ev_join, a->aux, a->compute);
 }
 
 psi_status psi_attn_partitioned(const psi_heads* Q, const psi_heads* K, const psi_heads* V,
