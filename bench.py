@@ -203,13 +203,29 @@ class BlockWorkload(Workload):
     def stream(self):
         return self.arena.compute
 
-    def step(self, X=None, Y=None):
+    def step(self, X=None, Y=None, marks=None):
         X = self.X if X is None else X
         Y = self.Y if Y is None else Y
         if len(self.blocks) == 1:
-            self.runner.forward(X, self.blocks[0], Y, self.flags)
+            self.runner.forward(X, self.blocks[0], Y, self.flags, marks)
         else:
             self.runner.stack(X, self.blocks, Y, self.tmp, self.flags)
+
+    def phase_split(self, steps=5):
+        """Per-operator time of a single block on the compute stream (ms):
+        QKV projection, attention, out-projection, FFN."""
+        torch = self.torch
+        if len(self.blocks) != 1:
+            return None
+        tot = [0.0] * 4
+        for _ in range(steps):
+            marks = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+            with torch.cuda.stream(self.stream):
+                self.step(marks=marks)
+            marks[4].synchronize()
+            for i in range(4):
+                tot[i] += marks[i].elapsed_time(marks[i + 1])
+        return {k: v / steps for k, v in zip(["qkv", "attention", "out_proj", "ffn"], tot)}
 
     def io(self):
         return self.X, self.Y
@@ -538,6 +554,8 @@ def main():
     ms_per_step = total_ms / args.steps
     value = wl.flops * world / (ms_per_step * 1e-3) / 1e12
 
+    phases = wl.phase_split() if hasattr(wl, "phase_split") else None
+
     # ------------------------------------------------------------ e2e ---
     Xd, Yd = wl.io()
     Xh = torch.empty(Xd.shape, dtype=Xd.dtype, pin_memory=True)
@@ -621,6 +639,7 @@ def main():
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "flops_per_step": wl.flops, "wall_s_timed": t_wall,
                        "step_roofline_ms": step_bound_ms,
+                       "phase_ms": phases,
                        "frac_of_step_roofline": step_bound_ms / ms_per_step},
             "roofline": roof, "ingest": ingest, "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step":

@@ -77,24 +77,38 @@ class BlockRunner:
     def _heads(self, t: torch.Tensor, col0: int, ld: int) -> psi.psi_heads:
         return psi.psi_heads(t.data_ptr() + 2 * col0, ld, self.s.dh)
 
-    def forward(self, X: torch.Tensor, W: BlockWeights, Y: torch.Tensor, flags: int = 0):
-        """Y = block(X); X and Y are [N x d] device BF16 (Y may not alias X)."""
+    def forward(self, X: torch.Tensor, W: BlockWeights, Y: torch.Tensor, flags: int = 0,
+                marks=None):
+        """Y = block(X); X and Y are [N x d] device BF16 (Y may not alias X).
+        ``marks``: optional list of 5 CUDA events recorded on the compute
+        stream at the operator boundaries (timing only)."""
         s, A = self.s, self.arena.handle
         H, dh, N = s.heads, s.dh, s.N
+        cs = self.arena.compute
+
+        def mark(i):
+            if marks is not None:
+                marks[i].record(cs)
+
+        mark(0)
         psi.psi_linear_paged(A, X.data_ptr(), N, s.d, W.qkv.desc(), W.bqkv.data_ptr(), None,
                              self.h.data_ptr(), s.qkv, flags)
+        mark(1)
         q = self._heads(self.h, 0, s.qkv)
         k = self._heads(self.h, H * dh, s.qkv)
         v = self._heads(self.h, 2 * H * dh, s.qkv)
         o = self._heads(self.att, 0, H * dh)
         psi.psi_attn_partitioned(q, k, v, o, H, N, N, dh, 1.0 / math.sqrt(dh), s.key_block,
-                                 self.arena.compute.cuda_stream, 0)
+                                 cs.cuda_stream, 0)
         self.attn_launches += 1
+        mark(2)
         psi.psi_linear_paged(A, self.att.data_ptr(), N, H * dh, W.out.desc(), W.bo.data_ptr(),
                              X.data_ptr(), self.x1.data_ptr(), s.d, flags)
+        mark(3)
         psi.psi_ffn_paged(A, self.x1.data_ptr(), N, W.ffn.desc(), W.a1.data_ptr(),
                           W.b1.data_ptr(), self.hid.data_ptr(), self.acc.data_ptr(),
                           self.x1.data_ptr(), Y.data_ptr(), flags)
+        mark(4)
 
     def stack(self, X: torch.Tensor, blocks: list, Y: torch.Tensor, tmp: torch.Tensor,
               flags: int = 0):
