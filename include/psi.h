@@ -255,6 +255,33 @@ psi_status psi_attn_partitioned(const psi_heads* Q, const psi_heads* K,
                                 float scale, int32_t key_block, void* stream,
                                 uint32_t flags);
 
+/* ------------------------------------------------- no-allocation FFN --- */
+/* The paper has no counterpart of this entry point; it serves callers that
+ * cannot allocate device memory (code running inside another framework's
+ * memory pool or a fixed budget handed out at start-up, plug-ins given
+ * device pointers but no allocator).  It computes exactly what
+ * psi_ffn_paged computes with PSI_RESIDENT (same kernels, same slice
+ * grouping, so the same bytes), on `stream` (cudaStream_t), with weights
+ * read in place from W->dev_resident (the packed page image, W->host is not
+ * used) and no arena.
+ *   X [N x d], residual (or NULL) and Y [N x r] (row stride r), a [h],
+ *   b [r]: device BF16, 16-byte aligned; flags: PSI_BOUNDARY_PREGELU_BF16.
+ * Workspace: the hidden slices of one group (N*2*slice*2 bytes, rounded up
+ * to 256) and the FP32 accumulator (N*r*4 bytes) live in one fixed 16 MiB
+ * device array inside the library, held on every GPU that loads it until
+ * the process exits.  Larger problems fail with PSI_ERR_CAPACITY before
+ * anything is enqueued.  The call makes no cudaMalloc or cudaFree and
+ * calls no allocating library routine.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * Every call shares the array: calls whose work overlaps on the GPU (other
+ * streams, other host threads) race on it and must be serialised by the
+ * caller.  The accumulator is written before it is read, so no clearing
+ * is needed between calls. */
+psi_status psi_ffn_resident_noalloc(const void* X, int64_t N, const psi_ffn_weight* W,
+                                    const void* a, const void* b, const void* residual,
+                                    void* Y, void* stream, uint32_t flags);
+
 #ifdef __cplusplus
 }
 #endif

@@ -37,6 +37,7 @@ EXPORTS = [
     "psi_arena_stats", "psi_arena_reset_stats", "psi_arena_set_timing",
     "psi_arena_fail_next_copy", "psi_debug_stall_next_gemm",
     "psi_linear_paged", "psi_ffn_paged", "psi_attn_partitioned",
+    "psi_ffn_resident_noalloc",
 ]
 
 
@@ -123,6 +124,8 @@ def load(path: str = LIB_PATH) -> C.CDLL:
                                vp, u32]),
         "psi_attn_partitioned": (st, [C.POINTER(psi_heads)] * 4 +
                                  [i32, i64, i64, i32, C.c_float, i32, vp, u32]),
+        "psi_ffn_resident_noalloc": (st, [vp, i64, C.POINTER(psi_ffn_weight), vp, vp, vp, vp,
+                                          vp, u32]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -243,3 +246,11 @@ def psi_attn_partitioned(Q: psi_heads, K: psi_heads, V: psi_heads, O: psi_heads,
                          flags: int = 0):
     _check(load().psi_attn_partitioned(C.byref(Q), C.byref(K), C.byref(V), C.byref(O), heads,
                                        Nq, Nk, dh, scale, key_block, stream, flags))
+
+
+def psi_ffn_resident_noalloc(X: int, N: int, W: psi_ffn_weight, a: int, b: int,
+                             residual: int | None, Y: int, stream: int, flags: int = 0):
+    """FFN with resident weights and the library's fixed workspace (for
+    callers that cannot allocate device memory); see include/psi.h."""
+    _check(load().psi_ffn_resident_noalloc(X, N, C.byref(W), a, b, residual or None, Y,
+                                           stream, flags))
