@@ -116,6 +116,10 @@ typedef struct {
   uint64_t timed_copies;     /* H2D copies bracketed by events */
   double copy_ms;            /* their summed device time */
   double copy_bytes;
+  double gemm_busy_ms;       /* length of the union of the timed page-GEMM
+                                intervals (launches on the two streams may
+                                overlap, so this can be below gemm_ms) */
+  double copy_busy_ms;       /* the same for the timed copies */
 } psi_stats;
 
 /* ---------------------------------------------------------------- misc -- */

@@ -1,0 +1,50 @@
+"""The N > 1 host path of bench.py on CPU: two gloo ranks run independent
+replicas (no data-path collective) and the job time is the maximum over
+ranks; the job value counts every rank's work."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+def _worker(rank, world, port, out):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    # rank r took 10 * (r + 1) ms for 5 steps of 2 TFLOP each
+    total, per_step, value = bench.aggregate_ranks(dist, torch.device("cpu"),
+                                                   10.0 * (rank + 1), 2e12, 5, world)
+    out[rank] = (total, per_step, value)
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_two_ranks_max_time_and_weak_scaling_value():
+    port = _free_port()
+    mgr = mp.Manager()
+    out = mgr.dict()
+    mp.spawn(_worker, args=(2, port, out), nprocs=2, join=True)
+    for r in range(2):
+        total, per_step, value = out[r]
+        assert total == 20.0                 # the slower rank's time
+        assert per_step == 4.0
+        assert value == pytest.approx(2 * 2e12 / 4e-3 / 1e12)   # both ranks' work
+
+
+def test_single_rank_needs_no_process_group():
+    import bench
+    total, per_step, value = bench.aggregate_ranks(None, torch.device("cpu"), 8.0, 1e12, 4, 1)
+    assert (total, per_step) == (8.0, 2.0)
+    assert value == pytest.approx(1e12 / 2e-3 / 1e12)

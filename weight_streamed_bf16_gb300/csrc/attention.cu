@@ -20,8 +20,9 @@
 //               max m and sum l in FP32, weights p = 2^(s - m) in FP32 split
 //               into p_hi = B(p) and p_lo = B(p - p_hi) (the tensor-core
 //               operand then carries p to within 2^-17 relative) and written
-//               over the row's S columns; O rescaled by eta in tensor memory
-//               when the max moves; O / l written as BF16 at the end.
+//               over the row's S columns (two passes over tensor memory:
+//               row extremum, then exponentials); O rescaled by eta in
+//               tensor memory when the max moves; O / l written as BF16.
 // While one softmax warpgroup works on its tile, the tensor core runs the
 // other tile's MMAs.
 #include "internal.h"
@@ -43,9 +44,9 @@ constexpr int OFF_V = OFF_K + 2 * 2 * TILE64;
 constexpr int OFF_BAR = OFF_V + 2 * 2 * TILE64;       // 192 KiB
 constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
 
-// tensor memory: tile t uses columns [256 t, 256 t + 128) for S (and P over
-// it: P_hi in the first 64 columns, P_lo in the next 64) and [256 t + 128,
-// 256 t + 256) for O
+// tensor memory: tile t uses columns [256 t, 256 t + 128) for S and P over
+// it (for keys 32c..32c+31: p_hi pairs in columns 32c..32c+15, p_lo pairs in
+// 32c+16..32c+31) and [256 t + 128, 256 t + 256) for O
 constexpr uint32_t TM_COLS = 512;
 __device__ __forceinline__ uint32_t tm_s(int t) { return 256u * t; }
 __device__ __forceinline__ uint32_t tm_o(int t) { return 256u * t + 128u; }
@@ -217,13 +218,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          // O_t += P_hi V_j + P_lo V_j: P from tensor memory (8 columns per
-          // 16 keys), V rows kk*16.. of both 64-wide dh blocks (LBO apart)
+          // O_t += P_hi V_j + P_lo V_j: P from tensor memory, keys 16kk..16kk+15
+          // at columns 32(kk/2) + 8(kk%2) (hi) and 16 further (lo); V rows
+          // 16kk.. of both 64-wide dh blocks (LBO apart)
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
 #pragma unroll
             for (int kk = 0; kk < BKEY / 16; ++kk) {
-              mma_bf16_ts(tmem + tm_o(t), tmem + tm_s(t) + half * 64 + kk * 8,
+              const uint32_t pcol = 32 * (kk >> 1) + 8 * (kk & 1) + 16 * half;
+              mma_bf16_ts(tmem + tm_o(t), tmem + tm_s(t) + pcol,
                           sdesc_sw128(sV + kk * 2048, TILE64, 1024), idesc_o,
                           (j | half | kk) != 0 ? 1u : 0u);
             }
@@ -262,49 +265,60 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      float s[BKEY];
-#pragma unroll
-      for (int c = 0; c < BKEY / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(tS + c * 32, r);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[i]);
-      }
+      // pass 1: row extremum of the raw scores (max, or min for a negative
+      // scale); scores are scaled inside the exponent below
+      const float c = args.scale_log2;  // scale * log2(e)
       const int kvalid = args.Nk - j * BKEY;  // keys of this tile that exist
-      float mx = -INFINITY;
+      float ext = c >= 0.f ? -INFINITY : INFINITY;
 #pragma unroll
-      for (int i = 0; i < BKEY; ++i) {
-        const float x = i < kvalid ? s[i] * args.scale_log2 : -INFINITY;
-        s[i] = x;
-        mx = fmaxf(mx, x);
+      for (int cc = 0; cc < BKEY / 32; ++cc) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tS + cc * 32, r);
+        tmem_wait_ld();
+        if (kvalid >= BKEY) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            ext = c >= 0.f ? fmaxf(ext, __uint_as_float(r[i])) : fminf(ext, __uint_as_float(r[i]));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (cc * 32 + i < kvalid)
+              ext = c >= 0.f ? fmaxf(ext, __uint_as_float(r[i]))
+                             : fminf(ext, __uint_as_float(r[i]));
+        }
       }
-      const float m_new = fmaxf(m2, mx);
-      const float eta = exp2f(m2 - m_new);  // 0 on the first tile
+      const float m_new = fmaxf(m2, ext * c);
+      const float eta = ex2_approx(m2 - m_new);  // 0 on the first tile
+      // pass 2: p = 2^(s*c - m) with one FFMA; the chunk of 32 keys is
+      // written back over its own 32 columns as 16 columns of p_hi pairs and
+      // 16 of p_lo pairs (keys 2i, 2i+1 share a column)
       float rs = 0.f;
 #pragma unroll
-      for (int i = 0; i < BKEY; ++i) {
-        const float p = exp2f(s[i] - m_new);
-        s[i] = p;
-        rs += p;
-      }
-      l = eta * l + rs;
-      m2 = m_new;
-      // P over the S columns (all of S is in registers): 64 columns of p_hi
-      // pairs, then 64 of p_lo pairs; keys 2i and 2i+1 share column i
+      for (int cc = 0; cc < BKEY / 32; ++cc) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tS + cc * 32, r);
+        tmem_wait_ld();
+        float p[32];
+        if (kvalid >= BKEY) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+          for (int i = 0; i < 32; ++i) p[i] = ex2_approx(fmaf(__uint_as_float(r[i]), c, -m_new));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            p[i] = cc * 32 + i < kvalid ? ex2_approx(fmaf(__uint_as_float(r[i]), c, -m_new)) : 0.f;
+        }
         uint32_t hi[16], lo[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float p0 = s[c * 32 + 2 * i];
-          const float p1 = s[c * 32 + 2 * i + 1];
-          hi[i] = pack_bf16x2(p0, p1);
-          lo[i] = pack_bf16x2(p0 - bf16_lo(hi[i]), p1 - bf16_hi(hi[i]));
+          rs += p[2 * i] + p[2 * i + 1];
+          hi[i] = pack_bf16x2(p[2 * i], p[2 * i + 1]);
+          lo[i] = pack_bf16x2(p[2 * i] - bf16_lo(hi[i]), p[2 * i + 1] - bf16_hi(hi[i]));
         }
-        tmem_st_32x32b_x16(tS + c * 16, hi);
-        tmem_st_32x32b_x16(tS + 64 + c * 16, lo);
+        tmem_st_32x32b_x16(tS + cc * 32, hi);
+        tmem_st_32x32b_x16(tS + cc * 32 + 16, lo);
       }
+      l = eta * l + rs;
+      m2 = m_new;
       if (j > 0) {
         // the previous PV of this tile has finished: O is stable
         if (!mbar_wait(&bars->pv_done[t], (j - 1) & 1, abort_flag, args.timeout_ns)) {

@@ -55,7 +55,8 @@ struct GemmArgs {
                         // consumers' bounded waits expire (see timeout_ns)
   int32_t k_split;      // k-blocks (of 64) read from the first page; the rest
                         // come from the second page (0: one page)
-  int32_t pad_;
+  int32_t n_split;      // output columns served by the first page; columns from
+                        // n_split on come from the second page (0: one page)
   const uint16_t* bias;   // [N]
   const uint16_t* resid;  // [M x ldo] or null
   uint16_t* out;          // [M x ldo]
@@ -69,7 +70,9 @@ struct GemmArgs {
 // D[M x N] = X[M x K] * P[N x K]^T with the chosen epilogue, on `stream`.
 // X and P are BF16 row-major with row strides ldx and ldp (elements).  With
 // args.k_split > 0 the K range is split over two pages: columns
-// [0, 64*k_split) of P come from P, the rest from P2 (same row stride).
+// [0, 64*k_split) of P come from P, the rest from P2 (same row stride); with
+// args.n_split > 0 the output columns are: rows [0, n_split) of P, then the
+// rows of P2 (n_split a multiple of the tile width).
 psi_status launch_page_gemm(const void* X, int64_t ldx, const void* P, int64_t ldp,
                             const GemmArgs& args, cudaStream_t stream,
                             const void* P2 = nullptr);

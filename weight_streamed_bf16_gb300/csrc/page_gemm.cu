@@ -226,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
     tma_prefetch_desc(&tmX);
     tma_prefetch_desc(&tmP);
-    if (args.k_split) tma_prefetch_desc(&tmP2);
+    if (args.k_split || args.n_split) tma_prefetch_desc(&tmP2);
   }
   if (warp == 1) {
     tmem_alloc(&bars->tmem_base, C::TMEM_COLS);
@@ -257,7 +257,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mbar_arrive_expect_tx(&bars->full[stage], C::STAGE_BYTES);
           tma_load_2d(sA + stage * C::A_BYTES, &tmX, &bars->full[stage], kb * BK, m0);
-          if (args.k_split == 0 || kb < args.k_split)
+          if (args.n_split > 0 && n0 >= args.n_split)
+            tma_load_2d(sB + stage * C::B_BYTES, &tmP2, &bars->full[stage], kb * BK,
+                        n0 - args.n_split);
+          else if (args.k_split == 0 || kb < args.k_split)
             tma_load_2d(sB + stage * C::B_BYTES, &tmP, &bars->full[stage], kb * BK, n0);
           else
             tma_load_2d(sB + stage * C::B_BYTES, &tmP2, &bars->full[stage],
@@ -428,12 +431,20 @@ psi_status launch_page_gemm(const void* X, int64_t ldx, const void* P, int64_t l
   CUtensorMap tx, tp, tp2;
   psi_status st = make_tmap_2d(&tx, X, a.M, a.K, ldx, BM, BK);
   if (st != PSI_OK) return st;
+  if (a.k_split > 0 && a.n_split > 0)
+    return set_error(PSI_ERR_INVALID_ARG, "page_gemm: K and N split together");
   if (a.k_split > 0) {
     const int64_t k1 = static_cast<int64_t>(a.k_split) * BK;
     if (!P2 || k1 >= a.K) return set_error(PSI_ERR_INVALID_ARG, "page_gemm: bad K split");
     st = make_tmap_2d(&tp, P, a.N, k1, ldp, bn, BK);
     if (st != PSI_OK) return st;
     st = make_tmap_2d(&tp2, P2, a.N, a.K - k1, ldp, bn, BK);
+  } else if (a.n_split > 0) {
+    if (!P2 || a.n_split >= a.N || a.n_split % bn)
+      return set_error(PSI_ERR_INVALID_ARG, "page_gemm: bad N split");
+    st = make_tmap_2d(&tp, P, a.n_split, a.K, ldp, bn, BK);
+    if (st != PSI_OK) return st;
+    st = make_tmap_2d(&tp2, P2, a.N - a.n_split, a.K, ldp, bn, BK);
   } else {
     st = make_tmap_2d(&tp, P, a.N, a.K, ldp, bn, BK);
     tp2 = tp;

@@ -426,25 +426,46 @@ psi_status psi_stream_wait(void* stream, int64_t timeout_ms) {
 psi_status psi_arena_stats(const psi_arena* ca, psi_stats* out) {
   if (!ca || !out) return set_error(PSI_ERR_INVALID_ARG, "arena_stats: null argument");
   psi_arena* a = const_cast<psi_arena*>(ca);
-  auto fold = [&](std::vector<TimedLaunch>& v, uint64_t* n, double* ms, double* work) -> psi_status {
+  // sums of the launch durations, and the union of the launch intervals
+  // (timestamps relative to the first event of the batch)
+  auto fold = [&](std::vector<TimedLaunch>& v, uint64_t* n, double* ms, double* work,
+                  double* busy) -> psi_status {
+    std::vector<std::pair<double, double>> iv;
     for (auto& t : v) {
       cudaError_t e = cudaEventSynchronize(t.stop);
       if (e != cudaSuccess) return cuda_error(e, "arena_stats: event");
-      float f = 0.f;
+      float f = 0.f, t0 = 0.f;
       e = cudaEventElapsedTime(&f, t.start, t.stop);
+      if (e == cudaSuccess) e = cudaEventElapsedTime(&t0, v.front().start, t.start);
       if (e != cudaSuccess) return cuda_error(e, "arena_stats: elapsed");
       *n += 1;
       *ms += f;
       *work += t.work;
+      iv.emplace_back(t0, t0 + f);
+    }
+    std::sort(iv.begin(), iv.end());
+    double end = -1e300;
+    for (auto& x : iv) {
+      if (x.first >= end) {
+        *busy += x.second - x.first;
+        end = x.second;
+      } else if (x.second > end) {
+        *busy += x.second - end;
+        end = x.second;
+      }
+    }
+    for (auto& t : v) {
       a->pool.push_back(t.start);
       a->pool.push_back(t.stop);
     }
     v.clear();
     return PSI_OK;
   };
-  psi_status st = fold(a->gemm_t, &a->stats.timed_gemms, &a->stats.gemm_ms, &a->stats.gemm_flops);
+  psi_status st = fold(a->gemm_t, &a->stats.timed_gemms, &a->stats.gemm_ms,
+                       &a->stats.gemm_flops, &a->stats.gemm_busy_ms);
   if (st != PSI_OK) return st;
-  st = fold(a->copy_t, &a->stats.timed_copies, &a->stats.copy_ms, &a->stats.copy_bytes);
+  st = fold(a->copy_t, &a->stats.timed_copies, &a->stats.copy_ms, &a->stats.copy_bytes,
+            &a->stats.copy_busy_ms);
   if (st != PSI_OK) return st;
   *out = a->stats;
   return PSI_OK;
@@ -598,11 +619,17 @@ psi_status psi_ffn_paged(psi_arena* a, const void* X, int64_t N, const psi_ffn_w
         if (st != PSI_OK) return st;
         dev[u] = static_cast<const char*>(pg[u].dev);
       }
-      // up projection slice: H_J = B(phi(X U_J^T + a_J)), columns u*sl of the group
+    }
+    // up projection of the group: H_J = B(phi(X U_J^T + a_J)) for each slice J,
+    // one launch over both pages when the slice is a whole number of tiles
+    const bool merged = gs > 1 && sl % 256 == 0;
+    for (int64_t u = 0; u < gs; u += merged ? gs : 1) {
+      const int64_t J = J0 + u;
       GemmArgs up{};
       up.M = static_cast<int32_t>(N);
-      up.N = static_cast<int32_t>(sl);
+      up.N = static_cast<int32_t>(merged ? gs * sl : sl);
       up.K = static_cast<int32_t>(d);
+      up.n_split = merged ? static_cast<int32_t>(sl) : 0;
       up.epi = EPI_GELU;
       up.pregelu = (flags & PSI_BOUNDARY_PREGELU_BF16) ? 1 : 0;
       up.bias = a16 + J * sl;
@@ -610,7 +637,7 @@ psi_status psi_ffn_paged(psi_arena* a, const void* X, int64_t N, const psi_ffn_w
       up.ldo = G * sl;
       up.err = err;
       up.timeout_ns = kWaitLimitNs;
-      psi_status st = arena_gemm(a, a->aux, X, d, dev[u], d, up);
+      psi_status st = arena_gemm(a, a->aux, X, d, dev[u], d, up, merged ? dev[u + 1] : nullptr);
       if (st != PSI_OK) return st;
     }
     {

@@ -71,7 +71,8 @@ class psi_stats(C.Structure):
                 ("resident_pages", C.c_uint64), ("kernels_launched", C.c_uint64),
                 ("timed_gemms", C.c_uint64), ("gemm_ms", C.c_double),
                 ("gemm_flops", C.c_double), ("timed_copies", C.c_uint64),
-                ("copy_ms", C.c_double), ("copy_bytes", C.c_double)]
+                ("copy_ms", C.c_double), ("copy_bytes", C.c_double),
+                ("gemm_busy_ms", C.c_double), ("copy_busy_ms", C.c_double)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}
