@@ -266,38 +266,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       // pass 1: row extremum of the raw scores (max, or min for a negative
-      // scale); scores are scaled inside the exponent below
+      // scale); all four chunks are loaded before one wait
       const float c = args.scale_log2;  // scale * log2(e)
       const int kvalid = args.Nk - j * BKEY;  // keys of this tile that exist
       float ext = c >= 0.f ? -INFINITY : INFINITY;
-#pragma unroll
-      for (int cc = 0; cc < BKEY / 32; ++cc) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(tS + cc * 32, r);
+      {
+        uint32_t ra[32], rb[32], rc[32], rd[32];
+        tmem_ld_32x32b_x32(tS + 0, ra);
+        tmem_ld_32x32b_x32(tS + 32, rb);
+        tmem_ld_32x32b_x32(tS + 64, rc);
+        tmem_ld_32x32b_x32(tS + 96, rd);
         tmem_wait_ld();
-        if (kvalid >= BKEY) {
+        auto scan = [&](const uint32_t (&r)[32], int base) {
+          if (kvalid >= BKEY) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            ext = c >= 0.f ? fmaxf(ext, __uint_as_float(r[i])) : fminf(ext, __uint_as_float(r[i]));
-        } else {
+            for (int i = 0; i < 32; ++i)
+              ext = c >= 0.f ? fmaxf(ext, __uint_as_float(r[i])) : fminf(ext, __uint_as_float(r[i]));
+          } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (cc * 32 + i < kvalid)
-              ext = c >= 0.f ? fmaxf(ext, __uint_as_float(r[i]))
-                             : fminf(ext, __uint_as_float(r[i]));
-        }
+            for (int i = 0; i < 32; ++i)
+              if (base + i < kvalid)
+                ext = c >= 0.f ? fmaxf(ext, __uint_as_float(r[i]))
+                               : fminf(ext, __uint_as_float(r[i]));
+          }
+        };
+        scan(ra, 0);
+        scan(rb, 32);
+        scan(rc, 64);
+        scan(rd, 96);
       }
       const float m_new = fmaxf(m2, ext * c);
       const float eta = ex2_approx(m2 - m_new);  // 0 on the first tile
       // pass 2: p = 2^(s*c - m) with one FFMA; the chunk of 32 keys is
       // written back over its own 32 columns as 16 columns of p_hi pairs and
-      // 16 of p_lo pairs (keys 2i, 2i+1 share a column)
+      // 16 of p_lo pairs (keys 2i, 2i+1 share a column).  The next chunk's
+      // load is in flight while this chunk is processed.
       float rs = 0.f;
-#pragma unroll
-      for (int cc = 0; cc < BKEY / 32; ++cc) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(tS + cc * 32, r);
-        tmem_wait_ld();
+      auto expo = [&](const uint32_t (&r)[32], int cc) {
         float p[32];
         if (kvalid >= BKEY) {
 #pragma unroll
@@ -316,6 +321,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_st_32x32b_x16(tS + cc * 32, hi);
         tmem_st_32x32b_x16(tS + cc * 32 + 16, lo);
+      };
+      {
+        uint32_t r0[32], r1[32];
+        tmem_ld_32x32b_x32(tS + 0, r0);
+        tmem_wait_ld();
+        tmem_ld_32x32b_x32(tS + 32, r1);
+        expo(r0, 0);
+        tmem_wait_ld();
+        tmem_ld_32x32b_x32(tS + 64, r0);
+        expo(r1, 1);
+        tmem_wait_ld();
+        tmem_ld_32x32b_x32(tS + 96, r1);
+        expo(r0, 2);
+        tmem_wait_ld();
+        expo(r1, 3);
       }
       l = eta * l + rs;
       m2 = m_new;
@@ -330,13 +350,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         if (__any_sync(0xffffffffu, eta != 1.0f)) {
 #pragma unroll 1
-          for (int c = 0; c < DH / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(tO + c * 32, r);
+          for (int cc = 0; cc < DH / 32; cc += 2) {
+            uint32_t ra[32], rb[32];
+            tmem_ld_32x32b_x32(tO + cc * 32, ra);
+            tmem_ld_32x32b_x32(tO + cc * 32 + 32, rb);
             tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * eta);
-            tmem_st_32x32b_x32(tO + c * 32, r);
+            for (int i = 0; i < 32; ++i) {
+              ra[i] = __float_as_uint(__uint_as_float(ra[i]) * eta);
+              rb[i] = __float_as_uint(__uint_as_float(rb[i]) * eta);
+            }
+            tmem_st_32x32b_x32(tO + cc * 32, ra);
+            tmem_st_32x32b_x32(tO + cc * 32 + 32, rb);
           }
         }
       }
