@@ -313,9 +313,13 @@ class LinearWorkload(Workload):
 class AttentionWorkload(Workload):
     timed_alone = True
 
-    def __init__(self, torch, dev):
+    def __init__(self, torch, dev, key_block=None):
+        import dataclasses
+
         import psi_synth
         cfg = psi_synth.ATTN
+        if key_block:
+            cfg = dataclasses.replace(cfg, key_block=key_block)
         self.cfg = cfg
         self.torch = torch
         self.Q, self.K, self.V = psi_synth.attn_inputs(cfg, device=dev)
@@ -324,7 +328,7 @@ class AttentionWorkload(Workload):
         self.flops = float(cfg.flops)
         self.weight_h2d = 0
         self.name = (f"partitioned attention: Q,K,V {cfg.heads}x{cfg.N}x{cfg.dh}, scale "
-                     f"1/sqrt({cfg.dh}), 128-key tiles, FP32 online softmax")
+                     f"1/sqrt({cfg.dh}), key blocks of {cfg.key_block}, FP32 online softmax")
 
     @property
     def stream(self):
@@ -337,7 +341,8 @@ class AttentionWorkload(Workload):
         O = self.O if Y is None else Y
         psi.psi_attn_partitioned(heads_view(Q), heads_view(self.K), heads_view(self.V),
                                  heads_view(O), self.cfg.heads, self.cfg.N, self.cfg.N,
-                                 self.cfg.dh, self.cfg.scale, 128, self._stream.cuda_stream, 0)
+                                 self.cfg.dh, self.cfg.scale, self.cfg.key_block,
+                                 self._stream.cuda_stream, 0)
 
     def io(self):
         return self.Q, self.O
@@ -353,7 +358,7 @@ def make_workload(torch, dev, args):
     if args.workload == "linear":
         return LinearWorkload(torch, dev)
     if args.workload == "attention":
-        return AttentionWorkload(torch, dev)
+        return AttentionWorkload(torch, dev, args.key_block)
     raise SystemExit(f"unknown workload {args.workload}")
 
 
@@ -483,6 +488,8 @@ def main():
     ap.add_argument("--blocks", type=int, default=48, help="stack depth (workload stack)")
     ap.add_argument("--arena-mib", type=int, default=80)
     ap.add_argument("--resident", action="store_true", help="weights resident (no streaming)")
+    ap.add_argument("--key-block", type=int, default=None,
+                    help="attention workload: keys per online-softmax block (default 256)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=512)
     args = ap.parse_args()

@@ -251,7 +251,9 @@ psi_status psi_ffn_paged(psi_arena* arena, const void* X, int64_t N,
  * Unmasked, noncausal, no dropout; Nk >= 1.
  *   Q [heads x Nq x dh], K, V [heads x Nk x dh], O [heads x Nq x dh]: dev
  *   BF16 views (psi_heads strides, 16-byte aligned rows).  dh == 128.
- *   key_block: 128 or 256.
+ *   key_block: 128 or 256 keys per online-softmax update (the kernel reads
+ *   K and V in 128-key sub-tiles; with 256 a CTA holds one 128-query tile,
+ *   with 128 two).
  * Enqueued on `stream` (cudaStream_t).  No arena: inputs are resident. */
 psi_status psi_attn_partitioned(const psi_heads* Q, const psi_heads* K,
                                 const psi_heads* V, const psi_heads* O,

@@ -27,34 +27,53 @@ def _qkv(H, Nq, Nk, seed, dh=128):
     return Q, K, V
 
 
+@pytest.mark.parametrize("key_block", [128, 256])
 @pytest.mark.parametrize("H,Nq,Nk", [
     (1, 128, 128),     # one tile each
     (2, 200, 300),     # ragged queries and keys (last key tile 44 keys)
     (3, 64, 1),        # a single key: O = B(v)
     (1, 130, 129),     # one key past a tile boundary
-    (2, 256, 1024),    # several key tiles (online rescaling)
+    (2, 256, 1024),    # several key blocks (online rescaling)
+    (1, 384, 384),     # 256-key blocks: the last block has one 128-key sub-tile
 ])
-def test_attention_shapes(H, Nq, Nk):
+def test_attention_shapes(H, Nq, Nk, key_block):
     Q, K, V = _qkv(H, Nq, Nk, H * 7 + Nq + Nk)
     sc = 1 / math.sqrt(128)
-    O = run_attention(Q.cuda(), K.cuda(), V.cuda(), sc).cpu()
+    O = run_attention(Q.cuda(), K.cuda(), V.cuda(), sc, key_block=key_block).cpu()
     res = ops.attention_heads(f64(Q), f64(K), f64(V), sc)
     rep = check(O, res, what=f"attn {H}x{Nq}x{Nk}")
     assert rep["all_finite"]
 
 
-def test_attention_single_key_exact():
+@pytest.mark.parametrize("key_block", [128, 256])
+def test_attention_single_key_exact(key_block):
     Q, K, V = _qkv(2, 100, 1, 3)
-    O = run_attention(Q.cuda(), K.cuda(), V.cuda(), 0.1).cpu()
+    O = run_attention(Q.cuda(), K.cuda(), V.cuda(), 0.1, key_block=key_block).cpu()
     assert torch.equal(O.view(torch.int16), V.expand(2, 100, 128).contiguous().view(torch.int16))
 
 
+def test_attention_key_block_partitions_agree():
+    """Eq.(4) gives the dense result for any complete key partition: 128- and
+    256-key blocks differ only by rounding (both within tolerance of the
+    oracle, and close to each other)."""
+    Q, K, V = _qkv(2, 256, 1000, 5)
+    sc = 1 / math.sqrt(128)
+    a = run_attention(Q.cuda(), K.cuda(), V.cuda(), sc, key_block=128).cpu()
+    b = run_attention(Q.cuda(), K.cuda(), V.cuda(), sc, key_block=256).cpu()
+    res = ops.attention_heads(f64(Q), f64(K), f64(V), sc)
+    check(a, res, what="kb128")
+    check(b, res, what="kb256")
+    d = (a.float() - b.float()).abs().max().item()
+    assert d <= 2 ** -6
+
+
 def test_attention_config_sampled_rows():
-    """Q, K, V [32 x 4096 x 128], scale 1/sqrt(128): the GPU runs the full
-    configuration; the oracle checks every head on sampled query rows."""
+    """Q, K, V [32 x 4096 x 128], scale 1/sqrt(128), key blocks of 256: the
+    GPU runs the full configuration; the oracle checks every head on sampled
+    query rows."""
     cfg = psi_synth.ATTN
     Q, K, V = psi_synth.attn_inputs(cfg)
-    O = run_attention(Q.cuda(), K.cuda(), V.cuda(), cfg.scale).cpu()
+    O = run_attention(Q.cuda(), K.cuda(), V.cuda(), cfg.scale, key_block=cfg.key_block).cpu()
     rows = np.array([0, 1, 127, 128, 2047, 2048, 4000, 4095])
     Of = f64(O)
     Qf, Kf, Vf = f64(Q), f64(K), f64(V)
@@ -67,7 +86,8 @@ def test_attention_config_sampled_rows():
     assert np.isfinite(Of).all()
 
 
-def test_attention_interleaved_layout():
+@pytest.mark.parametrize("key_block", [128, 256])
+def test_attention_interleaved_layout(key_block):
     """Heads interleaved within a token row (the fused QKV projection output):
     Q, K, V read in place from [tokens x 3*H*dh], O written to [tokens x H*dh]."""
     H, N, dh = 4, 300, 128
@@ -79,8 +99,9 @@ def test_attention_interleaved_layout():
     V = view[:, 2].permute(1, 0, 2)
     Obuf = torch.full((N, H * dh), float("nan"), dtype=torch.bfloat16, device="cuda")
     O = Obuf.view(N, H, dh).permute(1, 0, 2)
-    run_attention(Q, K, V, 1 / math.sqrt(dh), O=O)
-    ref = run_attention(Q.contiguous(), K.contiguous(), V.contiguous(), 1 / math.sqrt(dh))
+    run_attention(Q, K, V, 1 / math.sqrt(dh), key_block=key_block, O=O)
+    ref = run_attention(Q.contiguous(), K.contiguous(), V.contiguous(), 1 / math.sqrt(dh),
+                        key_block=key_block)
     assert torch.equal(O.contiguous().view(torch.int16), ref.view(torch.int16))
     res = ops.attention_heads(f64(Q), f64(K), f64(V), 1 / math.sqrt(dh))
     check(O.contiguous().cpu(), res, what="interleaved")

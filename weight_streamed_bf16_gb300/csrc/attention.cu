@@ -6,25 +6,26 @@
 // v_j, output z/l) and section III-A (FP32 online accumulation in place of
 // BF16 numerator exponential weights).
 //
-// One CTA per (head, 256 queries) = two 128-query tiles that share every K
-// and V tile.  Key tiles of 128:
-//   warp 0      TMA producer: Q (both tiles) once, then K_j and V_j into
-//               2-stage rings
-//   warp 1      TMEM owner and MMA issuer, ping-ponging the two query tiles:
-//                 S_t = Q_t K_j^T          (M=128, N=128 keys, K=128) into
-//                                          the S/P columns of tile t
-//                 O_t += P_t,hi V_j + P_t,lo V_j   (P read from tensor memory,
+// Keys are visited in blocks of key_block = 128 or 256 (one online update per
+// block), read as 128-key K/V sub-tiles.  A CTA holds NT query tiles of 128
+// (NT = 2 for 128-key blocks, 1 for 256-key blocks):
+//   warp 0      TMA producer: Q once, then per block its K sub-tiles and its
+//               V sub-tiles into 2-stage rings
+//   warp 1      TMEM owner and MMA issuer:
+//                 S_t = Q_t K^T            (M=128, N=128 per sub-tile, K=128)
+//                                          into the S/P columns of tile t
+//                 O_t += P_t,hi V + P_t,lo V   (P read from tensor memory,
 //                                          V read MN-major from shared memory)
-//   warps 2..5  softmax of tile 0, warps 6..9 softmax of tile 1, one query
-//               row per thread: scores scaled to log2 units in FP32, running
-//               max m and sum l in FP32, weights p = 2^(s - m) in FP32 split
-//               into p_hi = B(p) and p_lo = B(p - p_hi) (the tensor-core
-//               operand then carries p to within 2^-17 relative) and written
-//               over the row's S columns (two passes over tensor memory:
-//               row extremum, then exponentials); O rescaled by eta in
-//               tensor memory when the max moves; O / l written as BF16.
-// While one softmax warpgroup works on its tile, the tensor core runs the
-// other tile's MMAs.
+//               with two tiles it ping-pongs them: tile t's next S is issued
+//               right after its PV, while the other tile is in softmax
+//   warps 2..   softmax, 4 warps per query tile, one query row per thread:
+//               two passes over tensor memory (row extremum, then
+//               p = 2^(s*scale*log2e - m) by one FFMA and ex2), running max m
+//               and sum l in FP32, p split into p_hi = B(p) and
+//               p_lo = B(p - p_hi) (the tensor-core operand carries p to
+//               within 2^-17 relative) and written over the row's S
+//               columns; O rescaled by eta in tensor memory when the max
+//               moves; O / l written as BF16 at the end.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -32,30 +33,38 @@ namespace psi {
 namespace {
 
 constexpr int BQ = 128;      // queries per tile
-constexpr int NT = 2;        // query tiles per CTA
-constexpr int BKEY = 128;    // keys per tile
+constexpr int SUB = 128;     // keys per K/V sub-tile (one S = QK^T MMA of N = 128)
 constexpr int DH = 128;
-constexpr int kThreads = 64 + NT * 128;
 constexpr int TILE64 = 128 * 128;  // one [128 rows x 64 cols] BF16 swizzled block, bytes
 
-constexpr int OFF_Q = 0;                              // NT tiles x 2 column blocks
-constexpr int OFF_K = OFF_Q + NT * 2 * TILE64;        // 2 stages x 2 column blocks
-constexpr int OFF_V = OFF_K + 2 * 2 * TILE64;
-constexpr int OFF_BAR = OFF_V + 2 * 2 * TILE64;       // 192 KiB
-constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
-
-// tensor memory: tile t uses columns [256 t, 256 t + 128) for S and P over
-// it (for keys 32c..32c+31: p_hi pairs in columns 32c..32c+15, p_lo pairs in
-// 32c+16..32c+31) and [256 t + 128, 256 t + 256) for O
-constexpr uint32_t TM_COLS = 512;
-__device__ __forceinline__ uint32_t tm_s(int t) { return 256u * t; }
-__device__ __forceinline__ uint32_t tm_o(int t) { return 256u * t + 128u; }
+// Kernel shape for key blocks of KSUB sub-tiles (key_block = 128 * KSUB):
+// NT query tiles per CTA (two when the block is 128 keys, so the softmax
+// warpgroups ping-pong; one when it is 256 keys, whose S needs 256 TMEM
+// columns).  Tensor memory per tile: S and P over it (128 * KSUB columns;
+// for keys 32c..32c+31 of the block: p_hi pairs in columns 32c..32c+15, p_lo
+// pairs in 32c+16..32c+31), then O (128 columns).
+template <int KSUB>
+struct AShape {
+  static constexpr int NT = KSUB == 1 ? 2 : 1;
+  static constexpr int KB = SUB * KSUB;
+  static constexpr int kThreads = 64 + NT * 128;
+  static constexpr int OFF_Q = 0;                          // NT tiles x 2 column blocks
+  static constexpr int OFF_K = OFF_Q + NT * 2 * TILE64;    // 2 stages x 2 column blocks
+  static constexpr int OFF_V = OFF_K + 2 * 2 * TILE64;
+  static constexpr int OFF_BAR = OFF_V + 2 * 2 * TILE64;
+  static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
+  static constexpr uint32_t TILE_COLS = KB + 128;
+  static constexpr uint32_t TM_COLS = 512;
+  static_assert(NT * TILE_COLS <= TM_COLS, "tensor memory");
+  __device__ static uint32_t tm_s(int t) { return TILE_COLS * t; }
+  __device__ static uint32_t tm_o(int t) { return TILE_COLS * t + KB; }
+};
 
 struct __align__(8) ABars {
   uint64_t q_full;
   uint64_t k_full[2], k_empty[2];
   uint64_t v_full[2], v_empty[2];
-  uint64_t s_full[NT], p_full[NT], pv_done[NT];
+  uint64_t s_full[2], p_full[2], pv_done[2];
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -76,20 +85,25 @@ __device__ __forceinline__ void record_error(DevError* e, int code, int where, i
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+template <int KSUB>
+__global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const View vq, const View vk,
                 const View vv, const AttnArgs args) {
+  using A = AShape<KSUB>;
+  constexpr int NT = A::NT;
+  constexpr int KB = A::KB;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  ABars* bars = reinterpret_cast<ABars*>(smem + OFF_BAR);
+  ABars* bars = reinterpret_cast<ABars*>(smem + A::OFF_BAR);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int q_blocks = (args.Nq + NT * BQ - 1) / (NT * BQ);
   const int head = blockIdx.x / q_blocks;
   const int q0 = (blockIdx.x % q_blocks) * (NT * BQ);
-  const int nb = (args.Nk + BKEY - 1) / BKEY;
+  const int nsub = (args.Nk + SUB - 1) / SUB;  // K/V sub-tiles
+  const int nb = (args.Nk + KB - 1) / KB;      // online-softmax key blocks
   volatile int* abort_flag = &bars->abort_flag;
   constexpr int kWhere = KID_ATTN * 16;
 
@@ -114,7 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmV);
   }
   if (warp == 1) {
-    tmem_alloc(&bars->tmem_base, TM_COLS);
+    tmem_alloc(&bars->tmem_base, A::TM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -124,40 +138,47 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer --
+    // Q once; then per key block its K sub-tiles, then its V sub-tiles
+    // (sub-tile js lives in ring stage js & 1)
     if (lane == 0) {
       uint32_t k_armed = 0, v_armed = 0;  // per-stage parity of the last arming
       int k_cnt[2] = {0, 0}, v_cnt[2] = {0, 0};
       mbar_arrive_expect_tx(&bars->q_full, NT * 2 * TILE64);
       for (int t = 0; t < NT; ++t)
         for (int cb = 0; cb < 2; ++cb)
-          tma_load_2d(smem + OFF_Q + (t * 2 + cb) * TILE64, &tmQ, &bars->q_full,
+          tma_load_2d(smem + A::OFF_Q + (t * 2 + cb) * TILE64, &tmQ, &bars->q_full,
                       head * vq.hx + cb * 64, head * vq.hy + q0 + t * BQ);
-      for (int j = 0; j < nb; ++j) {
-        const int s = j & 1;
-        const uint32_t par = ((j >> 1) & 1) ^ 1;
-        const int key0 = j * BKEY;
-        if (!mbar_wait(&bars->k_empty[s], par, abort_flag, args.timeout_ns)) {
-          record_error(args.err, 1, kWhere + 0, j, 0);
-          bars->abort_flag = 1;
-          break;
+      bool ok = true;
+      for (int j = 0; j < nb && ok; ++j) {
+        for (int kv = 0; kv < 2 && ok; ++kv) {
+          for (int u = 0; u < KSUB; ++u) {
+            const int js = j * KSUB + u;
+            if (js >= nsub) break;
+            const int s = js & 1;
+            const uint32_t par = ((js >> 1) & 1) ^ 1;
+            uint64_t* empty = kv ? &bars->v_empty[s] : &bars->k_empty[s];
+            uint64_t* full = kv ? &bars->v_full[s] : &bars->k_full[s];
+            if (!mbar_wait(empty, par, abort_flag, args.timeout_ns)) {
+              record_error(args.err, 1, kWhere + 0, js, kv);
+              bars->abort_flag = 1;
+              ok = false;
+              break;
+            }
+            uint8_t* dst = smem + (kv ? A::OFF_V : A::OFF_K) + s * 2 * TILE64;
+            const CUtensorMap* m = kv ? &tmV : &tmK;
+            const View& vw = kv ? vv : vk;
+            mbar_arrive_expect_tx(full, 2 * TILE64);
+            tma_load_2d(dst, m, full, head * vw.hx, head * vw.hy + js * SUB);
+            tma_load_2d(dst + TILE64, m, full, head * vw.hx + 64, head * vw.hy + js * SUB);
+            if (kv) {
+              v_armed = (v_armed & ~(1u << s)) | (static_cast<uint32_t>(v_cnt[s] & 1) << s);
+              ++v_cnt[s];
+            } else {
+              k_armed = (k_armed & ~(1u << s)) | (static_cast<uint32_t>(k_cnt[s] & 1) << s);
+              ++k_cnt[s];
+            }
+          }
         }
-        uint8_t* kd = smem + OFF_K + s * 2 * TILE64;
-        mbar_arrive_expect_tx(&bars->k_full[s], 2 * TILE64);
-        tma_load_2d(kd, &tmK, &bars->k_full[s], head * vk.hx, head * vk.hy + key0);
-        tma_load_2d(kd + TILE64, &tmK, &bars->k_full[s], head * vk.hx + 64, head * vk.hy + key0);
-        k_armed = (k_armed & ~(1u << s)) | (static_cast<uint32_t>(k_cnt[s] & 1) << s);
-        ++k_cnt[s];
-        if (!mbar_wait(&bars->v_empty[s], par, abort_flag, args.timeout_ns)) {
-          record_error(args.err, 1, kWhere + 0, j, 1);
-          bars->abort_flag = 1;
-          break;
-        }
-        uint8_t* vd = smem + OFF_V + s * 2 * TILE64;
-        mbar_arrive_expect_tx(&bars->v_full[s], 2 * TILE64);
-        tma_load_2d(vd, &tmV, &bars->v_full[s], head * vv.hx, head * vv.hy + key0);
-        tma_load_2d(vd + TILE64, &tmV, &bars->v_full[s], head * vv.hx + 64, head * vv.hy + key0);
-        v_armed = (v_armed & ~(1u << s)) | (static_cast<uint32_t>(v_cnt[s] & 1) << s);
-        ++v_cnt[s];
       }
       // drain this thread's copies before the CTA exits
       int dummy = 0;
@@ -181,63 +202,76 @@ __global__ void __launch_bounds__(kThreads, 1)
         bars->abort_flag = 1;
         ok = false;
       };
-      // S_t = Q_t K_j^T into tile t's S/P columns
+      // S_t = Q_t K^T for the sub-tiles of key block j, into tile t's S columns
       auto issue_s = [&](int j, int t) {
-        const int s = j & 1;
-        if (t == 0) {
-          if (!mbar_wait(&bars->k_full[s], (j >> 1) & 1, abort_flag, args.timeout_ns)) {
-            fail(j, 0);
-            return;
+        const uint32_t sQ = smem_u32(smem + A::OFF_Q + t * 2 * TILE64);
+        for (int u = 0; u < KSUB; ++u) {
+          const int js = j * KSUB + u;
+          if (js >= nsub) break;
+          const int s = js & 1;
+          if (t == 0) {
+            if (!mbar_wait(&bars->k_full[s], (js >> 1) & 1, abort_flag, args.timeout_ns)) {
+              fail(js, 0);
+              return;
+            }
+            tc_fence_after();
           }
-          tc_fence_after();
-        }
-        const uint32_t sK = smem_u32(smem + OFF_K + s * 2 * TILE64);
-        const uint32_t sQ = smem_u32(smem + OFF_Q + t * 2 * TILE64);
+          const uint32_t sK = smem_u32(smem + A::OFF_K + s * 2 * TILE64);
 #pragma unroll
-        for (int kk = 0; kk < DH / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * TILE64 + (kk & 3) * 32;
-          mma_bf16_ss(tmem + tm_s(t), sdesc_sw128(sQ + off, 16, 1024),
-                      sdesc_sw128(sK + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < DH / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * TILE64 + (kk & 3) * 32;
+            mma_bf16_ss(tmem + A::tm_s(t) + SUB * u, sdesc_sw128(sQ + off, 16, 1024),
+                        sdesc_sw128(sK + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+          }
+          if (t == NT - 1) mma_commit(&bars->k_empty[s]);  // every tile has read it
+          issued = true;
         }
         mma_commit(&bars->s_full[t]);
-        if (t == NT - 1) mma_commit(&bars->k_empty[s]);  // both tiles have read K_j
-        issued = true;
       };
       if (!mbar_wait(&bars->q_full, 0, abort_flag, args.timeout_ns)) fail(-1, 2);
       for (int t = 0; t < NT && ok; ++t) issue_s(0, t);
       for (int j = 0; j < nb && ok; ++j) {
-        const int s = j & 1;
-        if (!mbar_wait(&bars->v_full[s], (j >> 1) & 1, abort_flag, args.timeout_ns)) {
-          fail(j, 4);
-          break;
-        }
-        const uint32_t sV = smem_u32(smem + OFF_V + s * 2 * TILE64);
         for (int t = 0; t < NT && ok; ++t) {
           if (!mbar_wait(&bars->p_full[t], j & 1, abort_flag, args.timeout_ns)) {
             fail(j, 3);
             break;
           }
           tc_fence_after();
-          // O_t += P_hi V_j + P_lo V_j: P from tensor memory, keys 16kk..16kk+15
-          // at columns 32(kk/2) + 8(kk%2) (hi) and 16 further (lo); V rows
-          // 16kk.. of both 64-wide dh blocks (LBO apart)
+          // O_t += P_hi V + P_lo V over the block's sub-tiles: P from tensor
+          // memory (keys 16kk.. of sub-tile u at column 128u + 32(kk/2) +
+          // 8(kk%2), lo 16 further), V rows 16kk.. of both 64-wide dh blocks
+          for (int u = 0; u < KSUB && ok; ++u) {
+            const int js = j * KSUB + u;
+            if (js >= nsub) break;
+            const int s = js & 1;
+            if (t == 0) {
+              if (!mbar_wait(&bars->v_full[s], (js >> 1) & 1, abort_flag, args.timeout_ns)) {
+                fail(js, 4);
+                break;
+              }
+              tc_fence_after();
+            }
+            const uint32_t sV = smem_u32(smem + A::OFF_V + s * 2 * TILE64);
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
+            for (int half = 0; half < 2; ++half) {
 #pragma unroll
-            for (int kk = 0; kk < BKEY / 16; ++kk) {
-              const uint32_t pcol = 32 * (kk >> 1) + 8 * (kk & 1) + 16 * half;
-              mma_bf16_ts(tmem + tm_o(t), tmem + tm_s(t) + pcol,
-                          sdesc_sw128(sV + kk * 2048, TILE64, 1024), idesc_o,
-                          (j | half | kk) != 0 ? 1u : 0u);
+              for (int kk = 0; kk < SUB / 16; ++kk) {
+                const uint32_t pcol = SUB * u + 32 * (kk >> 1) + 8 * (kk & 1) + 16 * half;
+                mma_bf16_ts(tmem + A::tm_o(t), tmem + A::tm_s(t) + pcol,
+                            sdesc_sw128(sV + kk * 2048, TILE64, 1024), idesc_o,
+                            (j | u | half | kk) != 0 ? 1u : 0u);
+              }
             }
           }
+          if (!ok) break;
           mma_commit(&bars->pv_done[t]);
           // tile t's next scores overwrite its P: issued after its PV MMAs,
           // which the tensor core executes first
           if (j + 1 < nb) issue_s(j + 1, t);
         }
         if (!ok) break;
-        mma_commit(&bars->v_empty[s]);
+        for (int u = 0; u < KSUB; ++u)
+          if (j * KSUB + u < nsub) mma_commit(&bars->v_empty[(j * KSUB + u) & 1]);
       }
       if (issued) {
         mma_commit(&bars->drain);
@@ -252,8 +286,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;          // TMEM lane quarter
     const int row = q * 32 + lane;   // query row within the tile
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-    const uint32_t tS = tmem + tm_s(t) + lane_off;
-    const uint32_t tO = tmem + tm_o(t) + lane_off;
+    const uint32_t tS = tmem + A::tm_s(t) + lane_off;
+    const uint32_t tO = tmem + A::tm_o(t) + lane_off;
+    constexpr int NCH = KB / 32;     // 32-key chunks per block
     float m2 = -INFINITY;  // running max, log2 units
     float l = 0.f;         // running sum of weights
     bool ok = true;
@@ -265,46 +300,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      // pass 1: row extremum of the raw scores (max, or min for a negative
-      // scale); all four chunks are loaded before one wait
+      // pass 1: row extremum of the raw scores over the block (max, or min for
+      // a negative scale); four chunks are loaded before each wait
       const float c = args.scale_log2;  // scale * log2(e)
-      const int kvalid = args.Nk - j * BKEY;  // keys of this tile that exist
+      const int kvalid = args.Nk - j * KB;  // keys of this block that exist
       float ext = c >= 0.f ? -INFINITY : INFINITY;
-      {
-        uint32_t ra[32], rb[32], rc[32], rd[32];
-        tmem_ld_32x32b_x32(tS + 0, ra);
-        tmem_ld_32x32b_x32(tS + 32, rb);
-        tmem_ld_32x32b_x32(tS + 64, rc);
-        tmem_ld_32x32b_x32(tS + 96, rd);
-        tmem_wait_ld();
-        auto scan = [&](const uint32_t (&r)[32], int base) {
-          if (kvalid >= BKEY) {
+      auto scan = [&](const uint32_t (&r)[32], int base) {
+        if (kvalid >= KB) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
+          for (int i = 0; i < 32; ++i)
+            ext = c >= 0.f ? fmaxf(ext, __uint_as_float(r[i])) : fminf(ext, __uint_as_float(r[i]));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (base + i < kvalid)
               ext = c >= 0.f ? fmaxf(ext, __uint_as_float(r[i])) : fminf(ext, __uint_as_float(r[i]));
-          } else {
+        }
+      };
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (base + i < kvalid)
-                ext = c >= 0.f ? fmaxf(ext, __uint_as_float(r[i]))
-                               : fminf(ext, __uint_as_float(r[i]));
-          }
-        };
-        scan(ra, 0);
-        scan(rb, 32);
-        scan(rc, 64);
-        scan(rd, 96);
+      for (int g = 0; g < NCH; g += 4) {
+        uint32_t ra[32], rb[32], rc[32], rd[32];
+        tmem_ld_32x32b_x32(tS + (g + 0) * 32, ra);
+        tmem_ld_32x32b_x32(tS + (g + 1) * 32, rb);
+        tmem_ld_32x32b_x32(tS + (g + 2) * 32, rc);
+        tmem_ld_32x32b_x32(tS + (g + 3) * 32, rd);
+        tmem_wait_ld();
+        scan(ra, (g + 0) * 32);
+        scan(rb, (g + 1) * 32);
+        scan(rc, (g + 2) * 32);
+        scan(rd, (g + 3) * 32);
       }
       const float m_new = fmaxf(m2, ext * c);
-      const float eta = ex2_approx(m2 - m_new);  // 0 on the first tile
-      // pass 2: p = 2^(s*c - m) with one FFMA; the chunk of 32 keys is
+      const float eta = ex2_approx(m2 - m_new);  // 0 on the first block
+      // pass 2: p = 2^(s*c - m) with one FFMA; each chunk of 32 keys is
       // written back over its own 32 columns as 16 columns of p_hi pairs and
       // 16 of p_lo pairs (keys 2i, 2i+1 share a column).  The next chunk's
       // load is in flight while this chunk is processed.
       float rs = 0.f;
       auto expo = [&](const uint32_t (&r)[32], int cc) {
         float p[32];
-        if (kvalid >= BKEY) {
+        if (kvalid >= KB) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) p[i] = ex2_approx(fmaf(__uint_as_float(r[i]), c, -m_new));
         } else {
@@ -324,18 +359,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       {
         uint32_t r0[32], r1[32];
-        tmem_ld_32x32b_x32(tS + 0, r0);
+        tmem_ld_32x32b_x32(tS, r0);
         tmem_wait_ld();
-        tmem_ld_32x32b_x32(tS + 32, r1);
-        expo(r0, 0);
-        tmem_wait_ld();
-        tmem_ld_32x32b_x32(tS + 64, r0);
-        expo(r1, 1);
-        tmem_wait_ld();
-        tmem_ld_32x32b_x32(tS + 96, r1);
-        expo(r0, 2);
-        tmem_wait_ld();
-        expo(r1, 3);
+#pragma unroll
+        for (int cc = 0; cc < NCH; cc += 2) {
+          tmem_ld_32x32b_x32(tS + (cc + 1) * 32, r1);
+          expo(r0, cc);
+          tmem_wait_ld();
+          if (cc + 2 < NCH) tmem_ld_32x32b_x32(tS + (cc + 2) * 32, r0);
+          expo(r1, cc + 1);
+          tmem_wait_ld();
+        }
       }
       l = eta * l + rs;
       m2 = m_new;
@@ -379,12 +413,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint16_t* orow =
             args.O + head * args.o_ld_head + static_cast<int64_t>(tok) * args.o_ld_token;
 #pragma unroll 1
-        for (int c = 0; c < DH / 32; ++c) {
+        for (int cc = 0; cc < DH / 32; ++cc) {
           uint32_t r[32];
-          tmem_ld_32x32b_x32(tO + c * 32, r);
+          tmem_ld_32x32b_x32(tO + cc * 32, r);
           tmem_wait_ld();
           if (tok < args.Nq) {
-            uint4* o4 = reinterpret_cast<uint4*>(orow + c * 32);
+            uint4* o4 = reinterpret_cast<uint4*>(orow + cc * 32);
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
               float v[8];
@@ -403,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, TM_COLS);
+    tmem_dealloc(tmem, A::TM_COLS);
   }
 }
 
@@ -429,6 +463,30 @@ psi_status make_view(const psi_heads* h, int heads, int64_t tokens, CUtensorMap*
                                         "interleaved within a row");
 }
 
+template <int KSUB>
+psi_status launch_k(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                    const View& vq, const View& vk, const View& vv, const AttnArgs& a,
+                    cudaStream_t stream) {
+  using A = AShape<KSUB>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(attn_kernel<KSUB>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         A::SMEM_BYTES);
+    if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute(attn)");
+    attr_set = true;
+  }
+  const int q_blocks = (a.Nq + A::NT * BQ - 1) / (A::NT * BQ);
+  const long long grid = static_cast<long long>(q_blocks) * a.heads;
+  if (grid <= 0) return PSI_OK;
+  if (grid > 0x7FFFFFFFLL) return set_error(PSI_ERR_UNSUPPORTED, "attention: grid too large");
+  attn_kernel<KSUB><<<static_cast<unsigned>(grid), A::kThreads, A::SMEM_BYTES, stream>>>(
+      mq, mk, mv, vq, vk, vv, a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_error(e, "attention launch");
+  return PSI_OK;
+}
+
 }  // namespace
 
 psi_status launch_attention(const psi_heads* Q, const psi_heads* K, const psi_heads* V,
@@ -439,22 +497,9 @@ psi_status launch_attention(const psi_heads* Q, const psi_heads* K, const psi_he
   if (st != PSI_OK) return st;
   if ((st = make_view(K, a.heads, a.Nk, &mk, &vk)) != PSI_OK) return st;
   if ((st = make_view(V, a.heads, a.Nk, &mv, &vv)) != PSI_OK) return st;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e =
-        cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute(attn)");
-    attr_set = true;
-  }
-  const int q_blocks = (a.Nq + NT * BQ - 1) / (NT * BQ);
-  const long long grid = static_cast<long long>(q_blocks) * a.heads;
-  if (grid <= 0) return PSI_OK;
-  if (grid > 0x7FFFFFFFLL) return set_error(PSI_ERR_UNSUPPORTED, "attention: grid too large");
-  attn_kernel<<<static_cast<unsigned>(grid), kThreads, SMEM_BYTES, stream>>>(mq, mk, mv, vq, vk,
-                                                                             vv, a);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_error(e, "attention launch");
-  return PSI_OK;
+  if (a.key_block == 128) return launch_k<1>(mq, mk, mv, vq, vk, vv, a, stream);
+  if (a.key_block == 256) return launch_k<2>(mq, mk, mv, vq, vk, vv, a, stream);
+  return set_error(PSI_ERR_UNSUPPORTED, "attention: key_block must be 128 or 256");
 }
 
 }  // namespace psi

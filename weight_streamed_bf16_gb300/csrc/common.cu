@@ -85,19 +85,24 @@ static psi_status get_encoder() {
   return PSI_OK;
 }
 
-psi_status make_tmap_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
-                        uint64_t ld, uint32_t box_rows, uint32_t box_cols) {
+psi_status make_tmap_2d_ex(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                           uint64_t ld, uint32_t box_rows, uint32_t box_cols, int elem_bytes,
+                           int swizzle_bytes) {
   psi_status st = get_encoder();
   if (st != PSI_OK) return st;
-  if ((reinterpret_cast<uintptr_t>(base) & 15) || ((ld * 2) & 15))
+  if ((reinterpret_cast<uintptr_t>(base) & 15) || ((ld * elem_bytes) & 15))
     return set_error(PSI_ERR_INVALID_ARG, "tensor map: base or row stride not 16-byte aligned");
   cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {ld * 2};
+  cuuint64_t strides[1] = {ld * static_cast<uint64_t>(elem_bytes)};
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
-                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  const CUtensorMapDataType dt =
+      elem_bytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapSwizzle sw = swizzle_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                      : CU_TENSOR_MAP_SWIZZLE_NONE;
+  CUresult r = g_encode(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     char buf[160];
@@ -107,6 +112,11 @@ psi_status make_tmap_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_
     return set_error(PSI_ERR_CUDA, buf);
   }
   return PSI_OK;
+}
+
+psi_status make_tmap_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                        uint64_t ld, uint32_t box_rows, uint32_t box_cols) {
+  return make_tmap_2d_ex(m, base, rows, cols, ld, box_rows, box_cols, 2, 128);
 }
 
 }  // namespace psi

@@ -34,6 +34,11 @@ psi_status cuda_error(cudaError_t e, const char* what);
 // {box_cols, box_rows}, 128-byte swizzle.
 psi_status make_tmap_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
                         uint64_t ld, uint32_t box_rows, uint32_t box_cols);
+// The same for a BF16 (elem_bytes 2) or FP32 (4) tensor with a 128-, 64-byte
+// or no swizzle (swizzle_bytes 128, 64, 0).
+psi_status make_tmap_2d_ex(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                           uint64_t ld, uint32_t box_rows, uint32_t box_cols, int elem_bytes,
+                           int swizzle_bytes);
 int num_sms();
 
 // ------------------------------------------------------------ page GEMM --

@@ -41,7 +41,11 @@ struct Cfg {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int TMEM_COLS = 2 * BN;
   static constexpr int BAR_OFFSET = STAGES * STAGE_BYTES;
-  static constexpr int SMEM_BYTES = BAR_OFFSET + 256 + 1024;  // + barriers + align slack
+  // one 4 KiB store-staging buffer per epilogue warp after the barriers
+  static constexpr int STG_OFFSET = BAR_OFFSET + 1024;
+  static constexpr int STG_BYTES = 4096;
+  static constexpr int SMEM_BYTES = STG_OFFSET + 8 * STG_BYTES + 1024;  // + align slack
+  static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
 struct __align__(8) Bars {
@@ -77,6 +81,9 @@ __device__ __forceinline__ float round_bf16_f(float x) {
 __device__ __forceinline__ bool epi_reads_acc(int epi) {
   return epi == EPI_ACC_ADD || epi == EPI_ACC_FINAL;
 }
+__device__ __forceinline__ bool epi_writes_f32(int epi) {
+  return epi == EPI_ACC_STORE || epi == EPI_ACC_ADD;
+}
 
 // The 32 FP32 accumulator values of one row chunk (full chunks only).
 __device__ __forceinline__ void load_acc32(const GemmArgs& a, int row, int col0,
@@ -87,35 +94,45 @@ __device__ __forceinline__ void load_acc32(const GemmArgs& a, int row, int col0,
   for (int j = 0; j < 8; ++j) q[j] = p4[j];
 }
 
-// Epilogue of 32 consecutive columns of one row.  v[] are the FP32
-// accumulator values; col0 is the first column; ncol <= 32 valid columns;
-// wq[] holds the FP32 workspace values of a full chunk (loaded ahead).
-__device__ __forceinline__ void epilogue_row32(const GemmArgs& a, int row, int col0, int ncol,
-                                               float (&v)[32], const float4 (&wq)[8]) {
-  const bool full = (ncol == 32);
-  if (a.epi == EPI_ACC_STORE || a.epi == EPI_ACC_ADD) {
-    float* p = a.accf + static_cast<int64_t>(row) * a.ldacc + col0;
-    if (full) {
-      float4* p4 = reinterpret_cast<float4*>(p);
+// Fused epilogue of 32 consecutive columns of one row.  v[] holds the FP32
+// MMA results; col0 is the first column, ncol <= 32 of them exist, row_ok
+// says whether the row exists (inputs of missing rows/columns are not read;
+// their outputs are clipped by the tensor store).  wq[] holds the FP32
+// workspace values of a full chunk, loaded ahead.  The results go to the
+// warp's staging buffer `stg` (row = lane) in the layout of the tensor
+// store: FP32 rows of 128 B with 128-byte swizzle, or BF16 rows of 64 B with
+// 64-byte swizzle.
+__device__ __forceinline__ void epilogue_row32(const GemmArgs& a, int row, bool row_ok,
+                                               int col0, int ncol, float (&v)[32],
+                                               const float4 (&wq)[8], uint8_t* stg, int lane) {
+  const bool full = (ncol == 32) && row_ok;
+  if (epi_writes_f32(a.epi)) {
+    if (a.epi == EPI_ACC_ADD) {
+      if (full) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        float4 o = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-        if (a.epi == EPI_ACC_ADD) {
-          o.x = wq[j].x + o.x;
-          o.y = wq[j].y + o.y;
-          o.z = wq[j].z + o.z;
-          o.w = wq[j].w + o.w;
+        for (int j = 0; j < 8; ++j) {
+          v[4 * j] = wq[j].x + v[4 * j];
+          v[4 * j + 1] = wq[j].y + v[4 * j + 1];
+          v[4 * j + 2] = wq[j].z + v[4 * j + 2];
+          v[4 * j + 3] = wq[j].w + v[4 * j + 3];
         }
-        p4[j] = o;
+      } else if (row_ok) {
+        const float* p = a.accf + static_cast<int64_t>(row) * a.ldacc + col0;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j < ncol) v[j] = p[j] + v[j];
       }
-    } else {
-      for (int j = 0; j < ncol; ++j) p[j] = (a.epi == EPI_ACC_ADD) ? p[j] + v[j] : v[j];
     }
+    uint8_t* rowp = stg + lane * 128;
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      *reinterpret_cast<float4*>(rowp + ((c ^ (lane & 7)) << 4)) =
+          make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
     return;
   }
-  // BF16 outputs: gather bias (and accumulator / residual) into v
+  // BF16 outputs: bias (+ FP32 accumulator) (+ GELU) (+ residual)
   float bia[32];
-  if (full) {
+  if (col0 + 32 <= a.N) {
     const uint4* b4 = reinterpret_cast<const uint4*>(a.bias + col0);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -133,7 +150,6 @@ __device__ __forceinline__ void epilogue_row32(const GemmArgs& a, int row, int c
       bia[j] = j < ncol ? __uint_as_float(static_cast<uint32_t>(a.bias[col0 + j]) << 16) : 0.f;
   }
   if (a.epi == EPI_ACC_FINAL) {
-    const float* p = a.accf + static_cast<int64_t>(row) * a.ldacc + col0;
     if (full) {
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
@@ -142,8 +158,11 @@ __device__ __forceinline__ void epilogue_row32(const GemmArgs& a, int row, int c
         v[4 * j + 2] = wq[j].z + v[4 * j + 2];
         v[4 * j + 3] = wq[j].w + v[4 * j + 3];
       }
-    } else {
-      for (int j = 0; j < ncol; ++j) v[j] = p[j] + v[j];
+    } else if (row_ok) {
+      const float* p = a.accf + static_cast<int64_t>(row) * a.ldacc + col0;
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < ncol) v[j] = p[j] + v[j];
     }
   }
 #pragma unroll
@@ -156,10 +175,9 @@ __device__ __forceinline__ void epilogue_row32(const GemmArgs& a, int row, int c
       v[j] = gelu_tanh(t);
     }
   }
-  uint16_t* out = a.out + static_cast<int64_t>(row) * a.ldo + col0;
-  const uint16_t* res = a.resid ? a.resid + static_cast<int64_t>(row) * a.ldo + col0 : nullptr;
-  if (full) {
-    if (res) {
+  if (a.resid && row_ok) {
+    const uint16_t* res = a.resid + static_cast<int64_t>(row) * a.ldo + col0;
+    if (ncol == 32) {
       const uint4* r4 = reinterpret_cast<const uint4*>(res);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -171,31 +189,26 @@ __device__ __forceinline__ void epilogue_row32(const GemmArgs& a, int row, int c
           v[8 * j + 2 * t + 1] += bf16_hi(w[t]);
         }
       }
-    }
-    uint4* o4 = reinterpret_cast<uint4*>(out);
+    } else {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      uint4 q;
-      q.x = pack_bf16x2(v[8 * j + 0], v[8 * j + 1]);
-      q.y = pack_bf16x2(v[8 * j + 2], v[8 * j + 3]);
-      q.z = pack_bf16x2(v[8 * j + 4], v[8 * j + 5]);
-      q.w = pack_bf16x2(v[8 * j + 6], v[8 * j + 7]);
-      o4[j] = q;
-    }
-  } else {
-    for (int j = 0; j < ncol; ++j) {
-      float t = v[j];
-      if (res) t += __uint_as_float(static_cast<uint32_t>(res[j]) << 16);
-      out[j] = static_cast<uint16_t>(pack_bf16x2(t, 0.f) & 0xFFFFu);
+      for (int j = 0; j < 32; ++j)
+        if (j < ncol) v[j] += __uint_as_float(static_cast<uint32_t>(res[j]) << 16);
     }
   }
+  uint8_t* rowp = stg + lane * 64;
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    *reinterpret_cast<uint4*>(rowp + ((c ^ ((lane >> 1) & 3)) << 4)) =
+        make_uint4(pack_bf16x2(v[8 * c + 0], v[8 * c + 1]), pack_bf16x2(v[8 * c + 2], v[8 * c + 3]),
+                   pack_bf16x2(v[8 * c + 4], v[8 * c + 5]), pack_bf16x2(v[8 * c + 6], v[8 * c + 7]));
 }
 
 template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     page_gemm_kernel(const __grid_constant__ CUtensorMap tmX,
                      const __grid_constant__ CUtensorMap tmP,
-                     const __grid_constant__ CUtensorMap tmP2, const GemmArgs args) {
+                     const __grid_constant__ CUtensorMap tmP2,
+                     const __grid_constant__ CUtensorMap tmOut, const GemmArgs args) {
   using C = Cfg<BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -227,6 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmX);
     tma_prefetch_desc(&tmP);
     if (args.k_split || args.n_split) tma_prefetch_desc(&tmP2);
+    tma_prefetch_desc(&tmOut);
   }
   if (warp == 1) {
     tmem_alloc(&bars->tmem_base, C::TMEM_COLS);
@@ -343,6 +357,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int half = (warp - 2) >> 2;       // column half of the tile
     constexpr int CH = BN / 64;             // 32-column chunks per half
     const bool pre = epi_reads_acc(args.epi);
+    const bool f32 = epi_writes_f32(args.epi);
+    // staging: 4 KiB per warp; FP32 chunks use all of it, BF16 chunks
+    // alternate between its two halves so a store can drain while the next
+    // chunk is written
+    uint8_t* stg_base = smem + C::STG_OFFSET + (warp - 2) * C::STG_BYTES;
+    int nstore = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
@@ -374,12 +394,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t r[32];
         tmem_ld_32x32b_x32(tbase + c * 32, r);
         tmem_wait_ld();
-        if (col0 < args.N && row_ok) {
+        if (col0 < args.N && m0 + q * 32 < args.M) {  // warp-uniform
+          uint8_t* stg = f32 ? stg_base : stg_base + (nstore & 1) * 2048;
+          // the store that last read this buffer has finished reading it
+          if (lane == 0) {
+            if (f32)
+              bulk_wait_read<0>();
+            else
+              bulk_wait_read<1>();
+          }
+          __syncwarp();
           float v[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
           const int ncol = min(32, args.N - col0);
-          epilogue_row32(args, row, col0, ncol, v, cur);
+          epilogue_row32(args, row, row_ok, col0, ncol, v, cur, stg, lane);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmOut, stg, col0, m0 + q * 32);
+            bulk_commit();
+          }
+          ++nstore;
         }
       }
       tc_fence_before();
@@ -390,6 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc_phase ^= 1;
       }
     }
+    if (lane == 0) bulk_wait<0>();  // this warp's stores are complete
   }
 
   tc_fence_before();
@@ -402,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int BN>
 psi_status launch_bn(const CUtensorMap& tx, const CUtensorMap& tp, const CUtensorMap& tp2,
-                     const GemmArgs& a, cudaStream_t s) {
+                     const CUtensorMap& to, const GemmArgs& a, cudaStream_t s) {
   using C = Cfg<BN>;
   static bool attr_set = false;  // per process; one device per process
   if (!attr_set) {
@@ -414,7 +451,7 @@ psi_status launch_bn(const CUtensorMap& tx, const CUtensorMap& tp, const CUtenso
   }
   const int tiles = ((a.M + BM - 1) / BM) * ((a.N + BN - 1) / BN);
   const int grid = tiles < num_sms() ? tiles : num_sms();
-  page_gemm_kernel<BN><<<grid, kThreads, C::SMEM_BYTES, s>>>(tx, tp, tp2, a);
+  page_gemm_kernel<BN><<<grid, kThreads, C::SMEM_BYTES, s>>>(tx, tp, tp2, to, a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_error(e, "page_gemm launch");
   return PSI_OK;
@@ -450,10 +487,17 @@ psi_status launch_page_gemm(const void* X, int64_t ldx, const void* P, int64_t l
     tp2 = tp;
   }
   if (st != PSI_OK) return st;
+  // the output tensor the epilogue stores into, in 32 x 32 boxes
+  CUtensorMap to;
+  if (a.epi == EPI_ACC_STORE || a.epi == EPI_ACC_ADD)
+    st = make_tmap_2d_ex(&to, a.accf, a.M, a.N, a.ldacc, 32, 32, 4, 128);
+  else
+    st = make_tmap_2d_ex(&to, a.out, a.M, a.N, a.ldo, 32, 32, 2, 64);
+  if (st != PSI_OK) return st;
   switch (bn) {
-    case 256: return launch_bn<256>(tx, tp, tp2, a, stream);
-    case 128: return launch_bn<128>(tx, tp, tp2, a, stream);
-    default: return launch_bn<64>(tx, tp, tp2, a, stream);
+    case 256: return launch_bn<256>(tx, tp, tp2, to, a, stream);
+    case 128: return launch_bn<128>(tx, tp, tp2, to, a, stream);
+    default: return launch_bn<64>(tx, tp, tp2, to, a, stream);
   }
 }
 

@@ -688,8 +688,8 @@ psi_status psi_attn_partitioned(const psi_heads* Q, const psi_heads* K, const ps
   if (heads <= 0 || Nq < 0 || Nk < 1)
     return set_error(PSI_ERR_INVALID_ARG, "attn: need heads >= 1, Nq >= 0 and at least one key");
   if (dh != 128) return set_error(PSI_ERR_UNSUPPORTED, "attn: this build handles dh = 128");
-  if (key_block != 128)
-    return set_error(PSI_ERR_UNSUPPORTED, "attn: key_block must be 128 in this build");
+  if (key_block != 128 && key_block != 256)
+    return set_error(PSI_ERR_UNSUPPORTED, "attn: key_block must be 128 or 256");
   if (!std::isfinite(scale)) return set_error(PSI_ERR_INVALID_ARG, "attn: scale not finite");
   if (!aligned16(O->ptr) || O->ld_token % 8 || O->ld_head % 8 || O->ld_token < dh)
     return set_error(PSI_ERR_INVALID_ARG, "attn: O rows must be 16-byte aligned");
