@@ -47,12 +47,17 @@ template <int KSUB>
 struct AShape {
   static constexpr int NT = KSUB == 1 ? 2 : 1;
   static constexpr int KB = SUB * KSUB;
-  static constexpr int kThreads = 64 + NT * 128;
+  static constexpr int SPLIT = 2;  // softmax warps per TMEM lane quarter (key halves)
+  static constexpr int kThreads = 64 + NT * 128 * SPLIT;
   static constexpr int OFF_Q = 0;                          // NT tiles x 2 column blocks
   static constexpr int OFF_K = OFF_Q + NT * 2 * TILE64;    // 2 stages x 2 column blocks
   static constexpr int OFF_V = OFF_K + 2 * 2 * TILE64;
   static constexpr int OFF_BAR = OFF_V + 2 * 2 * TILE64;
-  static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
+  // row-extremum and row-sum exchange between the two key halves of a row:
+  // [2 parities][NT tiles][SPLIT halves][128 rows] x (value, sequence)
+  static constexpr int OFF_X = OFF_BAR + 256;
+  static constexpr int X_BYTES = 2 * NT * SPLIT * 128 * 8;
+  static constexpr int SMEM_BYTES = OFF_X + X_BYTES + 1024;
   static constexpr uint32_t TILE_COLS = KB + 128;
   static constexpr uint32_t TM_COLS = 512;
   static_assert(NT * TILE_COLS <= TM_COLS, "tensor memory");
@@ -83,6 +88,34 @@ __device__ __forceinline__ void record_error(DevError* e, int code, int where, i
     e->info0 = i0;
     e->info1 = i1;
   }
+}
+
+// Publish a row value for the partner warp and read the partner's, through
+// a (value, sequence) pair in shared memory; the wait for the partner is
+// bounded.  Returns false on timeout or abort.
+__device__ __forceinline__ bool exchange(uint2* mine, const uint2* theirs, float v,
+                                         uint32_t seq, float* out, volatile int* abort,
+                                         uint64_t limit_ns) {
+  // one 8-byte access: value and sequence are seen together
+  asm volatile("st.volatile.shared.v2.u32 [%0], {%1, %2};" ::"r"(smem_u32(mine)),
+               "r"(__float_as_uint(v)), "r"(seq)
+               : "memory");
+  uint32_t val, s;
+  const uint32_t a = smem_u32(theirs);
+  asm volatile("ld.volatile.shared.v2.u32 {%0, %1}, [%2];" : "=r"(val), "=r"(s) : "r"(a) : "memory");
+  if (s != seq) {
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+      asm volatile("ld.volatile.shared.v2.u32 {%0, %1}, [%2];"
+                   : "=r"(val), "=r"(s)
+                   : "r"(a)
+                   : "memory");
+      if (s == seq) break;
+      if (*abort || globaltimer_ns() - t0 > limit_ns) return false;
+    }
+  }
+  *out = __uint_as_float(val);
+  return true;
 }
 
 template <int KSUB>
@@ -117,13 +150,17 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
     }
     for (int t = 0; t < NT; ++t) {
       mbar_init(&bars->s_full[t], 1);
-      mbar_init(&bars->p_full[t], 128);
+      mbar_init(&bars->p_full[t], 128 * A::SPLIT);
       mbar_init(&bars->pv_done[t], 1);
     }
     mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmQ);
+  }
+  for (int i = threadIdx.x; i < A::X_BYTES / 8; i += blockDim.x)
+    reinterpret_cast<uint2*>(smem + A::OFF_X)[i] = make_uint2(0u, 0u);
+  if (threadIdx.x == 0) {
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
   }
@@ -282,26 +319,36 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
     }
   } else {
     // ---------------------------------------------------------- softmax --
-    const int t = (warp - 2) >> 2;   // query tile of this warpgroup
-    const int q = warp & 3;          // TMEM lane quarter
-    const int row = q * 32 + lane;   // query row within the tile
+    // SPLIT warps share each TMEM lane quarter of a tile: warp half h owns
+    // the keys [h*KB/SPLIT, (h+1)*KB/SPLIT) of every block (and O columns
+    // [h*DH/SPLIT, ...)); the two halves exchange the row extremum once per
+    // block and the row sum once at the end.
+    constexpr int SPLIT = A::SPLIT;
+    const int e = warp - 2;
+    const int t = e / (4 * SPLIT);           // query tile
+    const int h = (e % (4 * SPLIT)) / 4;     // key half
+    const int q = warp & 3;                  // TMEM lane quarter
+    const int row = q * 32 + lane;           // query row within the tile
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     const uint32_t tS = tmem + A::tm_s(t) + lane_off;
     const uint32_t tO = tmem + A::tm_o(t) + lane_off;
-    constexpr int NCH = KB / 32;     // 32-key chunks per block
+    constexpr int NCH = KB / 32 / SPLIT;     // 32-key chunks of this half per block
+    const int ch0 = h * NCH;                 // first chunk of this half
+    uint2* xbase = reinterpret_cast<uint2*>(smem + A::OFF_X);
+    auto xslot = [&](int par, int half) { return xbase + ((par * NT + t) * SPLIT + half) * 128 + row; };
     float m2 = -INFINITY;  // running max, log2 units
-    float l = 0.f;         // running sum of weights
+    float l = 0.f;         // running sum of this half's weights
     bool ok = true;
     for (int j = 0; j < nb; ++j) {
       if (!mbar_wait(&bars->s_full[t], j & 1, abort_flag, args.timeout_ns)) {
-        if (lane == 0) record_error(args.err, 1, kWhere + 2, j, t * 4 + q);
+        if (lane == 0) record_error(args.err, 1, kWhere + 2, j, t * 8 + h * 4 + q);
         bars->abort_flag = 1;
         ok = false;
         break;
       }
       tc_fence_after();
-      // pass 1: row extremum of the raw scores over the block (max, or min for
-      // a negative scale); four chunks are loaded before each wait
+      // pass 1: row extremum of this half's raw scores (max, or min for a
+      // negative scale), then the other half's through shared memory
       const float c = args.scale_log2;  // scale * log2(e)
       const int kvalid = args.Nk - j * KB;  // keys of this block that exist
       float ext = c >= 0.f ? -INFINITY : INFINITY;
@@ -318,18 +365,23 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
         }
       };
 #pragma unroll
-      for (int g = 0; g < NCH; g += 4) {
-        uint32_t ra[32], rb[32], rc[32], rd[32];
-        tmem_ld_32x32b_x32(tS + (g + 0) * 32, ra);
-        tmem_ld_32x32b_x32(tS + (g + 1) * 32, rb);
-        tmem_ld_32x32b_x32(tS + (g + 2) * 32, rc);
-        tmem_ld_32x32b_x32(tS + (g + 3) * 32, rd);
+      for (int g = 0; g < NCH; g += 2) {
+        uint32_t ra[32], rb[32];
+        tmem_ld_32x32b_x32(tS + (ch0 + g) * 32, ra);
+        tmem_ld_32x32b_x32(tS + (ch0 + g + 1) * 32, rb);
         tmem_wait_ld();
-        scan(ra, (g + 0) * 32);
-        scan(rb, (g + 1) * 32);
-        scan(rc, (g + 2) * 32);
-        scan(rd, (g + 3) * 32);
+        scan(ra, (ch0 + g) * 32);
+        scan(rb, (ch0 + g + 1) * 32);
       }
+      float other;
+      if (!exchange(xslot(j & 1, h), xslot(j & 1, h ^ 1), ext, static_cast<uint32_t>(j + 1),
+                    &other, abort_flag, args.timeout_ns)) {
+        if (lane == 0) record_error(args.err, 1, kWhere + 6, j, t * 8 + h * 4 + q);
+        bars->abort_flag = 1;
+        ok = false;
+        break;
+      }
+      ext = c >= 0.f ? fmaxf(ext, other) : fminf(ext, other);
       const float m_new = fmaxf(m2, ext * c);
       const float eta = ex2_approx(m2 - m_new);  // 0 on the first block
       // pass 2: p = 2^(s*c - m) with one FFMA; each chunk of 32 keys is
@@ -359,15 +411,15 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
       };
       {
         uint32_t r0[32], r1[32];
-        tmem_ld_32x32b_x32(tS, r0);
+        tmem_ld_32x32b_x32(tS + ch0 * 32, r0);
         tmem_wait_ld();
 #pragma unroll
         for (int cc = 0; cc < NCH; cc += 2) {
-          tmem_ld_32x32b_x32(tS + (cc + 1) * 32, r1);
-          expo(r0, cc);
+          tmem_ld_32x32b_x32(tS + (ch0 + cc + 1) * 32, r1);
+          expo(r0, ch0 + cc);
           tmem_wait_ld();
-          if (cc + 2 < NCH) tmem_ld_32x32b_x32(tS + (cc + 2) * 32, r0);
-          expo(r1, cc + 1);
+          if (cc + 2 < NCH) tmem_ld_32x32b_x32(tS + (ch0 + cc + 2) * 32, r0);
+          expo(r1, ch0 + cc + 1);
           tmem_wait_ld();
         }
       }
@@ -376,15 +428,17 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
       if (j > 0) {
         // the previous PV of this tile has finished: O is stable
         if (!mbar_wait(&bars->pv_done[t], (j - 1) & 1, abort_flag, args.timeout_ns)) {
-          if (lane == 0) record_error(args.err, 1, kWhere + 3, j, t * 4 + q);
+          if (lane == 0) record_error(args.err, 1, kWhere + 3, j, t * 8 + h * 4 + q);
           bars->abort_flag = 1;
           ok = false;
           break;
         }
         tc_fence_after();
         if (__any_sync(0xffffffffu, eta != 1.0f)) {
+          // this half's O columns
+          constexpr int OCH = DH / 32 / SPLIT;
 #pragma unroll 1
-          for (int cc = 0; cc < DH / 32; cc += 2) {
+          for (int cc = h * OCH; cc < (h + 1) * OCH; cc += 2) {
             uint32_t ra[32], rb[32];
             tmem_ld_32x32b_x32(tO + cc * 32, ra);
             tmem_ld_32x32b_x32(tO + cc * 32 + 32, rb);
@@ -404,16 +458,25 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
       mbar_arrive(&bars->p_full[t]);
     }
     if (ok && nb > 0) {
+      float l_other = 0.f;
       if (!mbar_wait(&bars->pv_done[t], (nb - 1) & 1, abort_flag, args.timeout_ns)) {
-        if (lane == 0) record_error(args.err, 1, kWhere + 3, nb, t * 4 + q);
+        if (lane == 0) record_error(args.err, 1, kWhere + 3, nb, t * 8 + h * 4 + q);
+        bars->abort_flag = 1;
+      } else if (!exchange(xslot(nb & 1, h), xslot(nb & 1, h ^ 1), l,
+                           static_cast<uint32_t>(nb + 1), &l_other, abort_flag,
+                           args.timeout_ns)) {
+        if (lane == 0) record_error(args.err, 1, kWhere + 6, nb, t * 8 + h * 4 + q);
         bars->abort_flag = 1;
       } else {
+        // both halves' sums, added in the same order in both warps
+        const float lt = h == 0 ? l + l_other : l_other + l;
         tc_fence_after();
         const int tok = q0 + t * BQ + row;
         uint16_t* orow =
             args.O + head * args.o_ld_head + static_cast<int64_t>(tok) * args.o_ld_token;
+        constexpr int OCH = DH / 32 / SPLIT;
 #pragma unroll 1
-        for (int cc = 0; cc < DH / 32; ++cc) {
+        for (int cc = h * OCH; cc < (h + 1) * OCH; ++cc) {
           uint32_t r[32];
           tmem_ld_32x32b_x32(tO + cc * 32, r);
           tmem_wait_ld();
@@ -423,7 +486,7 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
             for (int u = 0; u < 4; ++u) {
               float v[8];
 #pragma unroll
-              for (int i = 0; i < 8; ++i) v[i] = __fdiv_rn(__uint_as_float(r[8 * u + i]), l);
+              for (int i = 0; i < 8; ++i) v[i] = __fdiv_rn(__uint_as_float(r[8 * u + i]), lt);
               o4[u] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
                                  pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
             }
