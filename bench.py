@@ -348,6 +348,72 @@ class AttentionWorkload(Workload):
         return self.Q, self.O
 
 
+def stack_sweep(args):
+    """The stack configuration's transport control: one 48-block stack (weights
+    in pinned host memory, plus a device-resident copy) run streamed through
+    arenas of several sizes and resident; step times and a bitwise
+    comparison of the outputs."""
+    import torch
+    from weight_streamed_bf16_gb300 import build, psi
+    from weight_streamed_bf16_gb300.block import BlockRunner
+    from weight_streamed_bf16_gb300.torch_io import Arena
+    build.build()
+    psi.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peaks = load_peaks()
+    link_gbs = h2d_probe(torch, dev)
+    t0 = time.perf_counter()
+    wl = BlockWorkload(torch, dev, args.blocks, 80, resident=True)
+    setup_s = time.perf_counter() - t0
+    wl.arena.close()
+    runs = []
+    ref = None
+    for mib, flags in [(32, 0), (80, 0), (256, 0), (80, psi.PSI_RESIDENT)]:
+        arena = Arena(wl.shape.page_bytes, mib * MiB // wl.shape.page_bytes, device=dev)
+        runner = BlockRunner(wl.shape, arena, device=dev)
+        Y = torch.empty_like(wl.X)
+        tmp = torch.empty_like(wl.X)
+        with torch.cuda.stream(arena.compute):
+            runner.stack(wl.X, wl.blocks, Y, tmp, flags)           # warm-up
+        arena.sync(600000)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        with torch.cuda.stream(arena.compute):
+            for a, b in ev:
+                a.record(arena.compute)
+                runner.stack(wl.X, wl.blocks, Y, tmp, flags)
+                b.record(arena.compute)
+        arena.sync(600000)
+        ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+        st = arena.stats()
+        same = None
+        if ref is None:
+            ref = Y.clone()
+        else:
+            same = bool(torch.equal(ref.view(torch.int16), Y.view(torch.int16)))
+        runs.append({"arena_mib": mib, "slots": arena.slots,
+                     "mode": "resident" if flags else "streamed",
+                     "ms_per_stack": ms, "tflops": wl.flops / (ms * 1e-3) / 1e12,
+                     "ingest_gbs": (0 if flags else len(wl.blocks) * psi_weight_bytes()) /
+                                   (ms * 1e-3) / 1e9,
+                     "bitwise_equal_to_first": same, "pages": st["pages_streamed"]})
+        arena.close()
+        del runner, Y, tmp
+    print(json.dumps({
+        "metric": METRIC, "workload": f"stack of {args.blocks} synthetic blocks, transport control",
+        "steps": args.steps, "unit": "TFLOP/s", "runs": runs, "setup_s": setup_s,
+        "link_probe_gbs": link_gbs, "peaks": peaks,
+        "all_bitwise_equal": all(r["bitwise_equal_to_first"] in (None, True) for r in runs),
+    }))
+    return 0
+
+
+def psi_weight_bytes():
+    import psi_synth
+    return psi_synth.BLOCK.weight_bytes
+
+
 def make_workload(torch, dev, args):
     if args.workload == "block":
         return BlockWorkload(torch, dev, 1, args.arena_mib, args.resident)
@@ -491,6 +557,8 @@ def main():
     ap.add_argument("--key-block", type=int, default=None,
                     help="attention workload: keys per online-softmax block (default 256)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="stack workload: arena sweep 32/80/256 MiB + resident, bitwise control")
     ap.add_argument("--cpu-rows", type=int, default=512)
     args = ap.parse_args()
     if args.warmup < 3:
@@ -498,6 +566,8 @@ def main():
 
     if args.impl == "reference":
         return reference_arm(args)
+    if args.sweep:
+        return stack_sweep(args)
 
     import torch
     rank, world, local = env_rank()

@@ -54,9 +54,9 @@ struct AShape {
   static constexpr int OFF_V = OFF_K + 2 * 2 * TILE64;
   static constexpr int OFF_BAR = OFF_V + 2 * 2 * TILE64;
   // row-extremum and row-sum exchange between the two key halves of a row:
-  // [2 parities][NT tiles][SPLIT halves][128 rows] x (value, sequence)
+  // [2 parities][NT tiles][SPLIT halves][128 rows] floats
   static constexpr int OFF_X = OFF_BAR + 256;
-  static constexpr int X_BYTES = 2 * NT * SPLIT * 128 * 8;
+  static constexpr int X_BYTES = 2 * NT * SPLIT * 128 * 4;
   static constexpr int SMEM_BYTES = OFF_X + X_BYTES + 1024;
   static constexpr uint32_t TILE_COLS = KB + 128;
   static constexpr uint32_t TM_COLS = 512;
@@ -70,6 +70,7 @@ struct __align__(8) ABars {
   uint64_t k_full[2], k_empty[2];
   uint64_t v_full[2], v_empty[2];
   uint64_t s_full[2], p_full[2], pv_done[2];
+  uint64_t xbar[2][4];  // per tile and lane quarter: the two key halves met
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -90,31 +91,16 @@ __device__ __forceinline__ void record_error(DevError* e, int code, int where, i
   }
 }
 
-// Publish a row value for the partner warp and read the partner's, through
-// a (value, sequence) pair in shared memory; the wait for the partner is
-// bounded.  Returns false on timeout or abort.
-__device__ __forceinline__ bool exchange(uint2* mine, const uint2* theirs, float v,
-                                         uint32_t seq, float* out, volatile int* abort,
-                                         uint64_t limit_ns) {
-  // one 8-byte access: value and sequence are seen together
-  asm volatile("st.volatile.shared.v2.u32 [%0], {%1, %2};" ::"r"(smem_u32(mine)),
-               "r"(__float_as_uint(v)), "r"(seq)
-               : "memory");
-  uint32_t val, s;
-  const uint32_t a = smem_u32(theirs);
-  asm volatile("ld.volatile.shared.v2.u32 {%0, %1}, [%2];" : "=r"(val), "=r"(s) : "r"(a) : "memory");
-  if (s != seq) {
-    const uint64_t t0 = globaltimer_ns();
-    while (true) {
-      asm volatile("ld.volatile.shared.v2.u32 {%0, %1}, [%2];"
-                   : "=r"(val), "=r"(s)
-                   : "r"(a)
-                   : "memory");
-      if (s == seq) break;
-      if (*abort || globaltimer_ns() - t0 > limit_ns) return false;
-    }
-  }
-  *out = __uint_as_float(val);
+// Publish a row value for the partner warp (same rows, other key half) and
+// read the partner's: both warps write their slot, arrive on the pair's
+// mbarrier and wait (bounded) for the phase.  Returns false on timeout.
+__device__ __forceinline__ bool exchange(float* mine, const float* theirs, float v,
+                                         uint64_t* bar, uint32_t parity, float* out,
+                                         volatile int* abort, uint64_t limit_ns) {
+  *mine = v;
+  mbar_arrive(bar);
+  if (!mbar_wait(bar, parity, abort, limit_ns)) return false;
+  *out = *theirs;
   return true;
 }
 
@@ -152,14 +138,13 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
       mbar_init(&bars->s_full[t], 1);
       mbar_init(&bars->p_full[t], 128 * A::SPLIT);
       mbar_init(&bars->pv_done[t], 1);
+      for (int qq = 0; qq < 4; ++qq) mbar_init(&bars->xbar[t][qq], 32 * A::SPLIT);
     }
     mbar_init(&bars->drain, 1);
     bars->abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmQ);
   }
-  for (int i = threadIdx.x; i < A::X_BYTES / 8; i += blockDim.x)
-    reinterpret_cast<uint2*>(smem + A::OFF_X)[i] = make_uint2(0u, 0u);
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
@@ -334,7 +319,8 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
     const uint32_t tO = tmem + A::tm_o(t) + lane_off;
     constexpr int NCH = KB / 32 / SPLIT;     // 32-key chunks of this half per block
     const int ch0 = h * NCH;                 // first chunk of this half
-    uint2* xbase = reinterpret_cast<uint2*>(smem + A::OFF_X);
+    float* xbase = reinterpret_cast<float*>(smem + A::OFF_X);
+    uint64_t* xb = &bars->xbar[t][q];
     auto xslot = [&](int par, int half) { return xbase + ((par * NT + t) * SPLIT + half) * 128 + row; };
     float m2 = -INFINITY;  // running max, log2 units
     float l = 0.f;         // running sum of this half's weights
@@ -364,18 +350,25 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
               ext = c >= 0.f ? fmaxf(ext, __uint_as_float(r[i])) : fminf(ext, __uint_as_float(r[i]));
         }
       };
+      // the half's first two chunks stay in registers for pass 2
+      uint32_t ra[32], rb[32];
+      tmem_ld_32x32b_x32(tS + ch0 * 32, ra);
+      tmem_ld_32x32b_x32(tS + (ch0 + 1) * 32, rb);
+      tmem_wait_ld();
+      scan(ra, ch0 * 32);
+      scan(rb, (ch0 + 1) * 32);
 #pragma unroll
-      for (int g = 0; g < NCH; g += 2) {
-        uint32_t ra[32], rb[32];
-        tmem_ld_32x32b_x32(tS + (ch0 + g) * 32, ra);
-        tmem_ld_32x32b_x32(tS + (ch0 + g + 1) * 32, rb);
+      for (int g = 2; g < NCH; g += 2) {
+        uint32_t rc[32], rd[32];
+        tmem_ld_32x32b_x32(tS + (ch0 + g) * 32, rc);
+        tmem_ld_32x32b_x32(tS + (ch0 + g + 1) * 32, rd);
         tmem_wait_ld();
-        scan(ra, (ch0 + g) * 32);
-        scan(rb, (ch0 + g + 1) * 32);
+        scan(rc, (ch0 + g) * 32);
+        scan(rd, (ch0 + g + 1) * 32);
       }
       float other;
-      if (!exchange(xslot(j & 1, h), xslot(j & 1, h ^ 1), ext, static_cast<uint32_t>(j + 1),
-                    &other, abort_flag, args.timeout_ns)) {
+      if (!exchange(xslot(j & 1, h), xslot(j & 1, h ^ 1), ext, xb, j & 1, &other, abort_flag,
+                    args.timeout_ns)) {
         if (lane == 0) record_error(args.err, 1, kWhere + 6, j, t * 8 + h * 4 + q);
         bars->abort_flag = 1;
         ok = false;
@@ -409,12 +402,15 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
         tmem_st_32x32b_x16(tS + cc * 32, hi);
         tmem_st_32x32b_x16(tS + cc * 32 + 16, lo);
       };
-      {
+      expo(ra, ch0);
+      expo(rb, ch0 + 1);
+      if (NCH > 2) {
+        // further chunks (256-key blocks): reloaded, next load in flight
         uint32_t r0[32], r1[32];
-        tmem_ld_32x32b_x32(tS + ch0 * 32, r0);
+        tmem_ld_32x32b_x32(tS + (ch0 + 2) * 32, r0);
         tmem_wait_ld();
 #pragma unroll
-        for (int cc = 0; cc < NCH; cc += 2) {
+        for (int cc = 2; cc < NCH; cc += 2) {
           tmem_ld_32x32b_x32(tS + (ch0 + cc + 1) * 32, r1);
           expo(r0, ch0 + cc);
           tmem_wait_ld();
@@ -462,9 +458,8 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
       if (!mbar_wait(&bars->pv_done[t], (nb - 1) & 1, abort_flag, args.timeout_ns)) {
         if (lane == 0) record_error(args.err, 1, kWhere + 3, nb, t * 8 + h * 4 + q);
         bars->abort_flag = 1;
-      } else if (!exchange(xslot(nb & 1, h), xslot(nb & 1, h ^ 1), l,
-                           static_cast<uint32_t>(nb + 1), &l_other, abort_flag,
-                           args.timeout_ns)) {
+      } else if (!exchange(xslot(nb & 1, h), xslot(nb & 1, h ^ 1), l, xb, nb & 1, &l_other,
+                           abort_flag, args.timeout_ns)) {
         if (lane == 0) record_error(args.err, 1, kWhere + 6, nb, t * 8 + h * 4 + q);
         bars->abort_flag = 1;
       } else {
