@@ -100,8 +100,8 @@ __device__ __forceinline__ void load_acc32(const GemmArgs& a, int row, int col0,
 // their outputs are clipped by the tensor store).  wq[] holds the FP32
 // workspace values of a full chunk, loaded ahead.  The results go to the
 // warp's staging buffer `stg` (row = lane) in the layout of the tensor
-// store: FP32 rows of 128 B with 128-byte swizzle, or BF16 rows of 64 B with
-// 64-byte swizzle.
+// store (BF16 rows of 64 B with 64-byte swizzle); FP32 results are left in
+// v[] for the caller.
 __device__ __forceinline__ void epilogue_row32(const GemmArgs& a, int row, bool row_ok,
                                                int col0, int ncol, float (&v)[32],
                                                const float4 (&wq)[8], uint8_t* stg, int lane) {
@@ -123,12 +123,7 @@ __device__ __forceinline__ void epilogue_row32(const GemmArgs& a, int row, bool 
           if (j < ncol) v[j] = p[j] + v[j];
       }
     }
-    uint8_t* rowp = stg + lane * 128;
-#pragma unroll
-    for (int c = 0; c < 8; ++c)
-      *reinterpret_cast<float4*>(rowp + ((c ^ (lane & 7)) << 4)) =
-          make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-    return;
+    return;  // FP32 results stay in v; the caller stages them per 16 columns
   }
   // BF16 outputs: bias (+ FP32 accumulator) (+ GELU) (+ residual)
   float bia[32];
@@ -395,27 +390,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_32x32b_x32(tbase + c * 32, r);
         tmem_wait_ld();
         if (col0 < args.N && m0 + q * 32 < args.M) {  // warp-uniform
-          uint8_t* stg = f32 ? stg_base : stg_base + (nstore & 1) * 2048;
-          // the store that last read this buffer has finished reading it
-          if (lane == 0) {
-            if (f32)
-              bulk_wait_read<0>();
-            else
-              bulk_wait_read<1>();
-          }
-          __syncwarp();
+          // The warp's 4 KiB holds two 2 KiB buffers used alternately: a BF16
+          // chunk (32 rows x 64 B) or an FP32 half chunk (32 rows x 16
+          // columns x 4 B) per buffer, so one tensor store drains while the
+          // next buffer is written.
           float v[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
           const int ncol = min(32, args.N - col0);
-          epilogue_row32(args, row, row_ok, col0, ncol, v, cur, stg, lane);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&tmOut, stg, col0, m0 + q * 32);
-            bulk_commit();
+          const int nparts = f32 ? 2 : 1;
+#pragma unroll
+          for (int part = 0; part < 2; ++part) {
+            if (part >= nparts) break;
+            uint8_t* stg = stg_base + (nstore & 1) * 2048;
+            if (lane == 0) bulk_wait_read<1>();  // this buffer's last store has read it
+            __syncwarp();
+            if (!f32) {
+              epilogue_row32(args, row, row_ok, col0, ncol, v, cur, stg, lane);
+            } else {
+              if (part == 0) epilogue_row32(args, row, row_ok, col0, ncol, v, cur, stg, lane);
+              uint8_t* rowp = stg + lane * 64;
+#pragma unroll
+              for (int k4 = 0; k4 < 4; ++k4) {
+                const int b = 16 * part + 4 * k4;
+                *reinterpret_cast<float4*>(rowp + ((k4 ^ ((lane >> 1) & 3)) << 4)) =
+                    make_float4(v[b], v[b + 1], v[b + 2], v[b + 3]);
+              }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              if (col0 + 16 * part < args.N)
+                tma_store_2d(&tmOut, stg, col0 + 16 * part, m0 + q * 32);
+              bulk_commit();
+            }
+            ++nstore;
           }
-          ++nstore;
         }
       }
       tc_fence_before();
@@ -490,7 +500,7 @@ psi_status launch_page_gemm(const void* X, int64_t ldx, const void* P, int64_t l
   // the output tensor the epilogue stores into, in 32 x 32 boxes
   CUtensorMap to;
   if (a.epi == EPI_ACC_STORE || a.epi == EPI_ACC_ADD)
-    st = make_tmap_2d_ex(&to, a.accf, a.M, a.N, a.ldacc, 32, 32, 4, 128);
+    st = make_tmap_2d_ex(&to, a.accf, a.M, a.N, a.ldacc, 32, 16, 4, 64);
   else
     st = make_tmap_2d_ex(&to, a.out, a.M, a.N, a.ldo, 32, 32, 2, 64);
   if (st != PSI_OK) return st;
