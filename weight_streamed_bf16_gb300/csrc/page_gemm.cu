@@ -22,16 +22,12 @@
 //               tile's epilogue
 // Every wait is bounded; on expiry the kernel records an error, drains its
 // own copies and MMAs, frees TMEM and returns.
-#include "internal.h"
-#include "ptx.cuh"
+#include "gemm_epilogue.cuh"
 
 namespace psi {
 namespace {
 
-constexpr int BM = 128;
-constexpr int BK = 64;  // one 128-byte swizzle row of BF16
 constexpr int kThreads = 320;  // producer, MMA, 8 epilogue warps
-constexpr int kEpiWarps = 8;
 
 template <int BN>
 struct Cfg {
@@ -57,146 +53,6 @@ struct __align__(8) Bars {
   uint32_t tmem_base;
   int abort_flag;
 };
-
-__device__ __forceinline__ void record_error(DevError* e, int code, int where, int i0, int i1) {
-  if (atomicCAS(&e->code, 0, code) == 0) {
-    e->where = where;
-    e->info0 = i0;
-    e->info1 = i1;
-  }
-}
-
-__device__ __forceinline__ float gelu_tanh(float x) {
-  // tanh form of GELU: x/2 (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3)))
-  const float k0 = 0.7978845608028654f;
-  const float k1 = 0.044715f;
-  const float u = k0 * fmaf(k1 * x * x, x, x);
-  return 0.5f * x * (1.0f + tanhf(u));
-}
-
-__device__ __forceinline__ float round_bf16_f(float x) {
-  return bf16_lo(pack_bf16x2(x, 0.f));
-}
-
-__device__ __forceinline__ bool epi_reads_acc(int epi) {
-  return epi == EPI_ACC_ADD || epi == EPI_ACC_FINAL;
-}
-__device__ __forceinline__ bool epi_writes_f32(int epi) {
-  return epi == EPI_ACC_STORE || epi == EPI_ACC_ADD;
-}
-
-// The 32 FP32 accumulator values of one row chunk (full chunks only).
-__device__ __forceinline__ void load_acc32(const GemmArgs& a, int row, int col0,
-                                           float4 (&q)[8]) {
-  const float4* p4 =
-      reinterpret_cast<const float4*>(a.accf + static_cast<int64_t>(row) * a.ldacc + col0);
-#pragma unroll
-  for (int j = 0; j < 8; ++j) q[j] = p4[j];
-}
-
-// Fused epilogue of 32 consecutive columns of one row.  v[] holds the FP32
-// MMA results; col0 is the first column, ncol <= 32 of them exist, row_ok
-// says whether the row exists (inputs of missing rows/columns are not read;
-// their outputs are clipped by the tensor store).  wq[] holds the FP32
-// workspace values of a full chunk, loaded ahead.  The results go to the
-// warp's staging buffer `stg` (row = lane) in the layout of the tensor
-// store (BF16 rows of 64 B with 64-byte swizzle); FP32 results are left in
-// v[] for the caller.
-__device__ __forceinline__ void epilogue_row32(const GemmArgs& a, int row, bool row_ok,
-                                               int col0, int ncol, float (&v)[32],
-                                               const float4 (&wq)[8], uint8_t* stg, int lane) {
-  const bool full = (ncol == 32) && row_ok;
-  if (epi_writes_f32(a.epi)) {
-    if (a.epi == EPI_ACC_ADD) {
-      if (full) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          v[4 * j] = wq[j].x + v[4 * j];
-          v[4 * j + 1] = wq[j].y + v[4 * j + 1];
-          v[4 * j + 2] = wq[j].z + v[4 * j + 2];
-          v[4 * j + 3] = wq[j].w + v[4 * j + 3];
-        }
-      } else if (row_ok) {
-        const float* p = a.accf + static_cast<int64_t>(row) * a.ldacc + col0;
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (j < ncol) v[j] = p[j] + v[j];
-      }
-    }
-    return;  // FP32 results stay in v; the caller stages them per 16 columns
-  }
-  // BF16 outputs: bias (+ FP32 accumulator) (+ GELU) (+ residual)
-  float bia[32];
-  if (col0 + 32 <= a.N) {
-    const uint4* b4 = reinterpret_cast<const uint4*>(a.bias + col0);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint4 q = __ldg(b4 + j);
-      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        bia[8 * j + 2 * t] = bf16_lo(w[t]);
-        bia[8 * j + 2 * t + 1] = bf16_hi(w[t]);
-      }
-    }
-  } else {
-#pragma unroll
-    for (int j = 0; j < 32; ++j)
-      bia[j] = j < ncol ? __uint_as_float(static_cast<uint32_t>(a.bias[col0 + j]) << 16) : 0.f;
-  }
-  if (a.epi == EPI_ACC_FINAL) {
-    if (full) {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        v[4 * j] = wq[j].x + v[4 * j];
-        v[4 * j + 1] = wq[j].y + v[4 * j + 1];
-        v[4 * j + 2] = wq[j].z + v[4 * j + 2];
-        v[4 * j + 3] = wq[j].w + v[4 * j + 3];
-      }
-    } else if (row_ok) {
-      const float* p = a.accf + static_cast<int64_t>(row) * a.ldacc + col0;
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (j < ncol) v[j] = p[j] + v[j];
-    }
-  }
-#pragma unroll
-  for (int j = 0; j < 32; ++j) v[j] = v[j] + bia[j];
-  if (a.epi == EPI_GELU) {
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      float t = v[j];
-      if (a.pregelu) t = round_bf16_f(t);
-      v[j] = gelu_tanh(t);
-    }
-  }
-  if (a.resid && row_ok) {
-    const uint16_t* res = a.resid + static_cast<int64_t>(row) * a.ldo + col0;
-    if (ncol == 32) {
-      const uint4* r4 = reinterpret_cast<const uint4*>(res);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint4 q = r4[j];
-        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          v[8 * j + 2 * t] += bf16_lo(w[t]);
-          v[8 * j + 2 * t + 1] += bf16_hi(w[t]);
-        }
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (j < ncol) v[j] += __uint_as_float(static_cast<uint32_t>(res[j]) << 16);
-    }
-  }
-  uint8_t* rowp = stg + lane * 64;
-#pragma unroll
-  for (int c = 0; c < 4; ++c)
-    *reinterpret_cast<uint4*>(rowp + ((c ^ ((lane >> 1) & 3)) << 4)) =
-        make_uint4(pack_bf16x2(v[8 * c + 0], v[8 * c + 1]), pack_bf16x2(v[8 * c + 2], v[8 * c + 3]),
-                   pack_bf16x2(v[8 * c + 4], v[8 * c + 5]), pack_bf16x2(v[8 * c + 6], v[8 * c + 7]));
-}
 
 template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -350,7 +206,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // --------------------------------------------------------- epilogue --
     const int q = warp & 3;                 // TMEM lane quarter this warp may access
     const int half = (warp - 2) >> 2;       // column half of the tile
-    constexpr int CH = BN / 64;             // 32-column chunks per half
     const bool pre = epi_reads_acc(args.epi);
     const bool f32 = epi_writes_f32(args.epi);
     // staging: 4 KiB per warp; FP32 chunks use all of it, BF16 chunks
@@ -377,57 +232,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t tbase = tmem + static_cast<uint32_t>(acc * BN + half * (BN / 2)) +
                              (static_cast<uint32_t>(q * 32) << 16);
-#pragma unroll 1
-      for (int c = 0; c < CH; ++c) {
-        float4 cur[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) cur[j] = nxt[j];
-        const int col0 = n0 + c * 32;
-        if (pre && c + 1 < CH && row_ok && col0 + 64 <= args.N)
-          load_acc32(args, row, col0 + 32, nxt);
-        __syncwarp();
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(tbase + c * 32, r);
-        tmem_wait_ld();
-        if (col0 < args.N && m0 + q * 32 < args.M) {  // warp-uniform
-          // The warp's 4 KiB holds two 2 KiB buffers used alternately: a BF16
-          // chunk (32 rows x 64 B) or an FP32 half chunk (32 rows x 16
-          // columns x 4 B) per buffer, so one tensor store drains while the
-          // next buffer is written.
-          float v[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-          const int ncol = min(32, args.N - col0);
-          const int nparts = f32 ? 2 : 1;
-#pragma unroll
-          for (int part = 0; part < 2; ++part) {
-            if (part >= nparts) break;
-            uint8_t* stg = stg_base + (nstore & 1) * 2048;
-            if (lane == 0) bulk_wait_read<1>();  // this buffer's last store has read it
-            __syncwarp();
-            if (!f32) {
-              epilogue_row32(args, row, row_ok, col0, ncol, v, cur, stg, lane);
-            } else {
-              if (part == 0) epilogue_row32(args, row, row_ok, col0, ncol, v, cur, stg, lane);
-              uint8_t* rowp = stg + lane * 64;
-#pragma unroll
-              for (int k4 = 0; k4 < 4; ++k4) {
-                const int b = 16 * part + 4 * k4;
-                *reinterpret_cast<float4*>(rowp + ((k4 ^ ((lane >> 1) & 3)) << 4)) =
-                    make_float4(v[b], v[b + 1], v[b + 2], v[b + 3]);
-              }
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              if (col0 + 16 * part < args.N)
-                tma_store_2d(&tmOut, stg, col0 + 16 * part, m0 + q * 32);
-              bulk_commit();
-            }
-            ++nstore;
-          }
-        }
-      }
+      epilogue_tile<BN>(args, &tmOut, tbase, m0, n0, q, row, row_ok, lane, pre, f32, stg_base,
+                        nstore, nxt);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->tempty[acc]);
@@ -471,10 +277,19 @@ psi_status launch_bn(const CUtensorMap& tx, const CUtensorMap& tp, const CUtenso
 
 int gemm_bn_for(int64_t N) { return N > 128 ? 256 : (N > 64 ? 128 : 64); }
 
+// page_gemm_pair.cu
+bool gemm_use_pair(int64_t M, int64_t N);
+psi_status launch_page_gemm_pair(const CUtensorMap& tx, const CUtensorMap& tp,
+                                 const CUtensorMap& tp2, const CUtensorMap& to, const GemmArgs& a,
+                                 cudaStream_t s);
+
 psi_status launch_page_gemm(const void* X, int64_t ldx, const void* P, int64_t ldp,
                             const GemmArgs& a, cudaStream_t stream, const void* P2) {
   if (a.M <= 0 || a.N <= 0 || a.K <= 0) return PSI_OK;
-  const int bn = gemm_bn_for(a.N);
+  // tiles of 256 x 256 on CTA pairs where the shape fills them, else one CTA
+  // per 128 x BN tile; the choice depends on the shape only
+  const bool pair = gemm_use_pair(a.M, a.N);
+  const int bn = pair ? 128 : gemm_bn_for(a.N);  // page rows per CTA and box
   CUtensorMap tx, tp, tp2;
   psi_status st = make_tmap_2d(&tx, X, a.M, a.K, ldx, BM, BK);
   if (st != PSI_OK) return st;
@@ -487,7 +302,7 @@ psi_status launch_page_gemm(const void* X, int64_t ldx, const void* P, int64_t l
     if (st != PSI_OK) return st;
     st = make_tmap_2d(&tp2, P2, a.N, a.K - k1, ldp, bn, BK);
   } else if (a.n_split > 0) {
-    if (!P2 || a.n_split >= a.N || a.n_split % bn)
+    if (!P2 || a.n_split >= a.N || a.n_split % (pair ? 256 : bn))
       return set_error(PSI_ERR_INVALID_ARG, "page_gemm: bad N split");
     st = make_tmap_2d(&tp, P, a.n_split, a.K, ldp, bn, BK);
     if (st != PSI_OK) return st;
@@ -504,6 +319,7 @@ psi_status launch_page_gemm(const void* X, int64_t ldx, const void* P, int64_t l
   else
     st = make_tmap_2d_ex(&to, a.out, a.M, a.N, a.ldo, 32, 32, 2, 64);
   if (st != PSI_OK) return st;
+  if (pair) return launch_page_gemm_pair(tx, tp, tp2, to, a, stream);
   switch (bn) {
     case 256: return launch_bn<256>(tx, tp, tp2, to, a, stream);
     case 128: return launch_bn<128>(tx, tp, tp2, to, a, stream);
