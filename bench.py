@@ -674,7 +674,7 @@ def main():
     out_bytes = Yh.numel() * Yh.element_size()
 
     # ------------------------------------------------ roofline (page GEMM) --
-    digest = source_digest("page_gemm.cu", "ptx.cuh")
+    digest = source_digest("page_gemm.cu", "page_gemm_pair.cu", "gemm_epilogue.cuh", "ptx.cuh")
     roof = None
     peak_t = peaks["bf16_tflops"] if wl.timed_alone else peaks["bf16_tflops_sustained"]
     if st and st["timed_gemms"]:
