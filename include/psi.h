@@ -58,6 +58,16 @@ typedef enum {
                                           pre-activation before GELU, the rounding
                                           order of the paper's native prototype
                                           (section III-A) */
+#define PSI_BIAS_AFTER_BF16       0x8u /* the paper's baseline variant (section
+                                          III-A): the FP32 matrix product is
+                                          rounded to BF16 before the bias (and
+                                          residual) is added, in every epilogue
+                                          that adds a bias */
+#define PSI_ATTN_BF16_WEIGHTS     0x10u /* attention: the numerator uses the
+                                          exponential weights rounded to BF16
+                                          (p_hi only), the baseline variant of
+                                          section III-A; the denominator keeps
+                                          the FP32 weights */
 
 typedef struct psi_arena psi_arena;
 

@@ -112,3 +112,32 @@ def test_attention_rejects_unsupported():
     with pytest.raises(psi.PsiError) as e:
         run_attention(Q.cuda(), K.cuda(), V.cuda(), 0.1, key_block=64)
     assert e.value.status == psi.PSI_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("key_block", [128, 256])
+def test_attention_bf16_numerator_weights(key_block):
+    """The baseline variant (section III-A): numerator weights rounded to
+    BF16, graded against the oracle's online recurrence over the same key
+    blocks; its error against exact attention is far above the FP32-weight
+    kernel's."""
+    Q, K, V = _qkv(2, 256, 1000, 9)
+    sc = 1 / math.sqrt(128)
+    s = torch.cuda.current_stream()
+    O = torch.empty(2, 256, 128, dtype=torch.bfloat16, device="cuda")
+    from weight_streamed_bf16_gb300.torch_io import heads_view
+    Qd, Kd, Vd = Q.cuda(), K.cuda(), V.cuda()
+    psi.psi_attn_partitioned(heads_view(Qd), heads_view(Kd), heads_view(Vd), heads_view(O), 2,
+                             256, 1000, 128, sc, key_block, s.cuda_stream,
+                             psi.PSI_ATTN_BF16_WEIGHTS)
+    psi.psi_stream_wait(s.cuda_stream)
+    Of = O.cpu()
+    for h in range(2):
+        res = ops.attention_bf16_weights(f64(Q)[h], f64(K)[h], f64(V)[h], sc, key_block)
+        check(Of[h], res, what=f"bf16 weights head {h}")
+    # against exact attention rounded once, the BF16 weights leave many more
+    # differing BF16 elements than the FP32 weights (the paper's probe metric)
+    exact = ops.attention_heads(f64(Q), f64(K), f64(V), sc)
+    fp32 = run_attention(Qd, Kd, Vd, sc, key_block=key_block).cpu()
+    n_b = int(np.count_nonzero(f64(Of) != exact.y))
+    n_f = int(np.count_nonzero(f64(fp32) != exact.y))
+    assert n_b > 3 * n_f, (n_b, n_f)

@@ -94,3 +94,14 @@ def test_ffn_odd_slice_count():
     X, U, V, a, b = _case(130, 128, 320, 96, 17)
     y = run_ffn(X, U, V, a, b, 64, 3)
     check(y, ops.ffn(f64(X), f64(U), f64(V), f64(a), f64(b)), what="odd slices")
+
+
+def test_ffn_baseline_variant():
+    """Baseline PSI numerics: pre-GELU BF16 write and products rounded to
+    BF16 before their biases (section III-A)."""
+    X, U, V, a, b = _case(130, 256, 1024, 256, 41)
+    flags = psi.PSI_BOUNDARY_PREGELU_BF16 | psi.PSI_BIAS_AFTER_BF16
+    y = run_ffn(X, U, V, a, b, 256, 3, flags=flags)
+    res = ops.ffn(f64(X), f64(U), f64(V), f64(a), f64(b), pregelu_bf16=True,
+                  bias_after_bf16=True)
+    check(y, res, what="ffn baseline")

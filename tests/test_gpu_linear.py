@@ -81,3 +81,18 @@ def test_linear_special_values():
     assert rep["max_raw_ulps"] <= 1
     z = run_linear(torch.zeros(3, 128, dtype=torch.bfloat16), W, b, 64, 2)
     assert torch.equal(z.view(torch.int16), b.expand(3, 128).contiguous().view(torch.int16))
+
+
+def test_linear_baseline_bias_after_bf16():
+    """The paper's baseline rounding order (section III-A): product rounded to
+    BF16 before the bias is added."""
+    g = torch.Generator().manual_seed(31)
+    X = torch.randn(300, 512, generator=g).to(torch.bfloat16)
+    W = (torch.randn(512, 512, generator=g) / math.sqrt(512)).to(torch.bfloat16)
+    b = (torch.randn(512, generator=g) * 0.5).to(torch.bfloat16)
+    R = torch.randn(300, 512, generator=g).to(torch.bfloat16)
+    y = run_linear(X, W, b, 256, 2, flags=psi.PSI_BIAS_AFTER_BF16, residual=R)
+    res = ops.linear(f64(X), f64(W), f64(b), residual=f64(R), bias_after_bf16=True)
+    check(y, res, what="bias after bf16")
+    y2 = run_linear(X, W, b, 256, 2, residual=R)
+    assert not torch.equal(y.view(torch.int16), y2.view(torch.int16))

@@ -304,3 +304,216 @@ def test_ffn_slack_is_small_on_random_inputs():
     jump = ops.hidden_rounding_jump(t, At, r.H)
     assert np.count_nonzero(jump) < 0.02 * jump.size
     assert np.all(r.slack <= 2.0 ** -7 * r.A)
+
+
+# ----------------------------------------------- baseline numerics variant --
+def test_linear_bias_after_bf16_worked():
+    """The rounding mechanism of section II-C Eq.(5) on a projection: the
+    product 1 + 2^-9 rounds to 1 before the bias 2^-8 is added (baseline
+    order, a tie that goes to even: 1), while adding the bias first gives
+    1 + 3*2^-9, which rounds to 1 + 2^-7 (modified order)."""
+    X = np.array([[1.0, 2.0 ** -9]])
+    W = np.array([[1.0, 1.0]])
+    b = np.array([2.0 ** -8])
+    assert ops.linear(X, W, b, bias_after_bf16=True).y[0, 0] == 1.0
+    assert ops.linear(X, W, b).y[0, 0] == 1.0 + 2.0 ** -7
+
+
+def test_linear_bias_after_bf16_against_definition():
+    rng = np.random.default_rng(21)
+    X = _rand_bf16(rng, (9, 33))
+    W = _rand_bf16(rng, (12, 33), 0.2)
+    b = _rand_bf16(rng, (12,), 0.5)
+    R = _rand_bf16(rng, (9, 12))
+    r = ops.linear(X, W, b, residual=R, bias_after_bf16=True)
+    p = F.linear(torch.from_numpy(X), torch.from_numpy(W)).numpy()
+    want = bf16.round_bf16(bf16.round_bf16(p) + b + R)
+    assert np.array_equal(r.y, want)
+
+
+def test_ffn_bias_after_bf16_against_definition():
+    rng = np.random.default_rng(22)
+    X = _rand_bf16(rng, (5, 24))
+    U = _rand_bf16(rng, (40, 24), 0.2)
+    V = _rand_bf16(rng, (16, 40), 0.15)
+    a = _rand_bf16(rng, (40,), 0.1)
+    b = _rand_bf16(rng, (16,), 0.1)
+    r = ops.ffn(X, U, V, a, b, pregelu_bf16=True, bias_after_bf16=True)
+    t = bf16.round_bf16(bf16.round_bf16(X @ U.T) + a)
+    H = bf16.round_bf16(F.gelu(torch.from_numpy(t), approximate="tanh").numpy())
+    assert np.array_equal(r.H, H)
+    assert np.array_equal(r.y, bf16.round_bf16(bf16.round_bf16(H @ V.T) + b))
+
+
+def test_attention_bf16_weights_definition():
+    """Numerator weights rounded to BF16 relative to the running max; with a
+    single key block this is sum B(e^{s-m}) v / sum e^{s-m}."""
+    rng = np.random.default_rng(23)
+    Q = _rand_bf16(rng, (7, 16))
+    K = _rand_bf16(rng, (50, 16))
+    V = _rand_bf16(rng, (50, 16))
+    sc = 0.25
+    r = ops.attention_bf16_weights(Q, K, V, sc, key_block=50)
+    S = sc * Q @ K.T
+    P = np.exp(S - S.max(axis=1, keepdims=True))
+    want = (bf16.round_bf16(P) @ V) / P.sum(axis=1, keepdims=True)
+    assert np.allclose(r.y64, want, rtol=0, atol=1e-14)
+    # one key: weight exactly 1
+    r1 = ops.attention_bf16_weights(Q, K[:1], V[:1], sc, key_block=128)
+    assert np.array_equal(r1.y, np.repeat(V[:1], 7, axis=0))
+    # the BF16 weights move the result by about 2^-9 of its scale, the FP32
+    # ones do not
+    dense = ops.attention(Q, K, V, sc)
+    d = np.abs(r.y64 - dense.y64).max() / np.abs(dense.y64).max()
+    assert 1e-5 < d < 2.0 ** -6
+
+
+# ------------------------------------------------- RMSNorm and split RoPE --
+def _round_rational(v: Fraction) -> float:
+    """RNE to 8 significant bits of any rational (normal range), by exact
+    integer arithmetic: v = n * 2^q with q the quantum's exponent."""
+    if v == 0:
+        return 0.0
+    a = abs(v)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1                        # now 2^e <= a < 2^(e+1)
+    q = Fraction(2) ** (e - 7)
+    n = a / q
+    k = n.numerator // n.denominator
+    rem = n - k
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and k % 2 == 1):
+        k += 1
+    return math.copysign(float(k * q), float(v))
+
+
+def test_rmsnorm_hand_worked():
+    g = json.load(open(os.path.join(GOLD, "rmsnorm_hand.json")))
+    for c in g["cases"]:
+        r = ops.rmsnorm(np.array([c["x"]]), np.array(c["gamma"]), c["eps"])
+        want = [_round_rational(Fraction(n, c["y_den"])) for n in c["y_num"]]
+        assert r.y[0].tolist() == want, c["note"]
+
+
+def test_rmsnorm_against_torch_rms_norm():
+    """torch's own RMSNorm in float64 (an independent library routine)."""
+    rng = np.random.default_rng(31)
+    X = _rand_bf16(rng, (17, 96), 3.0)
+    gmm = _rand_bf16(rng, (96,))
+    for eps in (0.0, 1e-6, 0.5):
+        r = ops.rmsnorm(X, gmm, eps)
+        t = F.rms_norm(torch.from_numpy(X), (96,), torch.from_numpy(gmm), eps).numpy()
+        assert np.allclose(r.y64, t, rtol=1e-13, atol=0)
+
+
+def test_rmsnorm_scale_invariance_and_unit_mean_square():
+    """With eps = 0 the map is invariant under x -> 2^k x (exact in float64)
+    and, with gamma = 1, the output's mean square is 1."""
+    rng = np.random.default_rng(32)
+    X = _rand_bf16(rng, (9, 64))
+    ones = np.ones(64)
+    r = ops.rmsnorm(X, ones, 0.0)
+    for k in (-20, 3):
+        assert np.array_equal(ops.rmsnorm(X * 2.0 ** k, ones, 0.0).y, r.y)
+    assert np.allclose((r.y64 ** 2).mean(axis=1), 1.0, rtol=1e-14)
+
+
+@pytest.mark.parametrize("tile", [1, 7, 64, 100, 256])
+def test_rmsnorm_width_partition(tile):
+    """Section II-B: partial sums of squares over any width partition give
+    the one global denominator (equal within the float64 bound)."""
+    rng = np.random.default_rng(33)
+    X = _rand_bf16(rng, (11, 256))
+    gmm = _rand_bf16(rng, (256,))
+    full = ops.rmsnorm(X, gmm, 1e-6)
+    part = ops.rmsnorm_partitioned(X, gmm, 1e-6, tile)
+    assert np.allclose(part.y64, full.y64, rtol=1e-14, atol=0)
+
+
+def test_rmsnorm_zero_row():
+    r = ops.rmsnorm(np.zeros((2, 8)), np.ones(8), 1e-6)
+    assert np.array_equal(r.y, np.zeros((2, 8)))
+
+
+def _rope_table(n, half, seed):
+    rng = np.random.default_rng(seed)
+    th = rng.uniform(-np.pi, np.pi, (n, half))
+    return np.cos(th).astype(np.float32).astype(np.float64), \
+        np.sin(th).astype(np.float32).astype(np.float64)
+
+
+def test_rope_split_against_complex_multiplication():
+    """The pair (t_j, t_{j+dh/2}) as the complex number t_j + i t_{j+dh/2},
+    multiplied by c + i s: an independent formulation of the rotation."""
+    rng = np.random.default_rng(34)
+    dh, H = 8, 3
+    T = rng.standard_normal((5, dh * H + 8))
+    c, s = _rope_table(5, dh // 2, 1)
+    out = ops.rope_split(T, c, s, dh, dh * H)
+    for h in range(H):
+        z = torch.complex(torch.from_numpy(T[:, h * dh:h * dh + dh // 2]),
+                          torch.from_numpy(T[:, h * dh + dh // 2:(h + 1) * dh]))
+        w = z * torch.complex(torch.from_numpy(c), torch.from_numpy(s))
+        assert np.allclose(out[:, h * dh:h * dh + dh // 2], w.real.numpy(), rtol=0, atol=1e-15)
+        assert np.allclose(out[:, h * dh + dh // 2:(h + 1) * dh], w.imag.numpy(), rtol=0, atol=1e-15)
+    assert np.array_equal(out[:, dh * H:], T[:, dh * H:])
+
+
+def test_linear_rope_quarter_turn_is_a_row_permutation():
+    """c = 0, s = 1 maps (a, b) to (-b, a): the rotated projection is the
+    plain projection of W and b with each head's halves swapped and the
+    first negated, rounded once (bitwise, exact ties included)."""
+    rng = np.random.default_rng(35)
+    dh, H, K = 8, 2, 40
+    M = dh * H + 8
+    X = _rand_bf16(rng, (6, K))
+    W = _rand_bf16(rng, (M, K), 0.2)
+    b = _rand_bf16(rng, (M,), 0.1)
+    c, s = np.zeros((6, dh // 2)), np.ones((6, dh // 2))
+    r = ops.linear_rope(X, W, b, c, s, dh, dh * H)
+    perm = np.arange(M)
+    sign = np.ones(M)
+    for h in range(H):
+        lo = np.arange(h * dh, h * dh + dh // 2)
+        perm[lo], perm[lo + dh // 2] = lo + dh // 2, lo
+        sign[lo] = -1.0
+    ref = ops.linear(X, W[perm] * sign[:, None], b[perm] * sign)
+    assert np.array_equal(r.y, ref.y)
+    ident = ops.linear_rope(X, W, b, np.ones_like(c), np.zeros_like(s), dh, dh * H)
+    assert np.array_equal(ident.y, ops.linear(X, W, b).y)
+
+
+def test_linear_rope_preserves_pair_norms():
+    """|rotated pair| = |pair| when c^2 + s^2 = 1 (within the table's FP32
+    rounding): a wrong pairing or sign breaks it."""
+    rng = np.random.default_rng(36)
+    dh, H, K = 16, 2, 24
+    X = _rand_bf16(rng, (7, K))
+    W = _rand_bf16(rng, (dh * H, K), 0.2)
+    b = np.zeros(dh * H)
+    th = rng.uniform(-np.pi, np.pi, (7, dh // 2))
+    r = ops.linear_rope(X, W, b, np.cos(th), np.sin(th), dh, dh * H)
+    t = X @ W.T
+    h = dh // 2
+    for h0 in range(0, dh * H, dh):
+        n_in = t[:, h0:h0 + h] ** 2 + t[:, h0 + h:h0 + dh] ** 2
+        n_out = r.y64[:, h0:h0 + h] ** 2 + r.y64[:, h0 + h:h0 + dh] ** 2
+        assert np.allclose(n_out, n_in, rtol=1e-13)
+
+
+def test_linear_rope_bf16_first_variant():
+    """The baseline materialisation rounds the projection before rotating:
+    equal to rotating the oracle's own rounded linear output; for c = 1,
+    s = 0 both variants equal the plain projection."""
+    rng = np.random.default_rng(37)
+    dh, K = 8, 32
+    X = _rand_bf16(rng, (5, K))
+    W = _rand_bf16(rng, (2 * dh, K), 0.3)
+    b = _rand_bf16(rng, (2 * dh,), 0.1)
+    c, s = _rope_table(5, dh // 2, 2)
+    r = ops.linear_rope(X, W, b, c, s, dh, dh, rope_after_bf16=True)
+    lin = ops.linear(X, W, b)
+    assert np.array_equal(r.y, bf16.round_bf16(ops.rope_split(lin.y, c, s, dh, dh)))
+    one = ops.linear_rope(X, W, b, np.ones_like(c), np.zeros_like(s), dh, dh,
+                          rope_after_bf16=True)
+    assert np.array_equal(one.y, lin.y)

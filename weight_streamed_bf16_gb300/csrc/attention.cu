@@ -274,8 +274,8 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
               tc_fence_after();
             }
             const uint32_t sV = smem_u32(smem + A::OFF_V + s * 2 * TILE64);
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
+            const int halves = args.bf16_weights ? 1 : 2;  // p_hi (and p_lo)
+            for (int half = 0; half < halves; ++half) {
 #pragma unroll
               for (int kk = 0; kk < SUB / 16; ++kk) {
                 const uint32_t pcol = SUB * u + 32 * (kk >> 1) + 8 * (kk & 1) + 16 * half;

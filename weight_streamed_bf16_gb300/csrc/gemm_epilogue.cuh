@@ -114,6 +114,10 @@ __device__ __forceinline__ void epilogue_row32(const GemmArgs& a, int row, bool 
         if (j < ncol) v[j] = p[j] + v[j];
     }
   }
+  if (a.bias_after_bf16) {  // the baseline variant: product rounded before the bias
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = round_bf16_f(v[j]);
+  }
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] = v[j] + bia[j];
   if (a.epi == EPI_GELU) {

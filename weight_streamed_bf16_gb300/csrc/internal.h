@@ -62,6 +62,8 @@ struct GemmArgs {
                         // come from the second page (0: one page)
   int32_t n_split;      // output columns served by the first page; columns from
                         // n_split on come from the second page (0: one page)
+  int32_t bias_after_bf16;  // round the FP32 product to BF16 before adding bias
+  int32_t pad_;
   const uint16_t* bias;   // [N]
   const uint16_t* resid;  // [M x ldo] or null
   uint16_t* out;          // [M x ldo]
@@ -89,7 +91,7 @@ struct AttnArgs {
   int32_t Nk;
   int32_t key_block;
   float scale_log2;  // scale * log2(e)
-  int32_t pad_;
+  int32_t bf16_weights;  // numerator with B(p) only (no p_lo correction)
   uint16_t* O;
   int64_t o_ld_token;
   int64_t o_ld_head;

@@ -549,6 +549,7 @@ psi_status psi_linear_paged(psi_arena* a, const void* X, int64_t N, int64_t K,
     g.N = static_cast<int32_t>(rows_p);
     g.K = static_cast<int32_t>(K);
     g.epi = EPI_LINEAR;
+    g.bias_after_bf16 = (flags & PSI_BIAS_AFTER_BF16) ? 1 : 0;
     g.bias = static_cast<const uint16_t*>(bias) + r0;
     g.resid = residual ? static_cast<const uint16_t*>(residual) + r0 : nullptr;
     g.out = static_cast<uint16_t*>(Y) + r0;
@@ -632,6 +633,7 @@ psi_status psi_ffn_paged(psi_arena* a, const void* X, int64_t N, const psi_ffn_w
       up.n_split = merged ? static_cast<int32_t>(sl) : 0;
       up.epi = EPI_GELU;
       up.pregelu = (flags & PSI_BOUNDARY_PREGELU_BF16) ? 1 : 0;
+      up.bias_after_bf16 = (flags & PSI_BIAS_AFTER_BF16) ? 1 : 0;
       up.bias = a16 + J * sl;
       up.out = Hg + u * sl;
       up.ldo = G * sl;
@@ -655,6 +657,7 @@ psi_status psi_ffn_paged(psi_arena* a, const void* X, int64_t N, const psi_ffn_w
     dn.ldacc = r;
     dn.err = err;
     dn.timeout_ns = kWaitLimitNs;
+    dn.bias_after_bf16 = (flags & PSI_BIAS_AFTER_BF16) ? 1 : 0;
     const bool first = J0 == 0, last = J0 + gs >= S;
     if (last) {
       dn.epi = first ? EPI_LINEAR : EPI_ACC_FINAL;
@@ -682,7 +685,6 @@ psi_status psi_attn_partitioned(const psi_heads* Q, const psi_heads* K, const ps
                                 const psi_heads* O, int32_t heads, int64_t Nq, int64_t Nk,
                                 int32_t dh, float scale, int32_t key_block, void* stream,
                                 uint32_t flags) {
-  (void)flags;
   if (!Q || !K || !V || !O || !O->ptr)
     return set_error(PSI_ERR_INVALID_ARG, "attn: null argument");
   if (heads <= 0 || Nq < 0 || Nk < 1)
@@ -702,6 +704,7 @@ psi_status psi_attn_partitioned(const psi_heads* Q, const psi_heads* K, const ps
   g.Nk = static_cast<int32_t>(Nk);
   g.key_block = key_block;
   g.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+  g.bf16_weights = (flags & PSI_ATTN_BF16_WEIGHTS) ? 1 : 0;
   g.O = static_cast<uint16_t*>(O->ptr);
   g.o_ld_token = O->ld_token;
   g.o_ld_head = O->ld_head;

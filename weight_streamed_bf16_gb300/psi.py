@@ -27,6 +27,8 @@ PSI_ERR_DEVICE = 7
 PSI_RESIDENT = 0x1
 PSI_SYNC_COPY = 0x2
 PSI_BOUNDARY_PREGELU_BF16 = 0x4
+PSI_BIAS_AFTER_BF16 = 0x8
+PSI_ATTN_BF16_WEIGHTS = 0x10
 
 # every entry point include/psi.h declares
 EXPORTS = [
