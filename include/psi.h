@@ -68,6 +68,11 @@ typedef enum {
                                           (p_hi only), the baseline variant of
                                           section III-A; the denominator keeps
                                           the FP32 weights */
+#define PSI_ROPE_AFTER_BF16       0x20u /* psi_linear_rope_paged: the projection
+                                          is rounded to BF16 before the rotation
+                                          and rounded again after it (an extra
+                                          materialisation, the baseline
+                                          variant's RoPE order) */
 
 typedef struct psi_arena psi_arena;
 
@@ -114,6 +119,20 @@ typedef struct {
   int64_t ld_token;
   int64_t ld_head;
 } psi_heads;
+
+/* Split RoPE table (section II-B): token n's head pair j (j < dh/2) is
+ * rotated by c = cos[n*ld + j], s = sin[n*ld + j] (device FP32; 16-byte
+ * aligned, ld % 4 == 0, ld >= dh/2).  The rotation covers the leading `cols`
+ * output columns (whole heads of dh = 64 or 128 columns: the query and key
+ * heads of a fused QKV projection); later columns pass through. */
+typedef struct {
+  const float* cos;
+  const float* sin;
+  int64_t ld;
+  int64_t cols;
+  int32_t dh;
+  int32_t pad_;
+} psi_rope;
 
 typedef struct {
   uint64_t pages_streamed;   /* H2D page requests */
@@ -235,6 +254,30 @@ psi_status psi_linear_paged(psi_arena* arena, const void* X, int64_t N, int64_t 
                             const psi_linear_weight* W, const void* bias,
                             const void* residual, void* Y, int64_t ldy,
                             uint32_t flags);
+
+/* Paged linear with split RoPE in the epilogue (section II-B): as
+ * psi_linear_paged without residual, and in each head among the leading
+ * rope->cols output columns the pair (a, b) = (t_j, t_{j+dh/2}) of the FP32
+ * values t = X W^T + b is written as B(c a - s b), B(s a + c b) with the
+ * table entries of the row's token: one BF16 write, the rotation applied to
+ * the exact pre-rotation pair.  W->page_rows must be a multiple of rope->dh
+ * (or cover W in one page).  Flags: PSI_RESIDENT, PSI_SYNC_COPY,
+ * PSI_BIAS_AFTER_BF16, PSI_ROPE_AFTER_BF16. */
+psi_status psi_linear_rope_paged(psi_arena* arena, const void* X, int64_t N, int64_t K,
+                                 const psi_linear_weight* W, const void* bias,
+                                 const psi_rope* rope, void* Y, int64_t ldy,
+                                 uint32_t flags);
+
+/* Full-row RMS normalisation, section II-B:
+ *   Y[n, i] = B(gamma_i * X[n, i] / sqrt(s_n/d + eps)),  s_n = sum_i X[n, i]^2
+ * with s_n summed in FP32 over the whole row (partial sums over width tiles
+ * combined once, in a fixed order) and one denominator for every tile.
+ *   X [N x d] row stride ldx, Y [N x d] row stride ldy, gamma [d]: device
+ *   BF16, 16-byte aligned, d, ldx, ldy multiples of 8, 1 <= d <= 8192.
+ *   eps >= 0 (finite).  Y must not overlap X.
+ * Enqueued on `stream` (cudaStream_t). */
+psi_status psi_rmsnorm(const void* X, int64_t ldx, int64_t N, int64_t d, const void* gamma,
+                       float eps, void* Y, int64_t ldy, void* stream);
 
 /* Paged FFN, Eq.(2) with the reuse schedule of section III-B.  Hidden
  * slices are taken in order in groups of G (G = 2 when there are at least

@@ -25,6 +25,7 @@ from __future__ import annotations
 import math
 from dataclasses import dataclass
 
+import numpy as np
 import torch
 
 __all__ = [
@@ -130,6 +131,7 @@ class BlockCfg:
     arena_bytes: int = 80 * MiB
     key_block: int = 256
     seed: int = 0
+    eps: float = 1e-6      # RMSNorm epsilon of the pre-norm variant
 
     @property
     def qkv_rows(self) -> int:
@@ -165,7 +167,7 @@ tensor_ids = {
     "X": 1, "W": 2, "b": 3, "U": 4, "V": 5, "a": 6, "b2": 7,
     "Q": 8, "K": 9, "Vt": 10,
     "Wqkv": 11, "bqkv": 12, "Wo": 13, "bo": 14, "W1": 15, "a1": 16,
-    "W2": 17, "b1": 18,
+    "W2": 17, "b1": 18, "gamma1": 19, "gamma2": 20,
 }
 
 
@@ -223,3 +225,26 @@ def block_weights(cfg: BlockCfg = BLOCK, block: int = 0, device="cpu"):
         "W2": normal_bf16((d, h), 1.0 / math.sqrt(h), s, _tid("W2", block), device),
         "b1": normal_bf16((d,), 0.02, s, _tid("b1", block), device),
     }
+
+
+def norm_gains(cfg: BlockCfg = BLOCK, block: int = 0, device="cpu"):
+    """RMSNorm gains gamma1 (before the QKV projection) and gamma2 (before
+    the FFN), each [d] ~ 1 + N(0, 0.1^2), drawn in FP32 and rounded to BF16."""
+    out = []
+    for name in ("gamma1", "gamma2"):
+        g = torch.Generator(device="cpu").manual_seed(_mix(cfg.seed, _tid(name, block)))
+        v = (1.0 + 0.1 * torch.randn(cfg.d, generator=g)).to(torch.bfloat16)
+        out.append(v.to(device))
+    return tuple(out)
+
+
+def rope_table(n_tokens: int, dh: int, base: float = 10000.0, pos0: int = 0):
+    """The cos/sin table a model hands to split RoPE: token n at position
+    pos0 + n, frequency base^(-2j/dh) for j < dh/2, angles and their cos/sin
+    in float64, rounded to FP32.  Returns two float32 CPU tensors
+    [n_tokens x dh/2]."""
+    pos = np.arange(pos0, pos0 + n_tokens, dtype=np.float64)[:, None]
+    inv = base ** (-2.0 * np.arange(dh // 2, dtype=np.float64) / dh)
+    ang = pos * inv[None, :]
+    return (torch.from_numpy(np.cos(ang).astype(np.float32)),
+            torch.from_numpy(np.sin(ang).astype(np.float32)))

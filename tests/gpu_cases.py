@@ -93,11 +93,54 @@ def run_attention(Q, K, V, scale, key_block=128, O=None):
     return O
 
 
+def run_linear_rope(X, W, b, cos, sin, dh, cols, page_rows, slots, flags=0):
+    """Paged QKV-style projection with split RoPE on the first ``cols``
+    output columns; cos/sin are [N x dh/2] float32 CPU tables."""
+    N, K = X.shape
+    M = W.shape[0]
+    ldy = (M + 7) // 8 * 8
+    dev = torch.device("cuda")
+    Xd, bd = X.to(dev), b.to(dev)
+    cd = cos.to(dev).contiguous()
+    sd = sin.to(dev).contiguous()
+    Y = torch.full((N, ldy), float("nan"), dtype=torch.bfloat16, device=dev)
+    page_bytes = (page_rows * K * 2 + 1023) // 1024 * 1024
+    arena = Arena(page_bytes, slots)
+    w = LinearWeight(W, page_bytes, page_rows=page_rows, resident=bool(flags & psi.PSI_RESIDENT))
+    rope = psi.psi_rope(cd.data_ptr(), sd.data_ptr(), cd.shape[1], cols, dh, 0)
+    try:
+        psi.psi_linear_rope_paged(arena.handle, Xd.data_ptr(), N, K, w.desc(), bd.data_ptr(),
+                                  rope, Y.data_ptr(), ldy, flags)
+        arena.sync()
+    finally:
+        arena.close()
+    return Y[:, :M].cpu()
+
+
+def run_rmsnorm(X, gamma, eps, ldx=None, ldy=None):
+    """X [N x d] CPU bf16 -> GPU RMSNorm output (CPU bf16 [N x d])."""
+    N, d = X.shape
+    ldx = ldx or d
+    ldy = ldy or d
+    dev = torch.device("cuda")
+    Xb = torch.zeros((N, ldx), dtype=torch.bfloat16)
+    Xb[:, :d] = X
+    Xd = Xb.to(dev)
+    gd = gamma.to(dev)
+    Y = torch.full((N, ldy), float("nan"), dtype=torch.bfloat16, device=dev)
+    s = torch.cuda.current_stream()
+    psi.psi_rmsnorm(Xd.data_ptr(), ldx, N, d, gd.data_ptr(), eps, Y.data_ptr(), ldy,
+                    s.cuda_stream)
+    torch.cuda.synchronize()
+    return Y[:, :d].cpu()
+
+
 def check(y_gpu: torch.Tensor, res, tol=2.0, what=""):
     rep = grade.report(f64(y_gpu), res, tol)
     assert rep["pass"], f"{what}: {rep}"
     return rep
 
 
-__all__ = ["ensure_lib", "f64", "run_linear", "run_ffn", "run_attention", "check", "ops",
+__all__ = ["ensure_lib", "f64", "run_linear", "run_linear_rope", "run_rmsnorm", "run_ffn",
+           "run_attention", "check", "ops",
            "grade", "bf16"]

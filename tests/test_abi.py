@@ -109,3 +109,32 @@ def test_header_documents_no_device_allocation():
     for f in os.listdir(src):
         body = open(os.path.join(src, f)).read()
         assert not re.search(r"\b(cudaMalloc\w*|cudaFree\w*|cuMemAlloc\w*)\s*\(", body), f
+
+
+def test_rmsnorm_argument_checks_need_no_gpu(lib):
+    """Shape, alignment and overlap checks of psi_rmsnorm return before any
+    CUDA call (fake 16-byte aligned addresses; nothing is dereferenced)."""
+    X, g, Y = 1 << 20, 1 << 21, 1 << 22
+    bad = [
+        (None, 64, 4, 64, g, 1e-6, Y, 64, psi.PSI_ERR_INVALID_ARG),   # null X
+        (X, 64, 4, 60, g, 1e-6, Y, 64, psi.PSI_ERR_INVALID_ARG),      # d % 8
+        (X, 32, 4, 64, g, 1e-6, Y, 64, psi.PSI_ERR_INVALID_ARG),      # ldx < d
+        (X, 16384, 4, 16384, g, 1e-6, Y, 16384, psi.PSI_ERR_UNSUPPORTED),  # d > 8192
+        (X, 64, 4, 64, g, -1.0, Y, 64, psi.PSI_ERR_INVALID_ARG),      # eps < 0
+        (X, 64, 4, 64, g, float("nan"), Y, 64, psi.PSI_ERR_INVALID_ARG),
+        (X + 2, 64, 4, 64, g, 1e-6, Y, 64, psi.PSI_ERR_INVALID_ARG),  # misaligned
+        (X, 64, 4, 64, g, 1e-6, X + 64, 64, psi.PSI_ERR_INVALID_ARG),  # Y overlaps X
+    ]
+    for *args, want in bad:
+        assert lib.psi_rmsnorm(*args, None) == want, args
+    assert lib.psi_rmsnorm(X, 64, 0, 64, g, 1e-6, Y, 64, None) == psi.PSI_OK  # no rows
+
+
+def test_linear_rope_argument_checks_need_no_gpu(lib):
+    W = psi.psi_linear_weight(None, None, 64, 64, 64)
+    rope = psi.psi_rope(1 << 20, 1 << 21, 64, 64, 128, 0)
+    r = lib.psi_linear_rope_paged(None, None, 1, 64, C.byref(W), None, C.byref(rope), None,
+                                  64, 0)
+    assert r == psi.PSI_ERR_INVALID_ARG
+    r = lib.psi_linear_rope_paged(1, 1, 1, 64, C.byref(W), 1, None, 1, 64, 0)
+    assert r == psi.PSI_ERR_INVALID_ARG and "rope" in psi.psi_last_error()

@@ -124,3 +124,74 @@ def test_stack_transport_controls_bitwise():
         arena.close()
     for o in outs[1:]:
         assert torch.equal(outs[0].view(torch.int16), o.view(torch.int16))
+
+
+# ---------------------------------------------------- pre-norm block (f2) --
+def _pn_shape():
+    return BlockShape(d=CFG.d, N=CFG.N, heads=CFG.heads, dh=CFG.dh, hidden=CFG.hidden,
+                      slice=CFG.slice, page_bytes=CFG.page_bytes, prenorm=True, eps=CFG.eps)
+
+
+@pytest.fixture(scope="module")
+def prenorm_run():
+    w = {k: v.cpu() for k, v in psi_synth.block_weights(CFG, block=0, device="cuda").items()}
+    w["gamma1"], w["gamma2"] = psi_synth.norm_gains(CFG)
+    bw = BlockWeights(w, _pn_shape(), resident=True)
+    cos, sin = psi_synth.rope_table(CFG.N, CFG.dh)
+    arena = Arena(CFG.page_bytes, 5)
+    runner = BlockRunner(_pn_shape(), arena, rope=(cos, sin))
+    X = psi_synth.block_input(CFG, device="cuda")
+    Y = torch.empty_like(X)
+    runner.forward(X, bw, Y, 0)
+    arena.sync()
+    Yr = torch.empty_like(X)
+    runner.forward(X, bw, Yr, psi.PSI_RESIDENT)
+    arena.sync()
+    # the first normalisation's output, recomputed by the same kernel (its
+    # buffer is reused by the second one)
+    n0 = torch.empty_like(X)
+    psi.psi_rmsnorm(X.data_ptr(), CFG.d, CFG.N, CFG.d, bw.gamma1.data_ptr(), CFG.eps,
+                    n0.data_ptr(), CFG.d, torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    out = {"X": X.cpu(), "n0": n0.cpu(), "h": runner.h.cpu(), "att": runner.att.cpu(),
+           "x1": runner.x1.cpu(), "n1": runner.xn.cpu(), "Y": Y.cpu(), "Yr": Yr.cpu(),
+           "w": w, "cos": cos.double().numpy(), "sin": sin.double().numpy()}
+    arena.close()
+    return out
+
+
+def test_prenorm_norm_probes(prenorm_run):
+    r, w = prenorm_run, prenorm_run["w"]
+    eps = np.float64(np.float32(CFG.eps))
+    check(r["n0"][ROWS], ops.rmsnorm(f64(r["X"][ROWS]), f64(w["gamma1"]), eps), what="norm 1")
+    check(r["n1"][ROWS], ops.rmsnorm(f64(r["x1"][ROWS]), f64(w["gamma2"]), eps), what="norm 2")
+
+
+def test_prenorm_qkv_rope_probe(prenorm_run):
+    r, w = prenorm_run, prenorm_run["w"]
+    H, dh = CFG.heads, CFG.dh
+    res = ops.linear_rope(f64(r["n0"][ROWS]), f64(w["Wqkv"]), f64(w["bqkv"]),
+                          r["cos"][ROWS], r["sin"][ROWS], dh, 2 * H * dh)
+    rep = check(r["h"][ROWS], res, what="qkv rope")
+    assert rep["max_rel_err"] <= 1e-2
+
+
+def test_prenorm_attention_and_ffn_probes(prenorm_run):
+    r, w = prenorm_run, prenorm_run["w"]
+    H, dh = CFG.heads, CFG.dh
+    h = f64(r["h"])
+    for hd in (0, 31):
+        q = h[ROWS, hd * dh:(hd + 1) * dh]
+        k = h[:, H * dh + hd * dh:H * dh + (hd + 1) * dh]
+        v = h[:, 2 * H * dh + hd * dh:2 * H * dh + (hd + 1) * dh]
+        check(r["att"][ROWS, hd * dh:(hd + 1) * dh], ops.attention(q, k, v, 1 / math.sqrt(dh)),
+              what=f"attention head {hd}")
+    res = ops.ffn(f64(r["n1"][ROWS]), f64(w["W1"]), f64(w["W2"]), f64(w["a1"]), f64(w["b1"]),
+                  residual=f64(r["x1"][ROWS]))
+    rep = check(r["Y"][ROWS], res, what="ffn")
+    assert rep["max_rel_err"] <= 1e-2
+
+
+def test_prenorm_resident_equals_streamed(prenorm_run):
+    assert torch.equal(prenorm_run["Y"].view(torch.int16), prenorm_run["Yr"].view(torch.int16))
+    assert torch.isfinite(prenorm_run["Y"].float()).all()

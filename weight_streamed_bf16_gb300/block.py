@@ -1,12 +1,20 @@
 """Synthetic transformer block and stack over the C ABI.
 
-Composition of one block (operator shapes of the paged-operator study; the
-norm and RoPE of a real block are not part of it):
+Composition of one block (operator shapes of the paged-operator study):
 
     h  = B(X Wqkv^T + bqkv)                      psi_linear_paged   [N x 3*H*dh]
     a  = attention(Q, K, V), heads read in place  psi_attn_partitioned [N x H*dh]
     x1 = B(X + a Wo^T + bo)                      psi_linear_paged (residual X)
     y  = B(x1 + F(x1))                           psi_ffn_paged (residual x1)
+
+With ``BlockShape.prenorm`` the block is a pre-norm block with the two
+partitioned operators of section II-B:
+
+    n0 = RMSNorm(X; gamma1)                      psi_rmsnorm
+    h  = B(rope(n0 Wqkv^T + bqkv))               psi_linear_rope_paged (Q, K heads)
+    a, x1 as above
+    n1 = RMSNorm(x1; gamma2)                     psi_rmsnorm
+    y  = B(x1 + F(n1))                           psi_ffn_paged (residual x1)
 
 Weights live in pinned host memory and stream through one arena; the page
 ring continues across operators and blocks, so it never drains between
@@ -33,6 +41,8 @@ class BlockShape:
     slice: int = 1024
     page_bytes: int = 16 << 20
     key_block: int = 128
+    prenorm: bool = False
+    eps: float = 1e-6
 
     @property
     def qkv(self) -> int:
@@ -54,6 +64,10 @@ class BlockWeights:
         self.bo = w["bo"].to(device)
         self.a1 = w["a1"].to(device)
         self.b1 = w["b1"].to(device)
+        self.gamma1 = w["gamma1"].to(device) if "gamma1" in w else None
+        self.gamma2 = w["gamma2"].to(device) if "gamma2" in w else None
+        if s.prenorm and (self.gamma1 is None or self.gamma2 is None):
+            raise ValueError("a pre-norm block needs gamma1 and gamma2")
 
     @property
     def host_bytes(self) -> int:
@@ -64,10 +78,23 @@ class BlockWeights:
 class BlockRunner:
     """Activation buffers and the arena for running blocks on one device."""
 
-    def __init__(self, shape: BlockShape, arena: Arena, device="cuda"):
+    def __init__(self, shape: BlockShape, arena: Arena, device="cuda", rope=None):
+        """``rope``: (cos, sin) FP32 tables [N x dh/2] (any device), required
+        for a pre-norm block."""
         s = shape
         self.s = s
         self.arena = arena
+        self.xn = None
+        if s.prenorm:
+            if rope is None:
+                raise ValueError("a pre-norm block needs the RoPE tables")
+            self.cos = rope[0].to(device=device, dtype=torch.float32).contiguous()
+            self.sin = rope[1].to(device=device, dtype=torch.float32).contiguous()
+            if self.cos.shape != (s.N, s.dh // 2) or self.sin.shape != self.cos.shape:
+                raise ValueError("RoPE tables must be [N x dh/2]")
+            self.rope = psi.psi_rope(self.cos.data_ptr(), self.sin.data_ptr(), s.dh // 2,
+                                     2 * s.heads * s.dh, s.dh, 0)
+            self.xn = torch.empty(s.N, s.d, dtype=torch.bfloat16, device=device)
         self.h = torch.empty(s.N, s.qkv, dtype=torch.bfloat16, device=device)
         self.att = torch.empty(s.N, s.heads * s.dh, dtype=torch.bfloat16, device=device)
         self.x1 = torch.empty(s.N, s.d, dtype=torch.bfloat16, device=device)
@@ -91,8 +118,15 @@ class BlockRunner:
                 marks[i].record(cs)
 
         mark(0)
-        psi.psi_linear_paged(A, X.data_ptr(), N, s.d, W.qkv.desc(), W.bqkv.data_ptr(), None,
-                             self.h.data_ptr(), s.qkv, flags)
+        if s.prenorm:
+            psi.psi_rmsnorm(X.data_ptr(), s.d, N, s.d, W.gamma1.data_ptr(), s.eps,
+                            self.xn.data_ptr(), s.d, cs.cuda_stream)
+            psi.psi_linear_rope_paged(A, self.xn.data_ptr(), N, s.d, W.qkv.desc(),
+                                      W.bqkv.data_ptr(), self.rope, self.h.data_ptr(), s.qkv,
+                                      flags)
+        else:
+            psi.psi_linear_paged(A, X.data_ptr(), N, s.d, W.qkv.desc(), W.bqkv.data_ptr(), None,
+                                 self.h.data_ptr(), s.qkv, flags)
         mark(1)
         q = self._heads(self.h, 0, s.qkv)
         k = self._heads(self.h, H * dh, s.qkv)
@@ -105,7 +139,12 @@ class BlockRunner:
         psi.psi_linear_paged(A, self.att.data_ptr(), N, H * dh, W.out.desc(), W.bo.data_ptr(),
                              X.data_ptr(), self.x1.data_ptr(), s.d, flags)
         mark(3)
-        psi.psi_ffn_paged(A, self.x1.data_ptr(), N, W.ffn.desc(), W.a1.data_ptr(),
+        ffn_in = self.x1
+        if s.prenorm:
+            psi.psi_rmsnorm(self.x1.data_ptr(), s.d, N, s.d, W.gamma2.data_ptr(), s.eps,
+                            self.xn.data_ptr(), s.d, cs.cuda_stream)
+            ffn_in = self.xn
+        psi.psi_ffn_paged(A, ffn_in.data_ptr(), N, W.ffn.desc(), W.a1.data_ptr(),
                           W.b1.data_ptr(), self.hid.data_ptr(), self.acc.data_ptr(),
                           self.x1.data_ptr(), Y.data_ptr(), flags)
         mark(4)

@@ -63,7 +63,12 @@ struct GemmArgs {
   int32_t n_split;      // output columns served by the first page; columns from
                         // n_split on come from the second page (0: one page)
   int32_t bias_after_bf16;  // round the FP32 product to BF16 before adding bias
-  int32_t pad_;
+  int32_t rope_dh;          // split RoPE head width (64 or 128); 0: no RoPE
+  int32_t rope_cols;        // leading output columns rotated (whole heads)
+  int32_t rope_after_bf16;  // round to BF16 before the rotation
+  const float* rope_cos;    // [M x rope_ld] FP32 table, row = token, index j < dh/2
+  const float* rope_sin;
+  int64_t rope_ld;
   const uint16_t* bias;   // [N]
   const uint16_t* resid;  // [M x ldo] or null
   uint16_t* out;          // [M x ldo]
@@ -99,6 +104,8 @@ struct AttnArgs {
   uint64_t timeout_ns;
 };
 
+psi_status launch_rmsnorm(const void* X, int64_t ldx, int64_t N, int64_t d, const void* gamma,
+                          float eps, void* Y, int64_t ldy, cudaStream_t stream);
 psi_status launch_attention(const psi_heads* Q, const psi_heads* K, const psi_heads* V,
                             const AttnArgs& args, cudaStream_t stream);
 

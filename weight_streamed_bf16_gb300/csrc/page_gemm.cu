@@ -232,8 +232,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t tbase = tmem + static_cast<uint32_t>(acc * BN + half * (BN / 2)) +
                              (static_cast<uint32_t>(q * 32) << 16);
-      epilogue_tile<BN>(args, &tmOut, tbase, m0, n0, q, row, row_ok, lane, pre, f32, stg_base,
-                        nstore, nxt);
+      if constexpr (BN == 256) {
+        if (args.rope_dh)
+          epilogue_tile_rope<BN>(args, &tmOut, tbase, m0, n0, q, row, row_ok, lane, stg_base,
+                                 nstore);
+        else
+          epilogue_tile<BN>(args, &tmOut, tbase, m0, n0, q, row, row_ok, lane, pre, f32,
+                            stg_base, nstore, nxt);
+      } else {
+        epilogue_tile<BN>(args, &tmOut, tbase, m0, n0, q, row, row_ok, lane, pre, f32, stg_base,
+                          nstore, nxt);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->tempty[acc]);
@@ -289,7 +298,15 @@ psi_status launch_page_gemm(const void* X, int64_t ldx, const void* P, int64_t l
   // tiles of 256 x 256 on CTA pairs where the shape fills them, else one CTA
   // per 128 x BN tile; the choice depends on the shape only
   const bool pair = gemm_use_pair(a.M, a.N);
-  const int bn = pair ? 128 : gemm_bn_for(a.N);  // page rows per CTA and box
+  // split RoPE needs whole heads in each epilogue warp's column half
+  const int bn = pair ? 128 : (a.rope_dh ? 256 : gemm_bn_for(a.N));  // page rows per CTA and box
+  if (a.rope_dh) {
+    if ((a.rope_dh != 64 && a.rope_dh != 128) || a.epi != EPI_LINEAR || a.resid ||
+        a.k_split > 0 || a.n_split > 0 || a.rope_cols % a.rope_dh || a.rope_ld % 4 ||
+        (reinterpret_cast<uintptr_t>(a.rope_cos) & 15) ||
+        (reinterpret_cast<uintptr_t>(a.rope_sin) & 15))
+      return set_error(PSI_ERR_INVALID_ARG, "page_gemm: bad RoPE arguments");
+  }
   CUtensorMap tx, tp, tp2;
   psi_status st = make_tmap_2d(&tx, X, a.M, a.K, ldx, BM, BK);
   if (st != PSI_OK) return st;

@@ -230,8 +230,12 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       tc_fence_after();
       const uint32_t tbase = tmem + static_cast<uint32_t>(acc * PTILE_N + half * (PTILE_N / 2)) +
                              (static_cast<uint32_t>(q * 32) << 16);
-      epilogue_tile<PTILE_N>(args, &tmOut, tbase, m0, n0, q, row, row_ok, lane, pre, f32,
-                             stg_base, nstore, nxt);
+      if (args.rope_dh)
+        epilogue_tile_rope<PTILE_N>(args, &tmOut, tbase, m0, n0, q, row, row_ok, lane, stg_base,
+                                    nstore);
+      else
+        epilogue_tile<PTILE_N>(args, &tmOut, tbase, m0, n0, q, row, row_ok, lane, pre, f32,
+                               stg_base, nstore, nxt);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&bars->tempty[acc]), 0));

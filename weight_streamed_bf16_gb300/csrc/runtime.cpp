@@ -499,9 +499,10 @@ psi_status psi_arena_fail_next_copy(psi_arena* a) {
 }
 
 // --------------------------------------------------------------------------
-psi_status psi_linear_paged(psi_arena* a, const void* X, int64_t N, int64_t K,
-                            const psi_linear_weight* W, const void* bias, const void* residual,
-                            void* Y, int64_t ldy, uint32_t flags) {
+static psi_status linear_paged(psi_arena* a, const void* X, int64_t N, int64_t K,
+                               const psi_linear_weight* W, const void* bias,
+                               const void* residual, void* Y, int64_t ldy, uint32_t flags,
+                               const psi_rope* rope) {
   if (!a || !X || !W || !bias || !Y)
     return set_error(PSI_ERR_INVALID_ARG, "linear_paged: null argument");
   if (N < 0 || K <= 0 || W->cols != K || W->rows <= 0 || W->page_rows <= 0)
@@ -522,6 +523,20 @@ psi_status psi_linear_paged(psi_arena* a, const void* X, int64_t N, int64_t K,
   const size_t max_page = static_cast<size_t>(std::min(W->page_rows, W->rows)) * K * 2;
   if (!resident && max_page > a->page_bytes)
     return set_error(PSI_ERR_CAPACITY, "linear_paged: weight tile exceeds page");
+  if (rope) {
+    if (rope->dh != 64 && rope->dh != 128)
+      return set_error(PSI_ERR_UNSUPPORTED, "linear_rope_paged: dh must be 64 or 128");
+    if (!rope->cos || !rope->sin || !aligned16(rope->cos) || !aligned16(rope->sin) ||
+        rope->ld % 4 || rope->ld < rope->dh / 2)
+      return set_error(PSI_ERR_INVALID_ARG,
+                       "linear_rope_paged: tables must be 16-byte aligned, ld % 4 == 0, ld >= dh/2");
+    if (rope->cols < 0 || rope->cols % rope->dh || rope->cols > W->rows)
+      return set_error(PSI_ERR_INVALID_ARG,
+                       "linear_rope_paged: cols must be whole heads within the output");
+    if (W->page_rows < W->rows && W->page_rows % rope->dh)
+      return set_error(PSI_ERR_INVALID_ARG,
+                       "linear_rope_paged: page_rows must be a multiple of dh");
+  }
   const int64_t npages = (W->rows + W->page_rows - 1) / W->page_rows;
   DevError* err = dev_error_ptr();
   // pages alternate between the compute and the auxiliary stream (outputs are
@@ -554,6 +569,14 @@ psi_status psi_linear_paged(psi_arena* a, const void* X, int64_t N, int64_t K,
     g.resid = residual ? static_cast<const uint16_t*>(residual) + r0 : nullptr;
     g.out = static_cast<uint16_t*>(Y) + r0;
     g.ldo = ldy;
+    if (rope && rope->cols > r0) {
+      g.rope_dh = rope->dh;
+      g.rope_cols = static_cast<int32_t>(std::min(rope->cols - r0, rows_p));
+      g.rope_after_bf16 = (flags & PSI_ROPE_AFTER_BF16) ? 1 : 0;
+      g.rope_cos = rope->cos;
+      g.rope_sin = rope->sin;
+      g.rope_ld = rope->ld;
+    }
     g.err = err;
     g.timeout_ns = kWaitLimitNs;
     psi_status st = arena_gemm(a, cs, X, K, dev, K, g);
@@ -561,6 +584,42 @@ psi_status psi_linear_paged(psi_arena* a, const void* X, int64_t N, int64_t K,
     if (!resident && (st = page_release_on(a, pg, cs)) != PSI_OK) return st;
   }
   return stream_after(a->ev_join, a->aux, a->compute);
+}
+
+psi_status psi_linear_paged(psi_arena* a, const void* X, int64_t N, int64_t K,
+                            const psi_linear_weight* W, const void* bias, const void* residual,
+                            void* Y, int64_t ldy, uint32_t flags) {
+  return linear_paged(a, X, N, K, W, bias, residual, Y, ldy, flags, nullptr);
+}
+
+psi_status psi_linear_rope_paged(psi_arena* a, const void* X, int64_t N, int64_t K,
+                                 const psi_linear_weight* W, const void* bias,
+                                 const psi_rope* rope, void* Y, int64_t ldy, uint32_t flags) {
+  if (!rope) return set_error(PSI_ERR_INVALID_ARG, "linear_rope_paged: null rope table");
+  return linear_paged(a, X, N, K, W, bias, nullptr, Y, ldy, flags, rope);
+}
+
+psi_status psi_rmsnorm(const void* X, int64_t ldx, int64_t N, int64_t d, const void* gamma,
+                       float eps, void* Y, int64_t ldy, void* stream) {
+  if (!X || !gamma || !Y) return set_error(PSI_ERR_INVALID_ARG, "rmsnorm: null argument");
+  if (N < 0 || d < 1 || d % 8 || ldx < d || ldy < d || ldx % 8 || ldy % 8)
+    return set_error(PSI_ERR_INVALID_ARG,
+                     "rmsnorm: need d, ldx, ldy multiples of 8 with ldx, ldy >= d");
+  if (d > 8192) return set_error(PSI_ERR_UNSUPPORTED, "rmsnorm: this build handles d <= 8192");
+  if (!(eps >= 0.0f) || !std::isfinite(eps))
+    return set_error(PSI_ERR_INVALID_ARG, "rmsnorm: eps must be finite and >= 0");
+  if (!aligned16(X) || !aligned16(Y) || !aligned16(gamma))
+    return set_error(PSI_ERR_INVALID_ARG, "rmsnorm: pointers must be 16-byte aligned");
+  {
+    const auto x0 = reinterpret_cast<uintptr_t>(X), y0 = reinterpret_cast<uintptr_t>(Y);
+    const uintptr_t xb = static_cast<uintptr_t>(((N - 1) * ldx + d) * 2);
+    const uintptr_t yb = static_cast<uintptr_t>(((N > 0 ? N - 1 : 0) * ldy + d) * 2);
+    if (N > 0 && x0 < y0 + yb && y0 < x0 + xb)
+      return set_error(PSI_ERR_INVALID_ARG, "rmsnorm: Y must not overlap X");
+  }
+  if (N > 0x7FFFFFFF) return set_error(PSI_ERR_UNSUPPORTED, "rmsnorm: row count above 2^31");
+  if (N == 0) return PSI_OK;
+  return launch_rmsnorm(X, ldx, N, d, gamma, eps, Y, ldy, static_cast<cudaStream_t>(stream));
 }
 
 psi_status psi_ffn_paged(psi_arena* a, const void* X, int64_t N, const psi_ffn_weight* W,

@@ -29,6 +29,7 @@ PSI_SYNC_COPY = 0x2
 PSI_BOUNDARY_PREGELU_BF16 = 0x4
 PSI_BIAS_AFTER_BF16 = 0x8
 PSI_ATTN_BF16_WEIGHTS = 0x10
+PSI_ROPE_AFTER_BF16 = 0x20
 
 # every entry point include/psi.h declares
 EXPORTS = [
@@ -38,7 +39,8 @@ EXPORTS = [
     "psi_page_stream", "psi_page_release", "psi_sync", "psi_stream_wait",
     "psi_arena_stats", "psi_arena_reset_stats", "psi_arena_set_timing",
     "psi_arena_fail_next_copy", "psi_debug_stall_next_gemm",
-    "psi_linear_paged", "psi_ffn_paged", "psi_attn_partitioned",
+    "psi_linear_paged", "psi_linear_rope_paged", "psi_rmsnorm",
+    "psi_ffn_paged", "psi_attn_partitioned",
     "psi_ffn_resident_noalloc",
 ]
 
@@ -62,6 +64,11 @@ class psi_linear_weight(C.Structure):
 class psi_ffn_weight(C.Structure):
     _fields_ = [("host", C.c_void_p), ("dev_resident", C.c_void_p), ("d", C.c_int64),
                 ("h", C.c_int64), ("r", C.c_int64), ("slice", C.c_int64)]
+
+
+class psi_rope(C.Structure):
+    _fields_ = [("cos", C.c_void_p), ("sin", C.c_void_p), ("ld", C.c_int64),
+                ("cols", C.c_int64), ("dh", C.c_int32), ("pad_", C.c_int32)]
 
 
 class psi_heads(C.Structure):
@@ -123,6 +130,9 @@ def load(path: str = LIB_PATH) -> C.CDLL:
         "psi_debug_stall_next_gemm": (st, [C.c_uint64]),
         "psi_linear_paged": (st, [vp, vp, i64, i64, C.POINTER(psi_linear_weight), vp, vp,
                                   vp, i64, u32]),
+        "psi_linear_rope_paged": (st, [vp, vp, i64, i64, C.POINTER(psi_linear_weight), vp,
+                                       C.POINTER(psi_rope), vp, i64, u32]),
+        "psi_rmsnorm": (st, [vp, i64, i64, i64, vp, C.c_float, vp, i64, vp]),
         "psi_ffn_paged": (st, [vp, vp, i64, C.POINTER(psi_ffn_weight), vp, vp, vp, vp, vp,
                                vp, u32]),
         "psi_attn_partitioned": (st, [C.POINTER(psi_heads)] * 4 +
@@ -236,6 +246,17 @@ def psi_linear_paged(arena: int, X: int, N: int, K: int, W: psi_linear_weight, b
                      residual: int | None, Y: int, ldy: int, flags: int = 0):
     _check(load().psi_linear_paged(arena, X, N, K, C.byref(W), bias, residual or None, Y,
                                    ldy, flags))
+
+
+def psi_linear_rope_paged(arena: int, X: int, N: int, K: int, W: psi_linear_weight, bias: int,
+                          rope: psi_rope, Y: int, ldy: int, flags: int = 0):
+    _check(load().psi_linear_rope_paged(arena, X, N, K, C.byref(W), bias, C.byref(rope), Y,
+                                        ldy, flags))
+
+
+def psi_rmsnorm(X: int, ldx: int, N: int, d: int, gamma: int, eps: float, Y: int, ldy: int,
+                stream: int):
+    _check(load().psi_rmsnorm(X, ldx, N, d, gamma, eps, Y, ldy, stream))
 
 
 def psi_ffn_paged(arena: int, X: int, N: int, W: psi_ffn_weight, a: int, b: int,
