@@ -181,14 +181,17 @@ class Workload:
 
 
 class BlockWorkload(Workload):
-    def __init__(self, torch, dev, blocks=1, arena_mib=80, resident=False):
+    def __init__(self, torch, dev, blocks=1, arena_mib=80, resident=False, prenorm=False,
+                 branches=1, journal=False):
         import psi_synth
         from weight_streamed_bf16_gb300.block import BlockRunner, BlockShape, BlockWeights
         from weight_streamed_bf16_gb300.torch_io import Arena, pinned_like
         cfg = psi_synth.BLOCK
         self.torch = torch
+        self.prenorm = prenorm
         self.shape = BlockShape(d=cfg.d, N=cfg.N, heads=cfg.heads, dh=cfg.dh,
-                                hidden=cfg.hidden, slice=cfg.slice, page_bytes=cfg.page_bytes)
+                                hidden=cfg.hidden, slice=cfg.slice, page_bytes=cfg.page_bytes,
+                                prenorm=prenorm, eps=cfg.eps)
         self.blocks = []
         for b in range(blocks):
             w = psi_synth.block_weights(cfg, block=b, device=dev)  # drawn on the GPU
@@ -196,23 +199,39 @@ class BlockWorkload(Workload):
             # FFN weights are packed into a pinned page image by BlockWeights
             w = {k: (pinned_like(v.cpu()) if k in ("Wqkv", "Wo") else
                      (v.cpu() if v.dim() == 2 else v)) for k, v in w.items()}
+            if prenorm:
+                w["gamma1"], w["gamma2"] = psi_synth.norm_gains(cfg, block=b, device=dev)
             self.blocks.append(BlockWeights(w, self.shape, resident=resident, device=dev))
             del w
         slots = arena_mib * MiB // cfg.page_bytes
         self.arena = Arena(cfg.page_bytes, slots, device=dev)
-        self.runner = BlockRunner(self.shape, self.arena, device=dev)
-        self.X = psi_synth.block_input(cfg, device=dev)
+        self.runner = BlockRunner(self.shape, self.arena, device=dev,
+                                  rope=psi_synth.rope_table(cfg.N, cfg.dh) if prenorm else None)
+        self.branches = branches
+        self.journal = None
+        X0 = psi_synth.block_input(cfg, device=dev)
+        if branches > 1 or journal:
+            # branch r's input: the block input scaled by 2^-r (distinct bytes)
+            self.X = torch.stack([X0 * (0.5 ** r) for r in range(branches)])
+        else:
+            self.X = X0
         self.Y = torch.empty_like(self.X)
-        self.tmp = torch.empty_like(self.X)
+        self.tmp = torch.empty_like(X0)
+        if journal:
+            from weight_streamed_bf16_gb300.torch_io import Journal
+            self.journal = Journal(self.arena, cfg.N * cfg.d * 2, 2 * branches)
         self.flags = 1 if resident else 0
-        self.flops = float(cfg.flops) * blocks
-        self.linear_flops = float(cfg.linear_flops) * blocks
-        self.weight_h2d = 0 if resident else cfg.weight_bytes * blocks
-        self.name = (f"synthetic transformer block x{blocks}: d_model {cfg.d}, {cfg.N} tokens, "
+        self.flops = float(cfg.flops) * blocks * branches
+        self.linear_flops = float(cfg.linear_flops) * blocks * branches
+        self.weight_h2d = 0 if resident else cfg.weight_bytes * blocks * branches
+        self.name = (("pre-norm (RMSNorm, split RoPE on Q/K) " if prenorm else "") +
+                     f"synthetic transformer block x{blocks}: d_model {cfg.d}, {cfg.N} tokens, "
                      f"{cfg.heads} heads x {cfg.dh}, QKV {cfg.qkv_rows}x{cfg.d} + out "
                      f"{cfg.d}x{cfg.d} + FFN {cfg.d}->{cfg.hidden}->{cfg.d} tanh-GELU, "
                      f"{cfg.page_bytes // MiB} MiB pages, {arena_mib} MiB arena "
-                     f"({slots} slots), weights {'resident' if resident else 'streamed from pinned host'}")
+                     f"({slots} slots), weights {'resident' if resident else 'streamed from pinned host'}" +
+                     (f", {branches} branch states" if branches > 1 or journal else "") +
+                     (" kept in the host journal (3 device state buffers)" if journal else ""))
 
     @property
     def stream(self):
@@ -221,7 +240,16 @@ class BlockWorkload(Workload):
     def step(self, X=None, Y=None, marks=None):
         X = self.X if X is None else X
         Y = self.Y if Y is None else Y
-        if len(self.blocks) == 1:
+        if self.journal is not None:
+            # branch inputs read from X[r], outputs written to Y[r]; every
+            # intermediate state lives in the host journal
+            self.runner.run_branches(self.blocks, self.journal, self.branches, self.flags,
+                                     inputs=[X[r] for r in range(self.branches)],
+                                     outputs=[Y[r] for r in range(self.branches)])
+        elif X.dim() == 3:
+            for r in range(X.shape[0]):
+                self.runner.stack(X[r], self.blocks, Y[r], self.tmp, self.flags)
+        elif len(self.blocks) == 1:
             self.runner.forward(X, self.blocks[0], Y, self.flags, marks)
         else:
             self.runner.stack(X, self.blocks, Y, self.tmp, self.flags)
@@ -230,17 +258,19 @@ class BlockWorkload(Workload):
         """Per-operator time of a single block on the compute stream (ms):
         QKV projection, attention, out-projection, FFN."""
         torch = self.torch
-        if len(self.blocks) != 1:
+        if len(self.blocks) != 1 or self.X.dim() == 3:
             return None
-        tot = [0.0] * 4
+        names = (["norm1", "qkv_rope", "attention", "out_proj", "norm2", "ffn"] if self.prenorm
+                 else ["qkv", "attention", "out_proj", "ffn"])
+        tot = [0.0] * len(names)
         for _ in range(steps):
-            marks = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+            marks = [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
             with torch.cuda.stream(self.stream):
                 self.step(marks=marks)
-            marks[4].synchronize()
-            for i in range(4):
+            marks[-1].synchronize()
+            for i in range(len(names)):
                 tot[i] += marks[i].elapsed_time(marks[i + 1])
-        return {k: v / steps for k, v in zip(["qkv", "attention", "out_proj", "ffn"], tot)}
+        return {k: v / steps for k, v in zip(names, tot)}
 
     def io(self):
         return self.X, self.Y
@@ -416,9 +446,10 @@ def psi_weight_bytes():
 
 def make_workload(torch, dev, args):
     if args.workload == "block":
-        return BlockWorkload(torch, dev, 1, args.arena_mib, args.resident)
+        return BlockWorkload(torch, dev, 1, args.arena_mib, args.resident, args.prenorm)
     if args.workload == "stack":
-        return BlockWorkload(torch, dev, args.blocks, args.arena_mib, args.resident)
+        return BlockWorkload(torch, dev, args.blocks, args.arena_mib, args.resident, args.prenorm,
+                             args.branches, args.journal)
     if args.workload == "ffn":
         return FfnWorkload(torch, dev)
     if args.workload == "linear":
@@ -556,6 +587,12 @@ def main():
     ap.add_argument("--resident", action="store_true", help="weights resident (no streaming)")
     ap.add_argument("--key-block", type=int, default=None,
                     help="attention workload: keys per online-softmax block (default 256)")
+    ap.add_argument("--prenorm", action="store_true",
+                    help="block/stack: pre-norm block (RMSNorm before QKV and FFN, split RoPE)")
+    ap.add_argument("--branches", type=int, default=1,
+                    help="stack: independent branch states run through every block")
+    ap.add_argument("--journal", action="store_true",
+                    help="stack: keep branch states in the host journal (3 device buffers)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true",
                     help="stack workload: arena sweep 32/80/256 MiB + resident, bitwise control")
@@ -603,7 +640,9 @@ def main():
         arena.sync()
         psi.psi_arena_reset_stats(arena.handle)
         psi.psi_arena_set_timing(arena.handle, True)
+    j0 = wl.journal.stats() if getattr(wl, "journal", None) is not None else None
     attn0 = getattr(getattr(wl, "runner", None), "attn_launches", 0)
+    norm0 = getattr(getattr(wl, "runner", None), "norm_launches", 0)
 
     # ------------------------------------------------ device-timed region --
     try:
@@ -634,9 +673,19 @@ def main():
             pass
     else:
         st = None
+    jst = None
+    if getattr(wl, "journal", None) is not None:
+        js = wl.journal.stats()
+        jst = {k: (js[k] - j0[k]) / args.steps
+               for k in ("commits", "reloads", "d2h_bytes", "h2d_bytes", "host_waits",
+                         "hazard_waits")}
+        jst["per"] = "step"
+        js = {k: js[k] - j0[k] for k in ("d2h_bytes", "h2d_bytes")}
+        jst["d2h_gbs_per_step_time"] = js["d2h_bytes"] / (total_ms * 1e-3) / 1e9
+        jst["h2d_gbs_per_step_time"] = js["h2d_bytes"] / (total_ms * 1e-3) / 1e9
     gpu_launches = (st["kernels_launched"] if st else 0)
     if hasattr(wl, "runner"):
-        gpu_launches += wl.runner.attn_launches - attn0
+        gpu_launches += wl.runner.attn_launches - attn0 + wl.runner.norm_launches - norm0
     elif isinstance(wl, AttentionWorkload):
         gpu_launches += args.steps
     total_ms, ms_per_step, value = aggregate_ranks(dist, dev, total_ms, wl.flops, args.steps,
@@ -701,6 +750,32 @@ def main():
                 "traffic": profile_traffic("attention_traffic.txt",
                                            source_digest("attention.cu", "ptx.cuh"))}
 
+    norm_roof = None
+    if getattr(wl, "prenorm", False) and wl.X.dim() == 2:
+        # the RMSNorm kernel timed alone, one launch per event pair with L2
+        # flushed before each (X and Y together fit in L2); algorithmic
+        # bytes = read X + write Y + gamma
+        import psi_synth
+        c = psi_synth.BLOCK
+        nb = 2 * c.N * c.d * 2 + 2 * c.d
+        r = wl.runner
+        reps = 10
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(reps)]
+        with torch.cuda.stream(stream):
+            for e0, e1 in evs:
+                flush.fill_(1)
+                e0.record(stream)
+                psi.psi_rmsnorm(wl.X.data_ptr(), c.d, c.N, c.d, wl.blocks[0].gamma1.data_ptr(),
+                                c.eps, r.xn.data_ptr(), c.d, stream.cuda_stream)
+                e1.record(stream)
+        evs[-1][1].synchronize()
+        us = sum(a.elapsed_time(b) for a, b in evs) * 1e3 / reps
+        g = nb / (us * 1e-6) / 1e9
+        norm_roof = {"kernel": "rmsnorm", "bound": "hbm", "avg_launch_us": us, "achieved": g,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": g / peaks["hbm_gbs"],
+                     "bytes_per_launch": nb}
+
     ingest = None
     if st and st["timed_copies"]:
         ce = st["copy_bytes"] / (st["copy_ms"] * 1e-3) / 1e9
@@ -731,9 +806,9 @@ def main():
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "flops_per_step": wl.flops, "wall_s_timed": t_wall,
                        "step_roofline_ms": step_bound_ms,
-                       "phase_ms": phases,
+                       "phase_ms": phases, "rmsnorm_roofline": norm_roof,
                        "frac_of_step_roofline": step_bound_ms / ms_per_step},
-            "roofline": roof, "ingest": ingest, "cpu_baseline": cpu,
+            "roofline": roof, "ingest": ingest, "journal": jst, "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step":
                     in_bytes + wl.weight_h2d, "d2h_bytes_per_step": out_bytes,
                     "ms_per_step": e2e_ms / args.steps},

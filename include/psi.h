@@ -314,6 +314,82 @@ psi_status psi_attn_partitioned(const psi_heads* Q, const psi_heads* K,
                                 float scale, int32_t key_block, void* stream,
                                 uint32_t flags);
 
+/* ------------------------------------------------------ state journal --- */
+/* Indexed host BF16 journal, section II-D (with the asynchronous pinned-host
+ * transport of section III-B): inactive state tensors are kept in a pinned
+ * host region, indexed by (block, branch, role), so that only the live state
+ * occupies device memory (the S_live term of Eq.(1)).
+ *
+ * The host region is cut into equal slots; an entry takes one slot.  The
+ * journal owns two copy streams (D2H and H2D, so both directions run at
+ * once) and orders every copy against the arena's compute stream:
+ *   - commit:  the D2H copy waits for the producer (the compute stream's
+ *              position at the call); the entry becomes valid when the copy
+ *              completes;
+ *   - reload:  the H2D copy waits for the entry to be valid, for the
+ *              consumers of the destination (the compute stream's position at
+ *              the call) and for every journal copy still reading the
+ *              destination; the compute stream waits for it only at
+ *              psi_journal_acquire, so a reload can run ahead of the work
+ *              enqueued before the acquire;
+ *   - a slot is rewritten only after its last reload has read it.
+ * The steady state needs no host-blocking wait.  Copies are byte-preserving:
+ * a reloaded tensor is bitwise the committed one.  One journal per arena,
+ * used by one host thread at a time. */
+typedef struct psi_journal psi_journal;
+
+typedef struct {
+  int32_t block;
+  int32_t branch;
+  int32_t role;
+} psi_key;
+
+typedef struct {
+  uint64_t commits;          /* D2H copies enqueued */
+  uint64_t reloads;          /* H2D copies enqueued */
+  uint64_t d2h_bytes;
+  uint64_t h2d_bytes;
+  uint64_t host_waits;       /* host-blocking waits (psi_journal_host_view) */
+  uint64_t hazard_waits;     /* cross-stream waits added for device-range hazards */
+  int32_t slots_in_use;
+  int32_t slots_total;
+} psi_journal_stats;
+
+/* host_base: pinned host memory (cudaHostAlloc/cudaHostRegister; pageable
+ * memory is refused with PSI_ERR_INVALID_ARG), 16-byte aligned, host_bytes
+ * >= slot_bytes; slot_bytes: a multiple of 256, the largest entry. */
+psi_status psi_journal_create(psi_arena* arena, void* host_base, size_t host_bytes,
+                              size_t slot_bytes, psi_journal** out);
+/* Waits (without limit) for the journal's copies, then frees its streams and
+ * events. */
+psi_status psi_journal_destroy(psi_journal* j);
+
+/* Journal `bytes` of device memory at dev_src under `key` (replacing an
+ * earlier entry of that key).  PSI_ERR_CAPACITY if bytes > slot_bytes or no
+ * slot is free.  dev_src must not be written until the copy has read it:
+ * call psi_journal_fence on the range first (the journal's own reloads
+ * already wait for it). */
+psi_status psi_journal_commit(psi_journal* j, psi_key key, const void* dev_src, size_t bytes);
+/* Copy the entry of `key` into dev_dst (bytes must equal the committed
+ * size; PSI_ERR_INVALID_ARG for an unknown key or another size). */
+psi_status psi_journal_reload(psi_journal* j, psi_key key, void* dev_dst, size_t bytes);
+/* The compute stream waits for the latest reload of `key`
+ * (PSI_ERR_INVALID_ARG if there is none since the last acquire or commit). */
+psi_status psi_journal_acquire(psi_journal* j, psi_key key);
+/* The compute stream waits for every journal copy that reads or writes
+ * [dev_ptr, dev_ptr + bytes) (none: no wait). */
+psi_status psi_journal_fence(psi_journal* j, const void* dev_ptr, size_t bytes);
+/* Free the entry's slot (its last reload still completes first). */
+psi_status psi_journal_drop(psi_journal* j, psi_key key);
+/* Host view of a committed entry: waits for its D2H copy (bounded by
+ * timeout_ms; PSI_ERR_TIMEOUT) and returns the host address and size. */
+psi_status psi_journal_host_view(psi_journal* j, psi_key key, int64_t timeout_ms,
+                                 const void** host_ptr, size_t* bytes);
+psi_status psi_journal_get_stats(const psi_journal* j, psi_journal_stats* out);
+/* Test hook: the next commit or reload fails with PSI_ERR_CUDA before it
+ * enqueues anything (host-side fault injection). */
+psi_status psi_journal_fail_next_copy(psi_journal* j);
+
 /* ------------------------------------------------- no-allocation FFN --- */
 /* The paper has no counterpart of this entry point; it serves callers that
  * cannot allocate device memory (code running inside another framework's

@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpsi.so")
 SOURCES = ["common.cu", "page_gemm.cu", "page_gemm_pair.cu", "attention.cu", "norm.cu", "runtime.cpp",
-           "noalloc.cu"]
+           "journal.cpp", "noalloc.cu"]
 HEADERS = ["internal.h", "ptx.cuh", "gemm_epilogue.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

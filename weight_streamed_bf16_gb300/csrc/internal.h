@@ -18,7 +18,7 @@ struct DevError {
   int info1;
 };
 
-enum KernelId : int { KID_GEMM = 1, KID_ATTN = 2 };
+enum KernelId : int { KID_GEMM = 1, KID_ATTN = 2, KID_NORM = 3 };
 
 // Returns the device address of the error record on the current device.
 DevError* dev_error_ptr();

@@ -1,63 +1,132 @@
 // norm.cu -- full-row RMS normalisation (PSI section II-B): every width
 // tile of a row is scaled by the one denominator sqrt(s/d + eps) formed
-// from the global sum of squares s.  HBM-bound: one read of X and one BF16
-// write of Y; gamma stays in L1/L2.
+// from the global sum of squares s.
 //
-// One warp per row.  The row lives in registers (NV 16-byte vectors per
-// lane, lane-strided so each warp load instruction covers 512 contiguous
-// bytes); each lane's partial sum over its vectors and a butterfly over the
-// lanes give s, i.e. the sum is taken over width partitions (one per lane)
-// and combined once, in a fixed order.
+// HBM-bound: one read of X and one BF16 write of Y.  A persistent CTA per
+// SM stages whole rows in shared memory with untiled bulk copies (one
+// producer thread keeps a ring of up to 24 rows in flight), consumer warps
+// normalise a row in place in shared memory, and a bulk store writes it
+// back, so the copy engine, not registers, holds the bytes in flight.
+// gamma is staged once per CTA.
+//
+// Sum of squares: each lane adds the squares of its lane-strided 8-element
+// vectors (the width partitions), then a butterfly over the 32 lanes
+// combines them: one fixed order, one denominator per row.
+#include <algorithm>
 #include "internal.h"
 #include "ptx.cuh"
 
 namespace psi {
 namespace {
 
-constexpr int kNormWarps = 8;
+constexpr int kConsumerWarps = 8;
+constexpr int kNormThreads = 32 * (1 + kConsumerWarps);
+constexpr int kStageBudget = 200 * 1024;  // shared bytes for gamma and the row ring
+constexpr int kMaxStages = 24;
 
-template <int NV>
-__global__ void __launch_bounds__(kNormWarps * 32)
-    rmsnorm_kernel(const uint16_t* __restrict__ X, int64_t ldx, int N, int d,
-                   const uint16_t* __restrict__ gamma, float eps, uint16_t* __restrict__ Y,
-                   int64_t ldy) {
-  // rows up to 4096 wide stay in registers between the two passes; wider
-  // rows are read twice (the second read hits L2)
-  constexpr bool kKeep = NV <= 16;
-  const int lane = threadIdx.x & 31;
-  const int nv = d >> 3;  // 16-byte vectors per row
-  const uint4* g4 = reinterpret_cast<const uint4*>(gamma);
-  for (int row = blockIdx.x * kNormWarps + (threadIdx.x >> 5); row < N;
-       row += gridDim.x * kNormWarps) {
-    const uint4* x4 = reinterpret_cast<const uint4*>(X + static_cast<int64_t>(row) * ldx);
-    uint4 v[kKeep ? NV : 1];
-    float ss = 0.f;
-#pragma unroll
-    for (int i = 0; i < NV; ++i) {
-      const int idx = i * 32 + lane;
-      uint4 x = make_uint4(0, 0, 0, 0);
-      if (idx < nv) x = kKeep ? __ldcs(x4 + idx) : __ldg(x4 + idx);
-      if constexpr (kKeep) v[i] = x;
-      const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const float a = bf16_lo(w[t]), b = bf16_hi(w[t]);
-        ss = fmaf(a, a, ss);
-        ss = fmaf(b, b, ss);
+__device__ __forceinline__ void norm_error(DevError* e, int role, int i0, int i1) {
+  if (atomicCAS(&e->code, 0, 1) == 0) {
+    e->where = KID_NORM * 16 + role;
+    e->info0 = i0;
+    e->info1 = i1;
+  }
+}
+
+struct NormArgs {
+  const uint16_t* X;
+  int64_t ldx;
+  uint16_t* Y;
+  int64_t ldy;
+  const uint16_t* gamma;
+  int N;
+  int d;
+  int stages;
+  float eps;
+  DevError* err;
+  uint64_t timeout_ns;
+};
+
+__global__ void __launch_bounds__(kNormThreads, 1) rmsnorm_kernel(NormArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t full[kMaxStages], empty[kMaxStages], gbar;
+  __shared__ int abort_flag;
+  __shared__ int n_issued;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rb = static_cast<uint32_t>(a.d) * 2;          // row bytes
+  const uint32_t stage_bytes = (rb + 127) & ~127u;
+  uint8_t* sg = smem;                                          // gamma
+  uint8_t* ring = smem + stage_bytes;
+  const int S = a.stages;
+  const int nrows = a.N > static_cast<int>(blockIdx.x)
+                        ? (a.N - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1
+                        : 0;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(&gbar, 1);
+    abort_flag = 0;
+    n_issued = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    // ------------------------------------------------------- producer --
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&gbar, rb);
+      bulk_load(sg, a.gamma, rb, &gbar);
+      for (int k = 0; k < nrows; ++k) {
+        const int s = k % S;
+        if (k >= S && !mbar_wait(&empty[s], ((k / S) - 1) & 1, &abort_flag, a.timeout_ns)) {
+          norm_error(a.err, 0, k, s);
+          abort_flag = 1;
+          break;
+        }
+        const int row = static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x);
+        mbar_arrive_expect_tx(&full[s], rb);
+        bulk_load(ring + static_cast<size_t>(s) * stage_bytes,
+                  a.X + static_cast<int64_t>(row) * a.ldx, rb, &full[s]);
+        n_issued = k + 1;
       }
     }
+  } else {
+    // ------------------------------------------------------ consumers --
+    const int c = warp - 1;
+    const int nv = a.d >> 3;  // 16-byte vectors per row
+    const float inv_d = 1.0f / static_cast<float>(a.d);
+    bool ok = mbar_wait(&gbar, 0, &abort_flag, a.timeout_ns);
+    if (!ok && lane == 0) norm_error(a.err, 1, -1, c);
+    const uint4* g4 = reinterpret_cast<const uint4*>(sg);
+    int prev_s = -1;
+    for (int k = c; ok && k < nrows; k += kConsumerWarps) {
+      const int s = k % S;
+      if (!mbar_wait(&full[s], (k / S) & 1, &abort_flag, a.timeout_ns)) {
+        if (lane == 0) norm_error(a.err, 2, k, s);
+        abort_flag = 1;
+        break;
+      }
+      uint4* r4 = reinterpret_cast<uint4*>(ring + static_cast<size_t>(s) * stage_bytes);
+      float ss = 0.f;
+#pragma unroll 4
+      for (int idx = lane; idx < nv; idx += 32) {
+        const uint4 x = r4[idx];
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-    const float r = 1.0f / sqrtf(ss / static_cast<float>(d) + eps);
-    uint4* y4 = reinterpret_cast<uint4*>(Y + static_cast<int64_t>(row) * ldy);
+        for (int t = 0; t < 4; ++t) {
+          const float lo = bf16_lo(w[t]), hi = bf16_hi(w[t]);
+          ss = fmaf(lo, lo, ss);
+          ss = fmaf(hi, hi, ss);
+        }
+      }
 #pragma unroll
-    for (int i = 0; i < NV; ++i) {
-      const int idx = i * 32 + lane;
-      if (idx < nv) {
-        uint4 x;
-        if constexpr (kKeep) x = v[i];
-        else x = __ldcs(x4 + idx);
-        const uint4 g = __ldg(g4 + idx);
+      for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+      const float r = 1.0f / sqrtf(ss * inv_d + a.eps);
+#pragma unroll 4
+      for (int idx = lane; idx < nv; idx += 32) {
+        const uint4 x = r4[idx];
+        const uint4 g = g4[idx];
         const uint32_t w[4] = {x.x, x.y, x.z, x.w};
         const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
         uint32_t o[4];
@@ -65,38 +134,73 @@ __global__ void __launch_bounds__(kNormWarps * 32)
         for (int t = 0; t < 4; ++t)
           o[t] = pack_bf16x2(bf16_lo(gw[t]) * (bf16_lo(w[t]) * r),
                              bf16_hi(gw[t]) * (bf16_hi(w[t]) * r));
-        __stcs(y4 + idx, make_uint4(o[0], o[1], o[2], o[3]));
+        r4[idx] = make_uint4(o[0], o[1], o[2], o[3]);
       }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        const int row = static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x);
+        bulk_store(a.Y + static_cast<int64_t>(row) * a.ldy, r4, rb);
+        bulk_commit();
+        // the previous row's store has read its stage: hand that stage back
+        if (prev_s >= 0) {
+          bulk_wait_read<1>();
+          mbar_arrive(&empty[prev_s]);
+        }
+      }
+      prev_s = s;
+      __syncwarp();
+    }
+    if (lane == 0) bulk_wait<0>();  // this warp's stores are complete
+  }
+  __syncthreads();
+  // every load the producer issued has landed before the CTA's shared
+  // memory is released (normally the consumers already waited for them)
+  if (threadIdx.x == 0) {
+    const int issued = n_issued;
+    for (int s = 0; s < S && s < issued; ++s) {
+      const int last_k = s + ((issued - 1 - s) / S) * S;
+      int none = 0;
+      if (!mbar_wait(&full[s], (last_k / S) & 1, &none, a.timeout_ns))
+        norm_error(a.err, 3, last_k, s);
     }
   }
-}
-
-template <int NV>
-psi_status launch_nv(const uint16_t* X, int64_t ldx, int N, int d, const uint16_t* gamma,
-                     float eps, uint16_t* Y, int64_t ldy, cudaStream_t s) {
-  const int blocks_needed = (N + kNormWarps - 1) / kNormWarps;
-  const int grid = std::min(blocks_needed, num_sms() * 8);
-  rmsnorm_kernel<NV><<<grid, kNormWarps * 32, 0, s>>>(X, ldx, N, d, gamma, eps, Y, ldy);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_error(e, "rmsnorm launch");
-  return PSI_OK;
 }
 
 }  // namespace
 
 psi_status launch_rmsnorm(const void* X, int64_t ldx, int64_t N, int64_t d, const void* gamma,
                           float eps, void* Y, int64_t ldy, cudaStream_t stream) {
-  const auto* x = static_cast<const uint16_t*>(X);
-  const auto* g = static_cast<const uint16_t*>(gamma);
-  auto* y = static_cast<uint16_t*>(Y);
-  const int n = static_cast<int>(N), dd = static_cast<int>(d);
-  const int per_lane = (static_cast<int>(d / 8) + 31) / 32;  // vectors per lane
-  if (per_lane <= 1) return launch_nv<1>(x, ldx, n, dd, g, eps, y, ldy, stream);
-  if (per_lane <= 2) return launch_nv<2>(x, ldx, n, dd, g, eps, y, ldy, stream);
-  if (per_lane <= 4) return launch_nv<4>(x, ldx, n, dd, g, eps, y, ldy, stream);
-  if (per_lane <= 8) return launch_nv<8>(x, ldx, n, dd, g, eps, y, ldy, stream);
-  if (per_lane <= 16) return launch_nv<16>(x, ldx, n, dd, g, eps, y, ldy, stream);
-  return launch_nv<32>(x, ldx, n, dd, g, eps, y, ldy, stream);
+  NormArgs a{};
+  a.X = static_cast<const uint16_t*>(X);
+  a.ldx = ldx;
+  a.Y = static_cast<uint16_t*>(Y);
+  a.ldy = ldy;
+  a.gamma = static_cast<const uint16_t*>(gamma);
+  a.N = static_cast<int>(N);
+  a.d = static_cast<int>(d);
+  a.eps = eps;
+  a.err = dev_error_ptr();
+  if (!a.err) return set_error(PSI_ERR_CUDA, "rmsnorm: kernel error record not reachable");
+  a.timeout_ns = kWaitLimitNs;
+  const int stage_bytes = static_cast<int>((d * 2 + 127) / 128 * 128);
+  a.stages = std::min(kMaxStages, (kStageBudget - stage_bytes) / stage_bytes);
+  if (a.stages <= kConsumerWarps)
+    return set_error(PSI_ERR_UNSUPPORTED, "rmsnorm: row too wide for the shared-memory ring");
+  const int smem = stage_bytes * (1 + a.stages);
+  static bool attr_set = false;  // per process; one device per process
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(rmsnorm_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kStageBudget);
+    if (e != cudaSuccess) return cuda_error(e, "rmsnorm: shared-memory attribute");
+    attr_set = true;
+  }
+  const int grid = static_cast<int>(std::min<int64_t>(N, num_sms()));
+  rmsnorm_kernel<<<grid, kNormThreads, smem, stream>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_error(e, "rmsnorm launch");
+  return PSI_OK;
 }
 
 }  // namespace psi

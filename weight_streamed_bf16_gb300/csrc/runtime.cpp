@@ -62,6 +62,12 @@ struct psi_arena {
   std::vector<cudaEvent_t> pool;
 };
 
+namespace psi {
+// the arena's compute stream and device, for the journal (journal.cpp)
+cudaStream_t arena_compute_stream(psi_arena* a) { return a->compute; }
+int arena_device(psi_arena* a) { return a->device; }
+}  // namespace psi
+
 namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }

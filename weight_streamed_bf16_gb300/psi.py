@@ -42,6 +42,9 @@ EXPORTS = [
     "psi_linear_paged", "psi_linear_rope_paged", "psi_rmsnorm",
     "psi_ffn_paged", "psi_attn_partitioned",
     "psi_ffn_resident_noalloc",
+    "psi_journal_create", "psi_journal_destroy", "psi_journal_commit", "psi_journal_reload",
+    "psi_journal_acquire", "psi_journal_fence", "psi_journal_drop", "psi_journal_host_view",
+    "psi_journal_get_stats", "psi_journal_fail_next_copy",
 ]
 
 
@@ -69,6 +72,20 @@ class psi_ffn_weight(C.Structure):
 class psi_rope(C.Structure):
     _fields_ = [("cos", C.c_void_p), ("sin", C.c_void_p), ("ld", C.c_int64),
                 ("cols", C.c_int64), ("dh", C.c_int32), ("pad_", C.c_int32)]
+
+
+class psi_key(C.Structure):
+    _fields_ = [("block", C.c_int32), ("branch", C.c_int32), ("role", C.c_int32)]
+
+
+class psi_journal_stats(C.Structure):
+    _fields_ = [("commits", C.c_uint64), ("reloads", C.c_uint64), ("d2h_bytes", C.c_uint64),
+                ("h2d_bytes", C.c_uint64), ("host_waits", C.c_uint64),
+                ("hazard_waits", C.c_uint64), ("slots_in_use", C.c_int32),
+                ("slots_total", C.c_int32)]
+
+    def as_dict(self):
+        return {k: getattr(self, k) for k, _ in self._fields_}
 
 
 class psi_heads(C.Structure):
@@ -139,6 +156,16 @@ def load(path: str = LIB_PATH) -> C.CDLL:
                                  [i32, i64, i64, i32, C.c_float, i32, vp, u32]),
         "psi_ffn_resident_noalloc": (st, [vp, i64, C.POINTER(psi_ffn_weight), vp, vp, vp, vp,
                                           vp, u32]),
+        "psi_journal_create": (st, [vp, vp, sz, sz, C.POINTER(vp)]),
+        "psi_journal_destroy": (st, [vp]),
+        "psi_journal_commit": (st, [vp, psi_key, vp, sz]),
+        "psi_journal_reload": (st, [vp, psi_key, vp, sz]),
+        "psi_journal_acquire": (st, [vp, psi_key]),
+        "psi_journal_fence": (st, [vp, vp, sz]),
+        "psi_journal_drop": (st, [vp, psi_key]),
+        "psi_journal_host_view": (st, [vp, psi_key, i64, C.POINTER(vp), C.POINTER(sz)]),
+        "psi_journal_get_stats": (st, [vp, C.POINTER(psi_journal_stats)]),
+        "psi_journal_fail_next_copy": (st, [vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -278,3 +305,55 @@ def psi_ffn_resident_noalloc(X: int, N: int, W: psi_ffn_weight, a: int, b: int,
     callers that cannot allocate device memory); see include/psi.h."""
     _check(load().psi_ffn_resident_noalloc(X, N, C.byref(W), a, b, residual or None, Y,
                                            stream, flags))
+
+
+# ------------------------------------------------------------- journal ---
+def psi_journal_create(arena: int, host: int, host_bytes: int, slot_bytes: int) -> int:
+    out = C.c_void_p()
+    _check(load().psi_journal_create(arena, host, host_bytes, slot_bytes, C.byref(out)))
+    return out.value
+
+
+def psi_journal_destroy(j: int):
+    _check(load().psi_journal_destroy(j))
+
+
+def _key(k) -> psi_key:
+    return k if isinstance(k, psi_key) else psi_key(*k)
+
+
+def psi_journal_commit(j: int, key, dev_src: int, nbytes: int):
+    _check(load().psi_journal_commit(j, _key(key), dev_src, nbytes))
+
+
+def psi_journal_reload(j: int, key, dev_dst: int, nbytes: int):
+    _check(load().psi_journal_reload(j, _key(key), dev_dst, nbytes))
+
+
+def psi_journal_acquire(j: int, key):
+    _check(load().psi_journal_acquire(j, _key(key)))
+
+
+def psi_journal_fence(j: int, dev_ptr: int, nbytes: int):
+    _check(load().psi_journal_fence(j, dev_ptr, nbytes))
+
+
+def psi_journal_drop(j: int, key):
+    _check(load().psi_journal_drop(j, _key(key)))
+
+
+def psi_journal_host_view(j: int, key, timeout_ms: int = 10000):
+    """(host address, bytes) of a committed entry, after its copy finished."""
+    p, n = C.c_void_p(), C.c_size_t()
+    _check(load().psi_journal_host_view(j, _key(key), timeout_ms, C.byref(p), C.byref(n)))
+    return p.value, n.value
+
+
+def psi_journal_get_stats(j: int) -> dict:
+    st = psi_journal_stats()
+    _check(load().psi_journal_get_stats(j, C.byref(st)))
+    return st.as_dict()
+
+
+def psi_journal_fail_next_copy(j: int):
+    _check(load().psi_journal_fail_next_copy(j))

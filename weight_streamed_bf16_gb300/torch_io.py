@@ -68,6 +68,55 @@ class Arena:
             pass
 
 
+class Journal:
+    """A host state journal over a pinned region of `slots * slot_bytes`,
+    ordered against `arena`'s compute stream."""
+
+    def __init__(self, arena: Arena, slot_bytes: int, slots: int):
+        self.arena = arena
+        self.slot_bytes = slot_bytes
+        self.host = torch.empty(slot_bytes * slots, dtype=torch.uint8, pin_memory=True)
+        self.handle = psi.psi_journal_create(arena.handle, self.host.data_ptr(),
+                                             slot_bytes * slots, slot_bytes)
+
+    def commit(self, key, t: torch.Tensor):
+        psi.psi_journal_commit(self.handle, key, t.data_ptr(), t.numel() * t.element_size())
+
+    def reload(self, key, t: torch.Tensor):
+        psi.psi_journal_reload(self.handle, key, t.data_ptr(), t.numel() * t.element_size())
+
+    def acquire(self, key):
+        psi.psi_journal_acquire(self.handle, key)
+
+    def fence(self, t: torch.Tensor):
+        psi.psi_journal_fence(self.handle, t.data_ptr(), t.numel() * t.element_size())
+
+    def drop(self, key):
+        psi.psi_journal_drop(self.handle, key)
+
+    def host_tensor(self, key, like: torch.Tensor, timeout_ms: int = 10000) -> torch.Tensor:
+        """A CPU copy of the committed entry, viewed with `like`'s dtype and
+        shape (waits for the entry's D2H copy)."""
+        addr, n = psi.psi_journal_host_view(self.handle, key, timeout_ms)
+        off = addr - self.host.data_ptr()
+        raw = self.host[off:off + n].clone()
+        return raw.view(like.dtype).view(like.shape)
+
+    def stats(self) -> dict:
+        return psi.psi_journal_get_stats(self.handle)
+
+    def close(self):
+        if self.handle:
+            psi.psi_journal_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
 class LinearWeight:
     """Host (pinned) and optional resident copies of W [rows x cols]."""
 
