@@ -354,6 +354,9 @@ class AttentionWorkload(Workload):
         self.torch = torch
         self.Q, self.K, self.V = psi_synth.attn_inputs(cfg, device=dev)
         self.O = torch.empty_like(self.Q)
+        from weight_streamed_bf16_gb300 import psi
+        nws = psi.psi_attn_workspace_size(cfg.key_block)
+        self.ws = torch.empty(nws // 4, dtype=torch.float32, device=dev)
         self._stream = torch.cuda.current_stream(dev)
         self.flops = float(cfg.flops)
         self.weight_h2d = 0
@@ -369,10 +372,11 @@ class AttentionWorkload(Workload):
         from weight_streamed_bf16_gb300.torch_io import heads_view
         Q = self.Q if X is None else X
         O = self.O if Y is None else Y
-        psi.psi_attn_partitioned(heads_view(Q), heads_view(self.K), heads_view(self.V),
-                                 heads_view(O), self.cfg.heads, self.cfg.N, self.cfg.N,
-                                 self.cfg.dh, self.cfg.scale, self.cfg.key_block,
-                                 self._stream.cuda_stream, 0)
+        psi.psi_attn_partitioned_ws(heads_view(Q), heads_view(self.K), heads_view(self.V),
+                                    heads_view(O), self.cfg.heads, self.cfg.N, self.cfg.N,
+                                    self.cfg.dh, self.cfg.scale, self.cfg.key_block,
+                                    self.ws.data_ptr(), self.ws.numel() * 4,
+                                    self._stream.cuda_stream, 0)
 
     def io(self):
         return self.Q, self.O
@@ -641,8 +645,7 @@ def main():
         psi.psi_arena_reset_stats(arena.handle)
         psi.psi_arena_set_timing(arena.handle, True)
     j0 = wl.journal.stats() if getattr(wl, "journal", None) is not None else None
-    attn0 = getattr(getattr(wl, "runner", None), "attn_launches", 0)
-    norm0 = getattr(getattr(wl, "runner", None), "norm_launches", 0)
+    k0 = psi.psi_kernel_launches()
 
     # ------------------------------------------------ device-timed region --
     try:
@@ -662,6 +665,7 @@ def main():
             wl.step()
             ev[i][1].record(stream)
     barrier()
+    k1 = psi.psi_kernel_launches()
     t_wall = time.perf_counter() - t_wall
     clk = clocks.stop()
     step_ms = [a.elapsed_time(b) for a, b in ev]
@@ -683,11 +687,8 @@ def main():
         js = {k: js[k] - j0[k] for k in ("d2h_bytes", "h2d_bytes")}
         jst["d2h_gbs_per_step_time"] = js["d2h_bytes"] / (total_ms * 1e-3) / 1e9
         jst["h2d_gbs_per_step_time"] = js["h2d_bytes"] / (total_ms * 1e-3) / 1e9
-    gpu_launches = (st["kernels_launched"] if st else 0)
-    if hasattr(wl, "runner"):
-        gpu_launches += wl.runner.attn_launches - attn0 + wl.runner.norm_launches - norm0
-    elif isinstance(wl, AttentionWorkload):
-        gpu_launches += args.steps
+    # the library's own count of the kernels it launched in the timed region
+    gpu_launches = k1 - k0
     total_ms, ms_per_step, value = aggregate_ranks(dist, dev, total_ms, wl.flops, args.steps,
                                                    world)
 

@@ -220,6 +220,9 @@ psi_status psi_sync(psi_arena* arena, int64_t timeout_ms);
 psi_status psi_stream_wait(void* stream, int64_t timeout_ms);
 
 psi_status psi_arena_stats(const psi_arena* arena, psi_stats* out);
+/* Kernels the library has launched in this process, over every entry point
+ * and device (a monotonic count). */
+uint64_t psi_kernel_launches(void);
 psi_status psi_arena_reset_stats(psi_arena* arena);
 /* enable != 0: bracket every page GEMM (compute stream) and every H2D copy
  * (copy stream) with CUDA events; psi_arena_stats sums them (it waits for
@@ -313,6 +316,22 @@ psi_status psi_attn_partitioned(const psi_heads* Q, const psi_heads* K,
                                 int32_t heads, int64_t Nq, int64_t Nk, int32_t dh,
                                 float scale, int32_t key_block, void* stream,
                                 uint32_t flags);
+/* The same with a device workspace (16-byte aligned, at least
+ * psi_attn_workspace_size bytes) for the tail split: the kernel runs one
+ * CTA per SM and (head, query tile) units; when the last wave of units is
+ * partial, each of its units is cut into ranges of whole key blocks, one
+ * CTA per range, and a second kernel combines the ranges' FP32 states
+ * (m, l, z) by the update of Eq.(4) before the one BF16 write.  Only the
+ * rounding of those units changes.  No split with PSI_ATTN_BF16_WEIGHTS
+ * (its rounded weights follow the kernel's running maximum).
+ * workspace NULL: no split (psi_attn_partitioned). */
+psi_status psi_attn_partitioned_ws(const psi_heads* Q, const psi_heads* K,
+                                   const psi_heads* V, const psi_heads* O,
+                                   int32_t heads, int64_t Nq, int64_t Nk, int32_t dh,
+                                   float scale, int32_t key_block, void* workspace,
+                                   size_t workspace_bytes, void* stream, uint32_t flags);
+/* Workspace bytes psi_attn_partitioned_ws needs on the current device. */
+psi_status psi_attn_workspace_size(int32_t key_block, size_t* bytes);
 
 /* ------------------------------------------------------ state journal --- */
 /* Indexed host BF16 journal, section II-D (with the asynchronous pinned-host

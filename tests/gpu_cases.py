@@ -80,15 +80,23 @@ def run_ffn(X, U, V, a, b, slice_, slots, flags=0, residual=None, return_hidden=
     return Y.cpu()
 
 
-def run_attention(Q, K, V, scale, key_block=128, O=None):
-    """Q [H x Nq x dh], K, V [H x Nk x dh] (device bf16 views); returns O."""
+def run_attention(Q, K, V, scale, key_block=128, O=None, split=False, flags=0):
+    """Q [H x Nq x dh], K, V [H x Nk x dh] (device bf16 views); returns O.
+    ``split``: pass a workspace, so a partial last wave is split by keys."""
     H, Nq, dh = Q.shape
     Nk = K.shape[1]
     if O is None:
         O = torch.full((H, Nq, dh), float("nan"), dtype=torch.bfloat16, device=Q.device)
     s = torch.cuda.current_stream()
-    psi.psi_attn_partitioned(heads_view(Q), heads_view(K), heads_view(V), heads_view(O), H, Nq,
-                             Nk, dh, scale, key_block, s.cuda_stream)
+    if split:
+        n = psi.psi_attn_workspace_size(key_block)
+        ws = torch.full((n // 4,), float("nan"), dtype=torch.float32, device=Q.device)
+        psi.psi_attn_partitioned_ws(heads_view(Q), heads_view(K), heads_view(V), heads_view(O),
+                                    H, Nq, Nk, dh, scale, key_block, ws.data_ptr(), n,
+                                    s.cuda_stream, flags)
+    else:
+        psi.psi_attn_partitioned(heads_view(Q), heads_view(K), heads_view(V), heads_view(O), H,
+                                 Nq, Nk, dh, scale, key_block, s.cuda_stream, flags)
     psi.psi_stream_wait(s.cuda_stream, 120000)
     return O
 

@@ -141,3 +141,50 @@ def test_attention_bf16_numerator_weights(key_block):
     n_b = int(np.count_nonzero(f64(Of) != exact.y))
     n_f = int(np.count_nonzero(f64(fp32) != exact.y))
     assert n_b > 3 * n_f, (n_b, n_f)
+
+
+@pytest.mark.parametrize("key_block,H,Nq,Nk", [
+    (128, 20, 2048, 2048),   # 160 units of 256 queries: 8 tail units, 16 key ranges each
+    (256, 10, 2048, 2000),   # 160 units of 128 queries, ragged last key block
+    (128, 20, 2000, 1500),   # ragged queries in the tail units, 12 key blocks
+])
+def test_attention_tail_split(key_block, H, Nq, Nk):
+    """With a workspace, the partial last wave of (head, query tile) units
+    is split into key ranges and merged by Eq.(4)'s update; the split units
+    (the last ones: the last heads) still match the oracle, and the other
+    units are bitwise those of the unsplit kernel."""
+    Q, K, V = _qkv(H, Nq, Nk, H + Nq + Nk)
+    sc = 1 / math.sqrt(128)
+    Qd, Kd, Vd = Q.cuda(), K.cuda(), V.cuda()
+    a = run_attention(Qd, Kd, Vd, sc, key_block=key_block, split=True).cpu()
+    b = run_attention(Qd, Kd, Vd, sc, key_block=key_block).cpu()
+    assert torch.isfinite(a.float()).all()
+    rows = np.array([0, 1, 127, 128, 255, 1000, Nq - 2, Nq - 1])
+    for hd in (0, H - 2, H - 1):
+        res = ops.attention(f64(Q)[hd], f64(K)[hd], f64(V)[hd], sc, rows=rows)
+        check(a[hd][rows], res, what=f"split head {hd}")
+    # the first heads are whole units in both launches
+    assert torch.equal(a[:H // 2].view(torch.int16), b[:H // 2].view(torch.int16))
+    assert (a.float() - b.float()).abs().max().item() <= 2 ** -6
+
+
+def test_attention_tail_split_full_rows():
+    """Every row of the split units against the oracle (one tail head)."""
+    H, Nq, Nk = 20, 2048, 2048
+    Q, K, V = _qkv(H, Nq, Nk, 77)
+    sc = 1 / math.sqrt(128)
+    a = run_attention(Q.cuda(), K.cuda(), V.cuda(), sc, key_block=128, split=True).cpu()
+    res = ops.attention(f64(Q)[H - 1], f64(K)[H - 1], f64(V)[H - 1], sc)
+    check(a[H - 1], res, what="tail head, all rows")
+
+
+def test_attention_workspace_too_small():
+    Q, K, V = _qkv(1, 8, 8, 1)
+    O = torch.empty(1, 8, 128, dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(16, dtype=torch.float32, device="cuda")
+    from weight_streamed_bf16_gb300.torch_io import heads_view
+    with pytest.raises(psi.PsiError) as e:
+        psi.psi_attn_partitioned_ws(heads_view(Q.cuda()), heads_view(K.cuda()),
+                                    heads_view(V.cuda()), heads_view(O), 1, 8, 8, 128, 0.1, 128,
+                                    ws.data_ptr(), 64, torch.cuda.current_stream().cuda_stream)
+    assert e.value.status == psi.PSI_ERR_INVALID_ARG

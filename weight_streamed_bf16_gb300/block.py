@@ -99,6 +99,9 @@ class BlockRunner:
         self.att = torch.empty(s.N, s.heads * s.dh, dtype=torch.bfloat16, device=device)
         self.x1 = torch.empty(s.N, s.d, dtype=torch.bfloat16, device=device)
         self.hid, self.acc = ffn_workspace(s.N, s.d, s.slice, device)
+        # attention tail-split workspace (FP32 partial states)
+        nws = psi.psi_attn_workspace_size(s.key_block)
+        self.attn_ws = torch.empty(nws // 4, dtype=torch.float32, device=device)
         self.attn_launches = 0
         self.norm_launches = 0
 
@@ -139,8 +142,9 @@ class BlockRunner:
         k = self._heads(self.h, H * dh, s.qkv)
         v = self._heads(self.h, 2 * H * dh, s.qkv)
         o = self._heads(self.att, 0, H * dh)
-        psi.psi_attn_partitioned(q, k, v, o, H, N, N, dh, 1.0 / math.sqrt(dh), s.key_block,
-                                 cs.cuda_stream, 0)
+        psi.psi_attn_partitioned_ws(q, k, v, o, H, N, N, dh, 1.0 / math.sqrt(dh), s.key_block,
+                                    self.attn_ws.data_ptr(), self.attn_ws.numel() * 4,
+                                    cs.cuda_stream, 0)
         self.attn_launches += 1
         mark(2 + pn)
         psi.psi_linear_paged(A, self.att.data_ptr(), N, H * dh, W.out.desc(), W.bo.data_ptr(),

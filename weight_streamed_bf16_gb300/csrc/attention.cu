@@ -26,6 +26,15 @@
 //               within 2^-17 relative) and written over the row's S
 //               columns; O rescaled by eta in tensor memory when the max
 //               moves; O / l written as BF16 at the end.
+//
+// Tail split: with one CTA per SM, the last wave of (head, query tile)
+// units is usually partial.  Given a workspace, the launch keeps whole
+// units for every full wave and cuts each unit of the last wave into
+// contiguous ranges of key blocks, one CTA per range.  Such a CTA stores its
+// unnormalised state (z, m, l) in FP32; merge_kernel then combines the
+// ranges of a unit by the same update as Eq.(4) (M = max m_r,
+// l = sum 2^(m_r - M) l_r, z = sum 2^(m_r - M) z_r) and writes B(z / l).
+#include <algorithm>
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -63,6 +72,14 @@ struct AShape {
   static_assert(NT * TILE_COLS <= TM_COLS, "tensor memory");
   __device__ static uint32_t tm_s(int t) { return TILE_COLS * t; }
   __device__ static uint32_t tm_o(int t) { return TILE_COLS * t + KB; }
+};
+
+// Workspace slot of one tail-split CTA: z [NT*128 rows x 128] then (m, l)
+// per row, FP32.
+template <int NT>
+struct PartSlot {
+  static constexpr int ROWS = NT * BQ;
+  static constexpr size_t FLOATS = static_cast<size_t>(ROWS) * (DH + 2);
 };
 
 struct __align__(8) ABars {
@@ -119,10 +136,20 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int q_blocks = (args.Nq + NT * BQ - 1) / (NT * BQ);
-  const int head = blockIdx.x / q_blocks;
-  const int q0 = (blockIdx.x % q_blocks) * (NT * BQ);
   const int nsub = (args.Nk + SUB - 1) / SUB;  // K/V sub-tiles
-  const int nb = (args.Nk + KB - 1) / KB;      // online-softmax key blocks
+  const int nb_all = (args.Nk + KB - 1) / KB;  // online-softmax key blocks
+  // this CTA's unit and key-block range [jb0, jb0 + nb)
+  int unit = blockIdx.x, jb0 = 0, nb = nb_all, slot = -1;
+  if (args.pieces > 0 && static_cast<int>(blockIdx.x) >= args.units_full) {
+    slot = blockIdx.x - args.units_full;
+    unit = args.units_full + slot / args.pieces;
+    const int piece = slot % args.pieces;
+    jb0 = piece * nb_all / args.pieces;
+    nb = (piece + 1) * nb_all / args.pieces - jb0;
+  }
+  const int head = unit / q_blocks;
+  const int q0 = (unit % q_blocks) * (NT * BQ);
+  const int js0 = jb0 * KSUB;                  // first sub-tile of the range
   volatile int* abort_flag = &bars->abort_flag;
   constexpr int kWhere = KID_ATTN * 16;
 
@@ -174,8 +201,8 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
       for (int j = 0; j < nb && ok; ++j) {
         for (int kv = 0; kv < 2 && ok; ++kv) {
           for (int u = 0; u < KSUB; ++u) {
-            const int js = j * KSUB + u;
-            if (js >= nsub) break;
+            const int js = j * KSUB + u;       // sub-tile within the range
+            if (js0 + js >= nsub) break;
             const int s = js & 1;
             const uint32_t par = ((js >> 1) & 1) ^ 1;
             uint64_t* empty = kv ? &bars->v_empty[s] : &bars->k_empty[s];
@@ -190,8 +217,9 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
             const CUtensorMap* m = kv ? &tmV : &tmK;
             const View& vw = kv ? vv : vk;
             mbar_arrive_expect_tx(full, 2 * TILE64);
-            tma_load_2d(dst, m, full, head * vw.hx, head * vw.hy + js * SUB);
-            tma_load_2d(dst + TILE64, m, full, head * vw.hx + 64, head * vw.hy + js * SUB);
+            const int key0 = (js0 + js) * SUB;
+            tma_load_2d(dst, m, full, head * vw.hx, head * vw.hy + key0);
+            tma_load_2d(dst + TILE64, m, full, head * vw.hx + 64, head * vw.hy + key0);
             if (kv) {
               v_armed = (v_armed & ~(1u << s)) | (static_cast<uint32_t>(v_cnt[s] & 1) << s);
               ++v_cnt[s];
@@ -229,7 +257,7 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
         const uint32_t sQ = smem_u32(smem + A::OFF_Q + t * 2 * TILE64);
         for (int u = 0; u < KSUB; ++u) {
           const int js = j * KSUB + u;
-          if (js >= nsub) break;
+          if (js0 + js >= nsub) break;
           const int s = js & 1;
           if (t == 0) {
             if (!mbar_wait(&bars->k_full[s], (js >> 1) & 1, abort_flag, args.timeout_ns)) {
@@ -264,7 +292,7 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
           // 8(kk%2), lo 16 further), V rows 16kk.. of both 64-wide dh blocks
           for (int u = 0; u < KSUB && ok; ++u) {
             const int js = j * KSUB + u;
-            if (js >= nsub) break;
+            if (js0 + js >= nsub) break;
             const int s = js & 1;
             if (t == 0) {
               if (!mbar_wait(&bars->v_full[s], (js >> 1) & 1, abort_flag, args.timeout_ns)) {
@@ -293,7 +321,7 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
         }
         if (!ok) break;
         for (int u = 0; u < KSUB; ++u)
-          if (j * KSUB + u < nsub) mma_commit(&bars->v_empty[(j * KSUB + u) & 1]);
+          if (js0 + j * KSUB + u < nsub) mma_commit(&bars->v_empty[(j * KSUB + u) & 1]);
       }
       if (issued) {
         mma_commit(&bars->drain);
@@ -336,7 +364,7 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
       // pass 1: row extremum of this half's raw scores (max, or min for a
       // negative scale), then the other half's through shared memory
       const float c = args.scale_log2;  // scale * log2(e)
-      const int kvalid = args.Nk - j * KB;  // keys of this block that exist
+      const int kvalid = args.Nk - (jb0 + j) * KB;  // keys of this block that exist
       float ext = c >= 0.f ? -INFINITY : INFINITY;
       auto scan = [&](const uint32_t (&r)[32], int base) {
         if (kvalid >= KB) {
@@ -467,6 +495,28 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
         const float lt = h == 0 ? l + l_other : l_other + l;
         tc_fence_after();
         const int tok = q0 + t * BQ + row;
+        if (slot >= 0) {
+          // a key range of a split unit: unnormalised z, and (m, l), FP32
+          float* zs = args.part + static_cast<size_t>(slot) * PartSlot<NT>::FLOATS;
+          float* zr = zs + static_cast<size_t>(t * BQ + row) * DH;
+          constexpr int OCH = DH / 32 / SPLIT;
+#pragma unroll 1
+          for (int cc = h * OCH; cc < (h + 1) * OCH; ++cc) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(tO + cc * 32, r);
+            tmem_wait_ld();
+            float4* z4 = reinterpret_cast<float4*>(zr + cc * 32);
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              z4[u] = make_float4(__uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1]),
+                                  __uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3]));
+          }
+          if (h == 0) {
+            float* ml = zs + static_cast<size_t>(PartSlot<NT>::ROWS) * DH + 2 * (t * BQ + row);
+            ml[0] = m2;
+            ml[1] = lt;
+          }
+        } else {
         uint16_t* orow =
             args.O + head * args.o_ld_head + static_cast<int64_t>(tok) * args.o_ld_token;
         constexpr int OCH = DH / 32 / SPLIT;
@@ -487,6 +537,7 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
             }
           }
         }
+        }
       }
     }
   }
@@ -497,6 +548,41 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, A::TM_COLS);
   }
+}
+
+// Combine the key ranges of each split unit: one warp per query row, four
+// output columns per lane; ranges in their order, FP32.
+template <int NT>
+__global__ void __launch_bounds__(256) merge_kernel(const AttnArgs a, int q_blocks,
+                                                    int n_tail) {
+  constexpr int ROWS = PartSlot<NT>::ROWS;
+  const int wg = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const int u = wg / ROWS, row = wg % ROWS;
+  if (u >= n_tail) return;
+  const int unit = a.units_full + u;
+  const int head = unit / q_blocks;
+  const int tok = (unit % q_blocks) * ROWS + row;
+  if (tok >= a.Nq) return;
+  const float* base = a.part + static_cast<size_t>(u) * a.pieces * PartSlot<NT>::FLOATS;
+  float M = -INFINITY;
+  for (int r = 0; r < a.pieces; ++r)
+    M = fmaxf(M, base[r * PartSlot<NT>::FLOATS + ROWS * DH + 2 * row]);
+  float l = 0.f, z[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int r = 0; r < a.pieces; ++r) {
+    const float* sr = base + r * PartSlot<NT>::FLOATS;
+    const float w = exp2f(sr[ROWS * DH + 2 * row] - M);
+    l = fmaf(w, sr[ROWS * DH + 2 * row + 1], l);
+    const float4 zv = *reinterpret_cast<const float4*>(sr + row * DH + 4 * lane);
+    z[0] = fmaf(w, zv.x, z[0]);
+    z[1] = fmaf(w, zv.y, z[1]);
+    z[2] = fmaf(w, zv.z, z[2]);
+    z[3] = fmaf(w, zv.w, z[3]);
+  }
+  uint16_t* orow = a.O + head * a.o_ld_head + static_cast<int64_t>(tok) * a.o_ld_token;
+  *reinterpret_cast<uint2*>(orow + 4 * lane) =
+      make_uint2(pack_bf16x2(__fdiv_rn(z[0], l), __fdiv_rn(z[1], l)),
+                 pack_bf16x2(__fdiv_rn(z[2], l), __fdiv_rn(z[3], l)));
 }
 
 // Choose the 2-D tensor map of a psi_heads view: head-major rows (ld_head a
@@ -535,17 +621,48 @@ psi_status launch_k(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensor
     attr_set = true;
   }
   const int q_blocks = (a.Nq + A::NT * BQ - 1) / (A::NT * BQ);
-  const long long grid = static_cast<long long>(q_blocks) * a.heads;
-  if (grid <= 0) return PSI_OK;
-  if (grid > 0x7FFFFFFFLL) return set_error(PSI_ERR_UNSUPPORTED, "attention: grid too large");
+  const long long units = static_cast<long long>(q_blocks) * a.heads;
+  if (units <= 0) return PSI_OK;
+  if (units > 0x3FFFFFFFLL) return set_error(PSI_ERR_UNSUPPORTED, "attention: grid too large");
+  // one CTA per SM: split the units of a partial last wave into key ranges
+  AttnArgs g = a;
+  g.units_full = static_cast<int32_t>(units);
+  g.pieces = 0;
+  int n_tail = 0;
+  const int sms = num_sms();
+  const int nb = (a.Nk + A::KB - 1) / A::KB;
+  if (a.part && !a.bf16_weights && units > sms && units % sms) {
+    const int tail = static_cast<int>(units % sms);
+    const int pieces = std::min(nb, sms / tail);
+    if (pieces >= 2) {
+      n_tail = tail;
+      g.units_full = static_cast<int32_t>(units - tail);
+      g.pieces = pieces;
+    }
+  }
+  const long long grid = g.units_full + static_cast<long long>(n_tail) * g.pieces;
   attn_kernel<KSUB><<<static_cast<unsigned>(grid), A::kThreads, A::SMEM_BYTES, stream>>>(
-      mq, mk, mv, vq, vk, vv, a);
+      mq, mk, mv, vq, vk, vv, g);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_error(e, "attention launch");
+  count_launch();
+  if (n_tail) {
+    const int warps = n_tail * PartSlot<A::NT>::ROWS;
+    merge_kernel<A::NT><<<(warps + 7) / 8, 256, 0, stream>>>(g, q_blocks, n_tail);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_error(e, "attention merge launch");
+    count_launch();
+  }
   return PSI_OK;
 }
 
 }  // namespace
+
+size_t attention_workspace_bytes(int key_block) {
+  const size_t per = key_block == 128 ? PartSlot<AShape<1>::NT>::FLOATS
+                                      : PartSlot<AShape<2>::NT>::FLOATS;
+  return per * sizeof(float) * static_cast<size_t>(num_sms());
+}
 
 psi_status launch_attention(const psi_heads* Q, const psi_heads* K, const psi_heads* V,
                             const AttnArgs& a, cudaStream_t stream) {

@@ -1,5 +1,6 @@
 // common.cu -- error reporting, the device error record, tensor-map
 // encoding and device queries shared by the kernels and the runtime.
+#include <atomic>
 #include <cstdio>
 #include <mutex>
 #include <string>
@@ -57,6 +58,10 @@ cudaError_t dev_error_take(DevError* out) {
   if (out->code != 0) e = cudaMemcpyToSymbol(g_dev_error, &zero, sizeof(DevError));
   return e;
 }
+
+// kernels launched by the library in this process (all entry points)
+static std::atomic<uint64_t> g_kernel_launches{0};
+void count_launch() { g_kernel_launches.fetch_add(1, std::memory_order_relaxed); }
 
 int num_sms() {
   int dev = 0;
@@ -120,3 +125,7 @@ psi_status make_tmap_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_
 }
 
 }  // namespace psi
+
+extern "C" uint64_t psi_kernel_launches(void) {
+  return psi::g_kernel_launches.load(std::memory_order_relaxed);
+}

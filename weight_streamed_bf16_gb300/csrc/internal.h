@@ -40,6 +40,8 @@ psi_status make_tmap_2d_ex(CUtensorMap* m, const void* base, uint64_t rows, uint
                            uint64_t ld, uint32_t box_rows, uint32_t box_cols, int elem_bytes,
                            int swizzle_bytes);
 int num_sms();
+// Count one kernel launch (psi_kernel_launches).
+void count_launch();
 
 // ------------------------------------------------------------ page GEMM --
 enum Epilogue : int {
@@ -100,9 +102,19 @@ struct AttnArgs {
   uint16_t* O;
   int64_t o_ld_token;
   int64_t o_ld_head;
+  // tail split: CTAs [0, units_full) take whole (head, query tile) units;
+  // the remaining units are cut into `pieces` contiguous key-block ranges,
+  // one CTA each, whose unnormalised partial results go to `part` and are
+  // combined by the merge kernel (pieces = 0: no split)
+  int32_t units_full;
+  int32_t pieces;
+  float* part;
   DevError* err;
   uint64_t timeout_ns;
 };
+
+// Bytes of the tail-split workspace for key_block (128 or 256) on this device.
+size_t attention_workspace_bytes(int key_block);
 
 psi_status launch_rmsnorm(const void* X, int64_t ldx, int64_t N, int64_t d, const void* gamma,
                           float eps, void* Y, int64_t ldy, cudaStream_t stream);

@@ -200,6 +200,7 @@ psi_status launch_rmsnorm(const void* X, int64_t ldx, int64_t N, int64_t d, cons
   rmsnorm_kernel<<<grid, kNormThreads, smem, stream>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_error(e, "rmsnorm launch");
+  count_launch();
   return PSI_OK;
 }
 

@@ -279,6 +279,7 @@ psi_status launch_bn(const CUtensorMap& tx, const CUtensorMap& tp, const CUtenso
   page_gemm_kernel<BN><<<grid, kThreads, C::SMEM_BYTES, s>>>(tx, tp, tp2, to, a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_error(e, "page_gemm launch");
+  count_launch();
   return PSI_OK;
 }
 

@@ -288,6 +288,7 @@ psi_status launch_page_gemm_pair(const CUtensorMap& tx, const CUtensorMap& tp,
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, page_gemm_pair_kernel, tx, tp, tp2, to, a);
   if (e != cudaSuccess) return cuda_error(e, "page_gemm_pair launch");
+  count_launch();
   return PSI_OK;
 }
 

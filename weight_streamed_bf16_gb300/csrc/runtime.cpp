@@ -746,10 +746,26 @@ psi_status psi_ffn_paged(psi_arena* a, const void* X, int64_t N, const psi_ffn_w
   return stream_after(a->ev_join, a->aux, a->compute);
 }
 
+psi_status psi_attn_workspace_size(int32_t key_block, size_t* bytes) {
+  if (!bytes) return set_error(PSI_ERR_INVALID_ARG, "attn_workspace_size: null");
+  if (key_block != 128 && key_block != 256)
+    return set_error(PSI_ERR_UNSUPPORTED, "attn: key_block must be 128 or 256");
+  *bytes = attention_workspace_bytes(key_block);
+  return PSI_OK;
+}
+
 psi_status psi_attn_partitioned(const psi_heads* Q, const psi_heads* K, const psi_heads* V,
                                 const psi_heads* O, int32_t heads, int64_t Nq, int64_t Nk,
                                 int32_t dh, float scale, int32_t key_block, void* stream,
                                 uint32_t flags) {
+  return psi_attn_partitioned_ws(Q, K, V, O, heads, Nq, Nk, dh, scale, key_block, nullptr, 0,
+                                 stream, flags);
+}
+
+psi_status psi_attn_partitioned_ws(const psi_heads* Q, const psi_heads* K, const psi_heads* V,
+                                   const psi_heads* O, int32_t heads, int64_t Nq, int64_t Nk,
+                                   int32_t dh, float scale, int32_t key_block, void* workspace,
+                                   size_t workspace_bytes, void* stream, uint32_t flags) {
   if (!Q || !K || !V || !O || !O->ptr)
     return set_error(PSI_ERR_INVALID_ARG, "attn: null argument");
   if (heads <= 0 || Nq < 0 || Nk < 1)
@@ -773,6 +789,12 @@ psi_status psi_attn_partitioned(const psi_heads* Q, const psi_heads* K, const ps
   g.O = static_cast<uint16_t*>(O->ptr);
   g.o_ld_token = O->ld_token;
   g.o_ld_head = O->ld_head;
+  if (workspace) {
+    if (!aligned16(workspace) || workspace_bytes < attention_workspace_bytes(key_block))
+      return set_error(PSI_ERR_INVALID_ARG,
+                       "attn: workspace must be 16-byte aligned and psi_attn_workspace_size bytes");
+    g.part = static_cast<float*>(workspace);
+  }
   g.err = dev_error_ptr();
   if (!g.err) return set_error(PSI_ERR_CUDA, "attn: kernel error record not reachable");
   g.timeout_ns = kWaitLimitNs;

@@ -37,10 +37,11 @@ EXPORTS = [
     "psi_plan_linear", "psi_ffn_page_bytes", "psi_ffn_pack", "psi_ffn_workspace",
     "psi_arena_create", "psi_arena_destroy", "psi_arena_slots",
     "psi_page_stream", "psi_page_release", "psi_sync", "psi_stream_wait",
-    "psi_arena_stats", "psi_arena_reset_stats", "psi_arena_set_timing",
+    "psi_arena_stats", "psi_arena_reset_stats", "psi_arena_set_timing", "psi_kernel_launches",
     "psi_arena_fail_next_copy", "psi_debug_stall_next_gemm",
     "psi_linear_paged", "psi_linear_rope_paged", "psi_rmsnorm",
-    "psi_ffn_paged", "psi_attn_partitioned",
+    "psi_ffn_paged", "psi_attn_partitioned", "psi_attn_partitioned_ws",
+    "psi_attn_workspace_size",
     "psi_ffn_resident_noalloc",
     "psi_journal_create", "psi_journal_destroy", "psi_journal_commit", "psi_journal_reload",
     "psi_journal_acquire", "psi_journal_fence", "psi_journal_drop", "psi_journal_host_view",
@@ -141,6 +142,7 @@ def load(path: str = LIB_PATH) -> C.CDLL:
         "psi_sync": (st, [vp, i64]),
         "psi_stream_wait": (st, [vp, i64]),
         "psi_arena_stats": (st, [vp, C.POINTER(psi_stats)]),
+        "psi_kernel_launches": (C.c_uint64, []),
         "psi_arena_reset_stats": (st, [vp]),
         "psi_arena_set_timing": (st, [vp, i32]),
         "psi_arena_fail_next_copy": (st, [vp]),
@@ -154,6 +156,9 @@ def load(path: str = LIB_PATH) -> C.CDLL:
                                vp, u32]),
         "psi_attn_partitioned": (st, [C.POINTER(psi_heads)] * 4 +
                                  [i32, i64, i64, i32, C.c_float, i32, vp, u32]),
+        "psi_attn_partitioned_ws": (st, [C.POINTER(psi_heads)] * 4 +
+                                    [i32, i64, i64, i32, C.c_float, i32, vp, sz, vp, u32]),
+        "psi_attn_workspace_size": (st, [i32, C.POINTER(sz)]),
         "psi_ffn_resident_noalloc": (st, [vp, i64, C.POINTER(psi_ffn_weight), vp, vp, vp, vp,
                                           vp, u32]),
         "psi_journal_create": (st, [vp, vp, sz, sz, C.POINTER(vp)]),
@@ -265,6 +270,11 @@ def psi_arena_fail_next_copy(arena: int):
     _check(load().psi_arena_fail_next_copy(arena))
 
 
+def psi_kernel_launches() -> int:
+    """Kernels the library has launched in this process."""
+    return load().psi_kernel_launches()
+
+
 def psi_debug_stall_next_gemm(timeout_ns: int):
     _check(load().psi_debug_stall_next_gemm(timeout_ns))
 
@@ -297,6 +307,21 @@ def psi_attn_partitioned(Q: psi_heads, K: psi_heads, V: psi_heads, O: psi_heads,
                          flags: int = 0):
     _check(load().psi_attn_partitioned(C.byref(Q), C.byref(K), C.byref(V), C.byref(O), heads,
                                        Nq, Nk, dh, scale, key_block, stream, flags))
+
+
+def psi_attn_partitioned_ws(Q: psi_heads, K: psi_heads, V: psi_heads, O: psi_heads,
+                            heads: int, Nq: int, Nk: int, dh: int, scale: float, key_block: int,
+                            workspace: int | None, workspace_bytes: int, stream: int,
+                            flags: int = 0):
+    _check(load().psi_attn_partitioned_ws(C.byref(Q), C.byref(K), C.byref(V), C.byref(O), heads,
+                                          Nq, Nk, dh, scale, key_block, workspace or None,
+                                          workspace_bytes, stream, flags))
+
+
+def psi_attn_workspace_size(key_block: int) -> int:
+    n = C.c_size_t()
+    _check(load().psi_attn_workspace_size(key_block, C.byref(n)))
+    return n.value
 
 
 def psi_ffn_resident_noalloc(X: int, N: int, W: psi_ffn_weight, a: int, b: int,
