@@ -7,18 +7,21 @@ decoder and round-to-nearest-even, and evaluates every operator from its
 plain dense definition in float64, rounding once to BF16 at each declared
 write boundary.
 
-Source: "Precision-Preserving Subtensor Inference" (PSI, arXiv 2611.08023),
-section II-B Eqs.(2)-(4) (partitioned FFN and online-softmax attention),
-section II-C Eq.(5) (BF16 round-to-nearest-even and write boundaries),
-section III-A (bias added before the single BF16 write, FP32-fidelity
-attention weights) and section IV-B Eq.(6) ("rounding the exact real sum
-once").
+Source: Precision-Preserving Subtensor Inference (PSI, arXiv 2611.08023),
+section II-B Eqs.(2)-(4) (partitioned FFN, online-softmax attention,
+full-row RMS normalisation, split RoPE), section II-C Eq.(5) (BF16
+round-to-nearest-even and write boundaries), section III-A (bias added
+before the single BF16 write, FP32-fidelity attention weights, and the
+baseline variant without those changes) and section IV-B Eq.(6) (the exact
+sum of an output element, rounded a single time).
 
 Modules
 -------
 bf16    decoding, encoding and rounding of BF16 values (float64 and exact
         dyadic rationals)
-ops     linear, FFN, attention (dense) and the online-softmax recurrence
+ops     linear (and its baseline rounding order), FFN, attention (dense,
+        online, and with BF16 numerator weights), RMSNorm, split RoPE and
+        the projection with RoPE
 grade   ulp distances and the tolerance used to compare a result with the
         oracle
 
