@@ -20,8 +20,9 @@
 //               right after its PV, while the other tile is in softmax
 //   warps 2..   softmax, 4 warps per query tile, one query row per thread:
 //               two passes over tensor memory (row extremum, then
-//               p = 2^(s*scale*log2e - m) by one FFMA and ex2), running max m
-//               and sum l in FP32, p split into p_hi = B(p) and
+//               p = 2^(s*scale*log2e - m) by one FFMA and ex2), reference
+//               point m (the running max, moved when it grows by more than
+//               2^8) and sum l in FP32, p split into p_hi = B(p) and
 //               p_lo = B(p - p_hi) (the tensor-core operand carries p to
 //               within 2^-17 relative) and written over the row's S
 //               columns; O rescaled by eta in tensor memory when the max
@@ -403,8 +404,14 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
         break;
       }
       ext = c >= 0.f ? fmaxf(ext, other) : fminf(ext, other);
-      const float m_new = fmaxf(m2, ext * c);
-      const float eta = ex2_approx(m2 - m_new);  // 0 on the first block
+      // reference point of the exponents: moved only when the running max
+      // exceeds it by more than 2^8 (the weights then stay below 2^8 and O is
+      // rescaled rarely); z and l are scaled alike, so z / l is unchanged.
+      // The BF16-weights variant keeps the exact running max: its rounded
+      // weights depend on the reference point.
+      const float mx = fmaxf(m2, ext * c);
+      const float m_new = mx > m2 + (args.bf16_weights ? 0.f : 8.f) ? mx : m2;
+      const float eta = ex2_approx(m2 - m_new);  // 0 on the first block, 1 if unmoved
       // pass 2: p = 2^(s*c - m) with one FFMA; each chunk of 32 keys is
       // written back over its own 32 columns as 16 columns of p_hi pairs and
       // 16 of p_lo pairs (keys 2i, 2i+1 share a column).  The next chunk's
