@@ -369,9 +369,15 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
       float ext = c >= 0.f ? -INFINITY : INFINITY;
       auto scan = [&](const uint32_t (&r)[32], int base) {
         if (kvalid >= KB) {
+          if (c >= 0.f) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            ext = c >= 0.f ? fmaxf(ext, __uint_as_float(r[i])) : fminf(ext, __uint_as_float(r[i]));
+            for (int i = 0; i < 32; i += 2)
+              ext = max3f(ext, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; i += 2)
+              ext = min3f(ext, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+          }
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i)
@@ -416,23 +422,57 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
       // written back over its own 32 columns as 16 columns of p_hi pairs and
       // 16 of p_lo pairs (keys 2i, 2i+1 share a column).  The next chunk's
       // load is in flight while this chunk is processed.
+      // 256-key blocks (one tile per CTA, registers to spare): pairs of keys
+      // go through the SIMD2 FP32 instructions (the scaled exponent, the row
+      // sum as two partial sums, the p_lo residual); 128-key blocks keep
+      // scalar FP32, which measured faster within their 96 registers
       float rs = 0.f;
+      uint64_t rs2 = f2_pack(0.f, 0.f);
+      const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(-m_new, -m_new);
       auto expo = [&](const uint32_t (&r)[32], int cc) {
         float p[32];
-        if (kvalid >= KB) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) p[i] = ex2_approx(fmaf(__uint_as_float(r[i]), c, -m_new));
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            p[i] = cc * 32 + i < kvalid ? ex2_approx(fmaf(__uint_as_float(r[i]), c, -m_new)) : 0.f;
-        }
         uint32_t hi[16], lo[16];
+        if constexpr (KSUB == 2) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          rs += p[2 * i] + p[2 * i + 1];
-          hi[i] = pack_bf16x2(p[2 * i], p[2 * i + 1]);
-          lo[i] = pack_bf16x2(p[2 * i] - bf16_lo(hi[i]), p[2 * i + 1] - bf16_hi(hi[i]));
+          for (int i = 0; i < 16; ++i) {
+            float e0, e1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])),
+                             c2, nm2),
+                      e0, e1);
+            p[2 * i] = ex2_approx(e0);
+            p[2 * i + 1] = ex2_approx(e1);
+          }
+          if (kvalid < KB) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (cc * 32 + i >= kvalid) p[i] = 0.f;
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const uint64_t pp = f2_pack(p[2 * i], p[2 * i + 1]);
+            rs2 = f2_add(rs2, pp);
+            hi[i] = pack_bf16x2(p[2 * i], p[2 * i + 1]);
+            float d0, d1;
+            f2_unpack(f2_sub(pp, f2_pack(bf16_lo(hi[i]), bf16_hi(hi[i]))), d0, d1);
+            lo[i] = pack_bf16x2(d0, d1);
+          }
+        } else {
+          if (kvalid >= KB) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              p[i] = ex2_approx(fmaf(__uint_as_float(r[i]), c, -m_new));
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              p[i] = cc * 32 + i < kvalid ? ex2_approx(fmaf(__uint_as_float(r[i]), c, -m_new))
+                                          : 0.f;
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            rs += p[2 * i] + p[2 * i + 1];
+            hi[i] = pack_bf16x2(p[2 * i], p[2 * i + 1]);
+            lo[i] = pack_bf16x2(p[2 * i] - bf16_lo(hi[i]), p[2 * i + 1] - bf16_hi(hi[i]));
+          }
         }
         tmem_st_32x32b_x16(tS + cc * 32, hi);
         tmem_st_32x32b_x16(tS + cc * 32 + 16, lo);
@@ -453,6 +493,11 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
           expo(r1, ch0 + cc + 1);
           tmem_wait_ld();
         }
+      }
+      if constexpr (KSUB == 2) {
+        float rs_a, rs_b;
+        f2_unpack(rs2, rs_a, rs_b);
+        rs = rs_a + rs_b;
       }
       l = eta * l + rs;
       m2 = m_new;
