@@ -618,9 +618,11 @@ __global__ void __launch_bounds__(256) merge_kernel(const AttnArgs a, int q_bloc
   if (tok >= a.Nq) return;
   const float* base = a.part + static_cast<size_t>(u) * a.pieces * PartSlot<NT>::FLOATS;
   float M = -INFINITY;
+#pragma unroll 4
   for (int r = 0; r < a.pieces; ++r)
     M = fmaxf(M, base[r * PartSlot<NT>::FLOATS + ROWS * DH + 2 * row]);
   float l = 0.f, z[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
   for (int r = 0; r < a.pieces; ++r) {
     const float* sr = base + r * PartSlot<NT>::FLOATS;
     const float w = exp2f(sr[ROWS * DH + 2 * row] - M);
