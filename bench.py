@@ -600,7 +600,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true",
                     help="stack workload: arena sweep 32/80/256 MiB + resident, bitwise control")
-    ap.add_argument("--cpu-rows", type=int, default=512)
+    ap.add_argument("--cpu-rows", type=int, default=1536)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
