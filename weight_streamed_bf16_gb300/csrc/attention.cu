@@ -122,6 +122,283 @@ __device__ __forceinline__ bool exchange(float* mine, const float* theirs, float
   return true;
 }
 
+// The softmax role of one warp (both attention kernels).  SPLIT = 2 warps
+// share each TMEM lane quarter of a tile: warp half h owns the keys
+// [h*KB/2, (h+1)*KB/2) of every block (and O columns [h*DH/2, ...)); the two
+// halves exchange the row extremum once per block and the row sum once at
+// the end.  With PAIR the P-ready arrivals go to the even CTA of the pair.
+template <int KSUB, int NT, bool PAIR, class Bars>
+__device__ __forceinline__ void softmax_role(Bars* bars, uint8_t* smem, int off_x, uint32_t tmem,
+                                             uint32_t tile_cols, int warp, int lane,
+                                             const AttnArgs& args, int nb, int jb0, int slot,
+                                             int head, int q0, volatile int* abort_flag) {
+  constexpr int KB = SUB * KSUB;
+  constexpr int SPLIT = 2;
+  constexpr int kWhere = KID_ATTN * 16;
+  // SPLIT warps share each TMEM lane quarter of a tile: warp half h owns
+  // the keys [h*KB/SPLIT, (h+1)*KB/SPLIT) of every block (and O columns
+  // [h*DH/SPLIT, ...)); the two halves exchange the row extremum once per
+  // block and the row sum once at the end.
+  
+  const int e = warp - 2;
+  const int t = e / (4 * SPLIT);           // query tile
+  const int h = (e % (4 * SPLIT)) / 4;     // key half
+  const int q = warp & 3;                  // TMEM lane quarter
+  const int row = q * 32 + lane;           // query row within the tile
+  const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+  const uint32_t tS = tmem + (tile_cols * static_cast<uint32_t>(t)) + lane_off;
+  const uint32_t tO = tmem + (tile_cols * static_cast<uint32_t>(t) + KB) + lane_off;
+  constexpr int NCH = KB / 32 / SPLIT;     // 32-key chunks of this half per block
+  const int ch0 = h * NCH;                 // first chunk of this half
+  float* xbase = reinterpret_cast<float*>(smem + off_x);
+  uint64_t* xb = &bars->xbar[t][q];
+  auto xslot = [&](int par, int half) { return xbase + ((par * NT + t) * SPLIT + half) * 128 + row; };
+  float m2 = -INFINITY;  // running max, log2 units
+  float l = 0.f;         // running sum of this half's weights
+  bool ok = true;
+  for (int j = 0; j < nb; ++j) {
+    if (!mbar_wait(&bars->s_full[t], j & 1, abort_flag, args.timeout_ns)) {
+      if (lane == 0) record_error(args.err, 1, kWhere + 2, j, t * 8 + h * 4 + q);
+      bars->abort_flag = 1;
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    // pass 1: row extremum of this half's raw scores (max, or min for a
+    // negative scale), then the other half's through shared memory
+    const float c = args.scale_log2;  // scale * log2(e)
+    const int kvalid = args.Nk - (jb0 + j) * KB;  // keys of this block that exist
+    float ext = c >= 0.f ? -INFINITY : INFINITY;
+    auto scan = [&](const uint32_t (&r)[32], int base) {
+      if (kvalid >= KB) {
+        if (c >= 0.f) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 2)
+            ext = max3f(ext, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; i += 2)
+            ext = min3f(ext, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (base + i < kvalid)
+            ext = c >= 0.f ? fmaxf(ext, __uint_as_float(r[i])) : fminf(ext, __uint_as_float(r[i]));
+      }
+    };
+    // the half's first two chunks stay in registers for pass 2
+    uint32_t ra[32], rb[32];
+    tmem_ld_32x32b_x32(tS + ch0 * 32, ra);
+    tmem_ld_32x32b_x32(tS + (ch0 + 1) * 32, rb);
+    tmem_wait_ld();
+    scan(ra, ch0 * 32);
+    scan(rb, (ch0 + 1) * 32);
+#pragma unroll
+    for (int g = 2; g < NCH; g += 2) {
+      uint32_t rc[32], rd[32];
+      tmem_ld_32x32b_x32(tS + (ch0 + g) * 32, rc);
+      tmem_ld_32x32b_x32(tS + (ch0 + g + 1) * 32, rd);
+      tmem_wait_ld();
+      scan(rc, (ch0 + g) * 32);
+      scan(rd, (ch0 + g + 1) * 32);
+    }
+    float other;
+    if (!exchange(xslot(j & 1, h), xslot(j & 1, h ^ 1), ext, xb, j & 1, &other, abort_flag,
+                  args.timeout_ns)) {
+      if (lane == 0) record_error(args.err, 1, kWhere + 6, j, t * 8 + h * 4 + q);
+      bars->abort_flag = 1;
+      ok = false;
+      break;
+    }
+    ext = c >= 0.f ? fmaxf(ext, other) : fminf(ext, other);
+    // reference point of the exponents: moved only when the running max
+    // exceeds it by more than 2^8 (the weights then stay below 2^8 and O is
+    // rescaled rarely); z and l are scaled alike, so z / l is unchanged.
+    // The BF16-weights variant keeps the exact running max: its rounded
+    // weights depend on the reference point.
+    const float mx = fmaxf(m2, ext * c);
+    const float m_new = mx > m2 + (args.bf16_weights ? 0.f : 8.f) ? mx : m2;
+    const float eta = ex2_approx(m2 - m_new);  // 0 on the first block, 1 if unmoved
+    // pass 2: p = 2^(s*c - m) with one FFMA; each chunk of 32 keys is
+    // written back over its own 32 columns as 16 columns of p_hi pairs and
+    // 16 of p_lo pairs (keys 2i, 2i+1 share a column).  The next chunk's
+    // load is in flight while this chunk is processed.
+    // 256-key blocks (one tile per CTA, registers to spare): pairs of keys
+    // go through the SIMD2 FP32 instructions (the scaled exponent, the row
+    // sum as two partial sums, the p_lo residual); 128-key blocks keep
+    // scalar FP32, which measured faster within their 96 registers
+    float rs = 0.f;
+    uint64_t rs2 = f2_pack(0.f, 0.f);
+    const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(-m_new, -m_new);
+    auto expo = [&](const uint32_t (&r)[32], int cc) {
+      float p[32];
+      uint32_t hi[16], lo[16];
+      if constexpr (KSUB == 2) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float e0, e1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])),
+                           c2, nm2),
+                    e0, e1);
+          p[2 * i] = ex2_approx(e0);
+          p[2 * i + 1] = ex2_approx(e1);
+        }
+        if (kvalid < KB) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (cc * 32 + i >= kvalid) p[i] = 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const uint64_t pp = f2_pack(p[2 * i], p[2 * i + 1]);
+          rs2 = f2_add(rs2, pp);
+          hi[i] = pack_bf16x2(p[2 * i], p[2 * i + 1]);
+          float d0, d1;
+          f2_unpack(f2_sub(pp, f2_pack(bf16_lo(hi[i]), bf16_hi(hi[i]))), d0, d1);
+          lo[i] = pack_bf16x2(d0, d1);
+        }
+      } else {
+        if (kvalid >= KB) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            p[i] = ex2_approx(fmaf(__uint_as_float(r[i]), c, -m_new));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            p[i] = cc * 32 + i < kvalid ? ex2_approx(fmaf(__uint_as_float(r[i]), c, -m_new))
+                                        : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          rs += p[2 * i] + p[2 * i + 1];
+          hi[i] = pack_bf16x2(p[2 * i], p[2 * i + 1]);
+          lo[i] = pack_bf16x2(p[2 * i] - bf16_lo(hi[i]), p[2 * i + 1] - bf16_hi(hi[i]));
+        }
+      }
+      tmem_st_32x32b_x16(tS + cc * 32, hi);
+      tmem_st_32x32b_x16(tS + cc * 32 + 16, lo);
+    };
+    expo(ra, ch0);
+    expo(rb, ch0 + 1);
+    if (NCH > 2) {
+      // further chunks (256-key blocks): reloaded, next load in flight
+      uint32_t r0[32], r1[32];
+      tmem_ld_32x32b_x32(tS + (ch0 + 2) * 32, r0);
+      tmem_wait_ld();
+#pragma unroll
+      for (int cc = 2; cc < NCH; cc += 2) {
+        tmem_ld_32x32b_x32(tS + (ch0 + cc + 1) * 32, r1);
+        expo(r0, ch0 + cc);
+        tmem_wait_ld();
+        if (cc + 2 < NCH) tmem_ld_32x32b_x32(tS + (ch0 + cc + 2) * 32, r0);
+        expo(r1, ch0 + cc + 1);
+        tmem_wait_ld();
+      }
+    }
+    if constexpr (KSUB == 2) {
+      float rs_a, rs_b;
+      f2_unpack(rs2, rs_a, rs_b);
+      rs = rs_a + rs_b;
+    }
+    l = eta * l + rs;
+    m2 = m_new;
+    if (j > 0) {
+      // the previous PV of this tile has finished: O is stable
+      if (!mbar_wait(&bars->pv_done[t], (j - 1) & 1, abort_flag, args.timeout_ns)) {
+        if (lane == 0) record_error(args.err, 1, kWhere + 3, j, t * 8 + h * 4 + q);
+        bars->abort_flag = 1;
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (__any_sync(0xffffffffu, eta != 1.0f)) {
+        // this half's O columns
+        constexpr int OCH = DH / 32 / SPLIT;
+#pragma unroll 1
+        for (int cc = h * OCH; cc < (h + 1) * OCH; cc += 2) {
+          uint32_t ra[32], rb[32];
+          tmem_ld_32x32b_x32(tO + cc * 32, ra);
+          tmem_ld_32x32b_x32(tO + cc * 32 + 32, rb);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            ra[i] = __float_as_uint(__uint_as_float(ra[i]) * eta);
+            rb[i] = __float_as_uint(__uint_as_float(rb[i]) * eta);
+          }
+          tmem_st_32x32b_x32(tO + cc * 32, ra);
+          tmem_st_32x32b_x32(tO + cc * 32 + 32, rb);
+        }
+      }
+    }
+    tmem_wait_st();
+    tc_fence_before();
+    if constexpr (PAIR)  // the even CTA of the pair issues the MMAs
+    mbar_arrive_cluster(mapa_shared(smem_u32(&bars->p_full[t]), 0));
+  else
+    mbar_arrive(&bars->p_full[t]);
+  }
+  if (ok && nb > 0) {
+    float l_other = 0.f;
+    if (!mbar_wait(&bars->pv_done[t], (nb - 1) & 1, abort_flag, args.timeout_ns)) {
+      if (lane == 0) record_error(args.err, 1, kWhere + 3, nb, t * 8 + h * 4 + q);
+      bars->abort_flag = 1;
+    } else if (!exchange(xslot(nb & 1, h), xslot(nb & 1, h ^ 1), l, xb, nb & 1, &l_other,
+                         abort_flag, args.timeout_ns)) {
+      if (lane == 0) record_error(args.err, 1, kWhere + 6, nb, t * 8 + h * 4 + q);
+      bars->abort_flag = 1;
+    } else {
+      // both halves' sums, added in the same order in both warps
+      const float lt = h == 0 ? l + l_other : l_other + l;
+      tc_fence_after();
+      const int tok = q0 + t * BQ + row;
+      if (slot >= 0) {
+        // a key range of a split unit: unnormalised z, and (m, l), FP32
+        float* zs = args.part + static_cast<size_t>(slot) * PartSlot<NT>::FLOATS;
+        float* zr = zs + static_cast<size_t>(t * BQ + row) * DH;
+        constexpr int OCH = DH / 32 / SPLIT;
+#pragma unroll 1
+        for (int cc = h * OCH; cc < (h + 1) * OCH; ++cc) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tO + cc * 32, r);
+          tmem_wait_ld();
+          float4* z4 = reinterpret_cast<float4*>(zr + cc * 32);
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            z4[u] = make_float4(__uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1]),
+                                __uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3]));
+        }
+        if (h == 0) {
+          float* ml = zs + static_cast<size_t>(PartSlot<NT>::ROWS) * DH + 2 * (t * BQ + row);
+          ml[0] = m2;
+          ml[1] = lt;
+        }
+      } else {
+      uint16_t* orow =
+          args.O + head * args.o_ld_head + static_cast<int64_t>(tok) * args.o_ld_token;
+      constexpr int OCH = DH / 32 / SPLIT;
+#pragma unroll 1
+      for (int cc = h * OCH; cc < (h + 1) * OCH; ++cc) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tO + cc * 32, r);
+        tmem_wait_ld();
+        if (tok < args.Nq) {
+          uint4* o4 = reinterpret_cast<uint4*>(orow + cc * 32);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            float v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = __fdiv_rn(__uint_as_float(r[8 * u + i]), lt);
+            o4[u] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                               pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+          }
+        }
+      }
+      }
+    }
+  }
+}
+
 template <int KSUB>
 __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -332,266 +609,8 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
       }
     }
   } else {
-    // ---------------------------------------------------------- softmax --
-    // SPLIT warps share each TMEM lane quarter of a tile: warp half h owns
-    // the keys [h*KB/SPLIT, (h+1)*KB/SPLIT) of every block (and O columns
-    // [h*DH/SPLIT, ...)); the two halves exchange the row extremum once per
-    // block and the row sum once at the end.
-    constexpr int SPLIT = A::SPLIT;
-    const int e = warp - 2;
-    const int t = e / (4 * SPLIT);           // query tile
-    const int h = (e % (4 * SPLIT)) / 4;     // key half
-    const int q = warp & 3;                  // TMEM lane quarter
-    const int row = q * 32 + lane;           // query row within the tile
-    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-    const uint32_t tS = tmem + A::tm_s(t) + lane_off;
-    const uint32_t tO = tmem + A::tm_o(t) + lane_off;
-    constexpr int NCH = KB / 32 / SPLIT;     // 32-key chunks of this half per block
-    const int ch0 = h * NCH;                 // first chunk of this half
-    float* xbase = reinterpret_cast<float*>(smem + A::OFF_X);
-    uint64_t* xb = &bars->xbar[t][q];
-    auto xslot = [&](int par, int half) { return xbase + ((par * NT + t) * SPLIT + half) * 128 + row; };
-    float m2 = -INFINITY;  // running max, log2 units
-    float l = 0.f;         // running sum of this half's weights
-    bool ok = true;
-    for (int j = 0; j < nb; ++j) {
-      if (!mbar_wait(&bars->s_full[t], j & 1, abort_flag, args.timeout_ns)) {
-        if (lane == 0) record_error(args.err, 1, kWhere + 2, j, t * 8 + h * 4 + q);
-        bars->abort_flag = 1;
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      // pass 1: row extremum of this half's raw scores (max, or min for a
-      // negative scale), then the other half's through shared memory
-      const float c = args.scale_log2;  // scale * log2(e)
-      const int kvalid = args.Nk - (jb0 + j) * KB;  // keys of this block that exist
-      float ext = c >= 0.f ? -INFINITY : INFINITY;
-      auto scan = [&](const uint32_t (&r)[32], int base) {
-        if (kvalid >= KB) {
-          if (c >= 0.f) {
-#pragma unroll
-            for (int i = 0; i < 32; i += 2)
-              ext = max3f(ext, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; i += 2)
-              ext = min3f(ext, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (base + i < kvalid)
-              ext = c >= 0.f ? fmaxf(ext, __uint_as_float(r[i])) : fminf(ext, __uint_as_float(r[i]));
-        }
-      };
-      // the half's first two chunks stay in registers for pass 2
-      uint32_t ra[32], rb[32];
-      tmem_ld_32x32b_x32(tS + ch0 * 32, ra);
-      tmem_ld_32x32b_x32(tS + (ch0 + 1) * 32, rb);
-      tmem_wait_ld();
-      scan(ra, ch0 * 32);
-      scan(rb, (ch0 + 1) * 32);
-#pragma unroll
-      for (int g = 2; g < NCH; g += 2) {
-        uint32_t rc[32], rd[32];
-        tmem_ld_32x32b_x32(tS + (ch0 + g) * 32, rc);
-        tmem_ld_32x32b_x32(tS + (ch0 + g + 1) * 32, rd);
-        tmem_wait_ld();
-        scan(rc, (ch0 + g) * 32);
-        scan(rd, (ch0 + g + 1) * 32);
-      }
-      float other;
-      if (!exchange(xslot(j & 1, h), xslot(j & 1, h ^ 1), ext, xb, j & 1, &other, abort_flag,
-                    args.timeout_ns)) {
-        if (lane == 0) record_error(args.err, 1, kWhere + 6, j, t * 8 + h * 4 + q);
-        bars->abort_flag = 1;
-        ok = false;
-        break;
-      }
-      ext = c >= 0.f ? fmaxf(ext, other) : fminf(ext, other);
-      // reference point of the exponents: moved only when the running max
-      // exceeds it by more than 2^8 (the weights then stay below 2^8 and O is
-      // rescaled rarely); z and l are scaled alike, so z / l is unchanged.
-      // The BF16-weights variant keeps the exact running max: its rounded
-      // weights depend on the reference point.
-      const float mx = fmaxf(m2, ext * c);
-      const float m_new = mx > m2 + (args.bf16_weights ? 0.f : 8.f) ? mx : m2;
-      const float eta = ex2_approx(m2 - m_new);  // 0 on the first block, 1 if unmoved
-      // pass 2: p = 2^(s*c - m) with one FFMA; each chunk of 32 keys is
-      // written back over its own 32 columns as 16 columns of p_hi pairs and
-      // 16 of p_lo pairs (keys 2i, 2i+1 share a column).  The next chunk's
-      // load is in flight while this chunk is processed.
-      // 256-key blocks (one tile per CTA, registers to spare): pairs of keys
-      // go through the SIMD2 FP32 instructions (the scaled exponent, the row
-      // sum as two partial sums, the p_lo residual); 128-key blocks keep
-      // scalar FP32, which measured faster within their 96 registers
-      float rs = 0.f;
-      uint64_t rs2 = f2_pack(0.f, 0.f);
-      const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(-m_new, -m_new);
-      auto expo = [&](const uint32_t (&r)[32], int cc) {
-        float p[32];
-        uint32_t hi[16], lo[16];
-        if constexpr (KSUB == 2) {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            float e0, e1;
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])),
-                             c2, nm2),
-                      e0, e1);
-            p[2 * i] = ex2_approx(e0);
-            p[2 * i + 1] = ex2_approx(e1);
-          }
-          if (kvalid < KB) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (cc * 32 + i >= kvalid) p[i] = 0.f;
-          }
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const uint64_t pp = f2_pack(p[2 * i], p[2 * i + 1]);
-            rs2 = f2_add(rs2, pp);
-            hi[i] = pack_bf16x2(p[2 * i], p[2 * i + 1]);
-            float d0, d1;
-            f2_unpack(f2_sub(pp, f2_pack(bf16_lo(hi[i]), bf16_hi(hi[i]))), d0, d1);
-            lo[i] = pack_bf16x2(d0, d1);
-          }
-        } else {
-          if (kvalid >= KB) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              p[i] = ex2_approx(fmaf(__uint_as_float(r[i]), c, -m_new));
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              p[i] = cc * 32 + i < kvalid ? ex2_approx(fmaf(__uint_as_float(r[i]), c, -m_new))
-                                          : 0.f;
-          }
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            rs += p[2 * i] + p[2 * i + 1];
-            hi[i] = pack_bf16x2(p[2 * i], p[2 * i + 1]);
-            lo[i] = pack_bf16x2(p[2 * i] - bf16_lo(hi[i]), p[2 * i + 1] - bf16_hi(hi[i]));
-          }
-        }
-        tmem_st_32x32b_x16(tS + cc * 32, hi);
-        tmem_st_32x32b_x16(tS + cc * 32 + 16, lo);
-      };
-      expo(ra, ch0);
-      expo(rb, ch0 + 1);
-      if (NCH > 2) {
-        // further chunks (256-key blocks): reloaded, next load in flight
-        uint32_t r0[32], r1[32];
-        tmem_ld_32x32b_x32(tS + (ch0 + 2) * 32, r0);
-        tmem_wait_ld();
-#pragma unroll
-        for (int cc = 2; cc < NCH; cc += 2) {
-          tmem_ld_32x32b_x32(tS + (ch0 + cc + 1) * 32, r1);
-          expo(r0, ch0 + cc);
-          tmem_wait_ld();
-          if (cc + 2 < NCH) tmem_ld_32x32b_x32(tS + (ch0 + cc + 2) * 32, r0);
-          expo(r1, ch0 + cc + 1);
-          tmem_wait_ld();
-        }
-      }
-      if constexpr (KSUB == 2) {
-        float rs_a, rs_b;
-        f2_unpack(rs2, rs_a, rs_b);
-        rs = rs_a + rs_b;
-      }
-      l = eta * l + rs;
-      m2 = m_new;
-      if (j > 0) {
-        // the previous PV of this tile has finished: O is stable
-        if (!mbar_wait(&bars->pv_done[t], (j - 1) & 1, abort_flag, args.timeout_ns)) {
-          if (lane == 0) record_error(args.err, 1, kWhere + 3, j, t * 8 + h * 4 + q);
-          bars->abort_flag = 1;
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, eta != 1.0f)) {
-          // this half's O columns
-          constexpr int OCH = DH / 32 / SPLIT;
-#pragma unroll 1
-          for (int cc = h * OCH; cc < (h + 1) * OCH; cc += 2) {
-            uint32_t ra[32], rb[32];
-            tmem_ld_32x32b_x32(tO + cc * 32, ra);
-            tmem_ld_32x32b_x32(tO + cc * 32 + 32, rb);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              ra[i] = __float_as_uint(__uint_as_float(ra[i]) * eta);
-              rb[i] = __float_as_uint(__uint_as_float(rb[i]) * eta);
-            }
-            tmem_st_32x32b_x32(tO + cc * 32, ra);
-            tmem_st_32x32b_x32(tO + cc * 32 + 32, rb);
-          }
-        }
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&bars->p_full[t]);
-    }
-    if (ok && nb > 0) {
-      float l_other = 0.f;
-      if (!mbar_wait(&bars->pv_done[t], (nb - 1) & 1, abort_flag, args.timeout_ns)) {
-        if (lane == 0) record_error(args.err, 1, kWhere + 3, nb, t * 8 + h * 4 + q);
-        bars->abort_flag = 1;
-      } else if (!exchange(xslot(nb & 1, h), xslot(nb & 1, h ^ 1), l, xb, nb & 1, &l_other,
-                           abort_flag, args.timeout_ns)) {
-        if (lane == 0) record_error(args.err, 1, kWhere + 6, nb, t * 8 + h * 4 + q);
-        bars->abort_flag = 1;
-      } else {
-        // both halves' sums, added in the same order in both warps
-        const float lt = h == 0 ? l + l_other : l_other + l;
-        tc_fence_after();
-        const int tok = q0 + t * BQ + row;
-        if (slot >= 0) {
-          // a key range of a split unit: unnormalised z, and (m, l), FP32
-          float* zs = args.part + static_cast<size_t>(slot) * PartSlot<NT>::FLOATS;
-          float* zr = zs + static_cast<size_t>(t * BQ + row) * DH;
-          constexpr int OCH = DH / 32 / SPLIT;
-#pragma unroll 1
-          for (int cc = h * OCH; cc < (h + 1) * OCH; ++cc) {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(tO + cc * 32, r);
-            tmem_wait_ld();
-            float4* z4 = reinterpret_cast<float4*>(zr + cc * 32);
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-              z4[u] = make_float4(__uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1]),
-                                  __uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3]));
-          }
-          if (h == 0) {
-            float* ml = zs + static_cast<size_t>(PartSlot<NT>::ROWS) * DH + 2 * (t * BQ + row);
-            ml[0] = m2;
-            ml[1] = lt;
-          }
-        } else {
-        uint16_t* orow =
-            args.O + head * args.o_ld_head + static_cast<int64_t>(tok) * args.o_ld_token;
-        constexpr int OCH = DH / 32 / SPLIT;
-#pragma unroll 1
-        for (int cc = h * OCH; cc < (h + 1) * OCH; ++cc) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(tO + cc * 32, r);
-          tmem_wait_ld();
-          if (tok < args.Nq) {
-            uint4* o4 = reinterpret_cast<uint4*>(orow + cc * 32);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              float v[8];
-#pragma unroll
-              for (int i = 0; i < 8; ++i) v[i] = __fdiv_rn(__uint_as_float(r[8 * u + i]), lt);
-              o4[u] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
-                                 pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
-            }
-          }
-        }
-        }
-      }
-    }
+    softmax_role<KSUB, NT, false>(bars, smem, A::OFF_X, tmem, A::TILE_COLS, warp, lane, args, nb,
+                                  jb0, slot, head, q0, abort_flag);
   }
 
   tc_fence_before();
