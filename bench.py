@@ -254,6 +254,22 @@ class BlockWorkload(Workload):
         else:
             self.runner.stack(X, self.blocks, Y, self.tmp, self.flags)
 
+    def managed_bytes(self):
+        """Device bytes of the block step by the terms of Eq.(1): the page
+        arena (W + 2P in the paper's notation, here all slots), live state
+        (activations of one step) and bounded workspace; the library itself
+        allocates none."""
+        r = self.runner
+        nb = lambda t: t.numel() * t.element_size()  # noqa: E731
+        live = [self.X, self.Y, r.h, r.att, r.x1] + ([r.xn] if r.xn is not None else [])
+        if hasattr(r, "states"):
+            live += r.states
+        work = [r.hid, r.acc, r.attn_ws]
+        out = {"arena": self.arena.buf.numel(), "live_state": sum(nb(t) for t in live),
+               "workspace": sum(nb(t) for t in work), "library_allocations": 0}
+        out["total"] = out["arena"] + out["live_state"] + out["workspace"]
+        return out
+
     def phase_split(self, steps=5):
         """Per-operator time of a single block on the compute stream (ms):
         QKV projection, attention, out-projection, FFN."""
@@ -403,7 +419,11 @@ def stack_sweep(args):
     wl.arena.close()
     runs = []
     ref = None
-    for mib, flags in [(32, 0), (80, 0), (256, 0), (80, psi.PSI_RESIDENT)]:
+    # the arena sweep (Table V analog), the resident control, and the
+    # synchronous-transport control (copies on the compute stream, no
+    # prefetch: the scheduling comparison of Table IV)
+    for mib, flags in [(32, 0), (80, 0), (256, 0), (80, psi.PSI_RESIDENT),
+                       (80, psi.PSI_SYNC_COPY)]:
         arena = Arena(wl.shape.page_bytes, mib * MiB // wl.shape.page_bytes, device=dev)
         runner = BlockRunner(wl.shape, arena, device=dev)
         Y = torch.empty_like(wl.X)
@@ -427,9 +447,11 @@ def stack_sweep(args):
         else:
             same = bool(torch.equal(ref.view(torch.int16), Y.view(torch.int16)))
         runs.append({"arena_mib": mib, "slots": arena.slots,
-                     "mode": "resident" if flags else "streamed",
+                     "mode": ("resident" if flags & psi.PSI_RESIDENT else
+                              "streamed, copies on the compute stream" if flags else "streamed"),
                      "ms_per_stack": ms, "tflops": wl.flops / (ms * 1e-3) / 1e12,
-                     "ingest_gbs": (0 if flags else len(wl.blocks) * psi_weight_bytes()) /
+                     "ingest_gbs": (0 if flags & psi.PSI_RESIDENT else
+                                    len(wl.blocks) * psi_weight_bytes()) /
                                    (ms * 1e-3) / 1e9,
                      "bitwise_equal_to_first": same, "pages": st["pages_streamed"]})
         arena.close()
@@ -837,6 +859,8 @@ def main():
                        "flops_per_step": wl.flops, "wall_s_timed": t_wall,
                        "step_roofline_ms": step_bound_ms,
                        "phase_ms": phases, "rmsnorm_roofline": norm_roof,
+                       "managed_device_bytes": (wl.managed_bytes()
+                                                if hasattr(wl, "managed_bytes") else None),
                        "frac_of_step_roofline": step_bound_ms / ms_per_step},
             "roofline": roof, "ingest": ingest, "journal": jst, "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step":
