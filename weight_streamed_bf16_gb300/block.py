@@ -102,8 +102,6 @@ class BlockRunner:
         # attention tail-split workspace (FP32 partial states)
         nws = psi.psi_attn_workspace_size(s.key_block)
         self.attn_ws = torch.empty(nws // 4, dtype=torch.float32, device=device)
-        self.attn_launches = 0
-        self.norm_launches = 0
 
     def _heads(self, t: torch.Tensor, col0: int, ld: int) -> psi.psi_heads:
         return psi.psi_heads(t.data_ptr() + 2 * col0, ld, self.s.dh)
@@ -129,7 +127,6 @@ class BlockRunner:
         if s.prenorm:
             psi.psi_rmsnorm(X.data_ptr(), s.d, N, s.d, W.gamma1.data_ptr(), s.eps,
                             self.xn.data_ptr(), s.d, cs.cuda_stream)
-            self.norm_launches += 1
             mark(1)
             psi.psi_linear_rope_paged(A, self.xn.data_ptr(), N, s.d, W.qkv.desc(),
                                       W.bqkv.data_ptr(), self.rope, self.h.data_ptr(), s.qkv,
@@ -145,7 +142,6 @@ class BlockRunner:
         psi.psi_attn_partitioned_ws(q, k, v, o, H, N, N, dh, 1.0 / math.sqrt(dh), s.key_block,
                                     self.attn_ws.data_ptr(), self.attn_ws.numel() * 4,
                                     cs.cuda_stream, 0)
-        self.attn_launches += 1
         mark(2 + pn)
         psi.psi_linear_paged(A, self.att.data_ptr(), N, H * dh, W.out.desc(), W.bo.data_ptr(),
                              X.data_ptr(), self.x1.data_ptr(), s.d, flags)
@@ -154,7 +150,6 @@ class BlockRunner:
         if s.prenorm:
             psi.psi_rmsnorm(self.x1.data_ptr(), s.d, N, s.d, W.gamma2.data_ptr(), s.eps,
                             self.xn.data_ptr(), s.d, cs.cuda_stream)
-            self.norm_launches += 1
             mark(5)
             ffn_in = self.xn
         psi.psi_ffn_paged(A, ffn_in.data_ptr(), N, W.ffn.desc(), W.a1.data_ptr(),
