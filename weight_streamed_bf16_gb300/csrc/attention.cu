@@ -636,21 +636,37 @@ __global__ void __launch_bounds__(256) merge_kernel(const AttnArgs a, int q_bloc
   const int tok = (unit % q_blocks) * ROWS + row;
   if (tok >= a.Nq) return;
   const float* base = a.part + static_cast<size_t>(u) * a.pieces * PartSlot<NT>::FLOATS;
+  // the ranges' (m, l) are read one per lane (32 ranges at a time); the
+  // maximum, the weights and the sum are formed across the warp in a fixed
+  // order; every lane then accumulates its four columns of z
   float M = -INFINITY;
-#pragma unroll 4
-  for (int r = 0; r < a.pieces; ++r)
-    M = fmaxf(M, base[r * PartSlot<NT>::FLOATS + ROWS * DH + 2 * row]);
+  for (int r0 = 0; r0 < a.pieces; r0 += 32) {
+    const int r = r0 + lane;
+    if (r < a.pieces) M = fmaxf(M, base[r * PartSlot<NT>::FLOATS + ROWS * DH + 2 * row]);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   float l = 0.f, z[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-  for (int r = 0; r < a.pieces; ++r) {
-    const float* sr = base + r * PartSlot<NT>::FLOATS;
-    const float w = exp2f(sr[ROWS * DH + 2 * row] - M);
-    l = fmaf(w, sr[ROWS * DH + 2 * row + 1], l);
-    const float4 zv = *reinterpret_cast<const float4*>(sr + row * DH + 4 * lane);
-    z[0] = fmaf(w, zv.x, z[0]);
-    z[1] = fmaf(w, zv.y, z[1]);
-    z[2] = fmaf(w, zv.z, z[2]);
-    z[3] = fmaf(w, zv.w, z[3]);
+  for (int r0 = 0; r0 < a.pieces; r0 += 32) {
+    const int r = r0 + lane;
+    float w = 0.f, wl = 0.f;
+    if (r < a.pieces) {
+      const float* ml = base + r * PartSlot<NT>::FLOATS + ROWS * DH + 2 * row;
+      w = exp2f(ml[0] - M);
+      wl = w * ml[1];
+    }
+    const int n = min(32, a.pieces - r0);
+#pragma unroll 8
+    for (int k = 0; k < n; ++k) {
+      const float wk = __shfl_sync(0xffffffffu, w, k);
+      l += __shfl_sync(0xffffffffu, wl, k);
+      const float4 zv = *reinterpret_cast<const float4*>(
+          base + (r0 + k) * PartSlot<NT>::FLOATS + row * DH + 4 * lane);
+      z[0] = fmaf(wk, zv.x, z[0]);
+      z[1] = fmaf(wk, zv.y, z[1]);
+      z[2] = fmaf(wk, zv.z, z[2]);
+      z[3] = fmaf(wk, zv.w, z[3]);
+    }
   }
   uint16_t* orow = a.O + head * a.o_ld_head + static_cast<int64_t>(tok) * a.o_ld_token;
   *reinterpret_cast<uint2*>(orow + 4 * lane) =
