@@ -180,6 +180,44 @@ class Workload:
         raise NotImplementedError
 
 
+def workload_name(args) -> str:
+    """The workload description both arms print in config.workload."""
+    import dataclasses
+
+    import psi_synth
+    w = args.workload
+    if w in ("block", "stack"):
+        cfg = psi_synth.BLOCK
+        blocks = 1 if w == "block" else args.blocks
+        slots = args.arena_mib * MiB // cfg.page_bytes
+        journal = w == "stack" and args.journal
+        branches = args.branches if w == "stack" else 1
+        return (("pre-norm (RMSNorm, split RoPE on Q/K) " if args.prenorm else "") +
+                f"synthetic transformer block x{blocks}: d_model {cfg.d}, {cfg.N} tokens, "
+                f"{cfg.heads} heads x {cfg.dh}, QKV {cfg.qkv_rows}x{cfg.d} + out "
+                f"{cfg.d}x{cfg.d} + FFN {cfg.d}->{cfg.hidden}->{cfg.d} tanh-GELU, "
+                f"{cfg.page_bytes // MiB} MiB pages, {args.arena_mib} MiB arena "
+                f"({slots} slots), weights "
+                f"{'resident' if args.resident else 'streamed from pinned host'}" +
+                (f", {branches} branch states" if branches > 1 or journal else "") +
+                (" kept in the host journal (3 device state buffers)" if journal else ""))
+    if w == "ffn":
+        cfg = psi_synth.FFN
+        return (f"paged FFN: X {cfg.N}x{cfg.d}, W1 {cfg.h}x{cfg.d}, W2 {cfg.d}x{cfg.h}, "
+                f"{cfg.slice}-wide hidden slices, {cfg.slots}-slice arena, streamed")
+    if w == "linear":
+        cfg = psi_synth.LINEAR
+        return (f"single paged linear: X {cfg.N}x{cfg.K}, W {cfg.M}x{cfg.K}, "
+                f"{cfg.page_rows}-row pages, {cfg.slots}-page arena (latency-bound)")
+    if w == "attention":
+        cfg = psi_synth.ATTN
+        if args.key_block:
+            cfg = dataclasses.replace(cfg, key_block=args.key_block)
+        return (f"partitioned attention: Q,K,V {cfg.heads}x{cfg.N}x{cfg.dh}, scale "
+                f"1/sqrt({cfg.dh}), key blocks of {cfg.key_block}, FP32 online softmax")
+    raise SystemExit(f"unknown workload {w}")
+
+
 class BlockWorkload(Workload):
     def __init__(self, torch, dev, blocks=1, arena_mib=80, resident=False, prenorm=False,
                  branches=1, journal=False):
@@ -590,7 +628,7 @@ def reference_arm(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": tot_s / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": args.workload, "sample": desc},
+        "config": {"workload": workload_name(args), "sample": desc},
         "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": os.cpu_count(),
                          "kind": "oracle", "sample": desc},
         "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
