@@ -57,14 +57,16 @@ template <int KSUB>
 struct AShape {
   static constexpr int NT = KSUB == 1 ? 2 : 1;
   static constexpr int KB = SUB * KSUB;
-  static constexpr int SPLIT = 2;  // softmax warps per TMEM lane quarter (key halves)
+  // softmax warps per TMEM lane quarter (key ranges): 2 with two tiles, 4
+  // with one, which halves each warp's share of a 256-key block
+  static constexpr int SPLIT = KSUB == 1 ? 2 : 4;
   static constexpr int kThreads = 64 + NT * 128 * SPLIT;
   static constexpr int OFF_Q = 0;                          // NT tiles x 2 column blocks
   static constexpr int OFF_K = OFF_Q + NT * 2 * TILE64;    // 2 stages x 2 column blocks
   static constexpr int OFF_V = OFF_K + 2 * 2 * TILE64;
   static constexpr int OFF_BAR = OFF_V + 2 * 2 * TILE64;
-  // row-extremum and row-sum exchange between the two key halves of a row:
-  // [2 parities][NT tiles][SPLIT halves][128 rows] floats
+  // row-extremum and row-sum exchange between the key ranges of a row:
+  // [2 parities][NT tiles][SPLIT ranges][128 rows] floats
   static constexpr int OFF_X = OFF_BAR + 256;
   static constexpr int X_BYTES = 2 * NT * SPLIT * 128 * 4;
   static constexpr int SMEM_BYTES = OFF_X + X_BYTES + 1024;
@@ -88,7 +90,7 @@ struct __align__(8) ABars {
   uint64_t k_full[2], k_empty[2];
   uint64_t v_full[2], v_empty[2];
   uint64_t s_full[2], p_full[2], pv_done[2];
-  uint64_t xbar[2][4];  // per tile and lane quarter: the two key halves met
+  uint64_t xbar[2][4];  // per tile and lane quarter: the row's key ranges met
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -109,52 +111,58 @@ __device__ __forceinline__ void record_error(DevError* e, int code, int where, i
   }
 }
 
-// Publish a row value for the partner warp (same rows, other key half) and
-// read the partner's: both warps write their slot, arrive on the pair's
-// mbarrier and wait (bounded) for the phase.  Returns false on timeout.
-__device__ __forceinline__ bool exchange(float* mine, const float* theirs, float v,
-                                         uint64_t* bar, uint32_t parity, float* out,
+// Publish a row value to the other warps of the row (same rows, other key
+// ranges) and gather the row's SPLIT values in range order (out[h] = v):
+// every warp writes its slot, arrives on the row group's mbarrier and waits
+// (bounded) for the phase, then reads the other slots.  All warps of the row
+// then combine the same values in the same order.  Returns false on timeout.
+template <int SPLIT>
+__device__ __forceinline__ bool exchange(float* slots, int h, float v, uint64_t* bar,
+                                         uint32_t parity, float (&out)[SPLIT],
                                          volatile int* abort, uint64_t limit_ns) {
-  *mine = v;
+  slots[h * 128] = v;
   mbar_arrive(bar);
   if (!mbar_wait(bar, parity, abort, limit_ns)) return false;
-  *out = *theirs;
+  if constexpr (SPLIT == 2) {
+    const float w = slots[(h ^ 1) * 128];
+    out[0] = h == 0 ? v : w;
+    out[1] = h == 0 ? w : v;
+  } else {
+#pragma unroll
+    for (int i = 0; i < SPLIT; ++i) out[i] = slots[i * 128];
+  }
   return true;
 }
 
-// The softmax role of one warp (both attention kernels).  SPLIT = 2 warps
-// share each TMEM lane quarter of a tile: warp half h owns the keys
-// [h*KB/2, (h+1)*KB/2) of every block (and O columns [h*DH/2, ...)); the two
-// halves exchange the row extremum once per block and the row sum once at
-// the end.  With PAIR the P-ready arrivals go to the even CTA of the pair.
-template <int KSUB, int NT, bool PAIR, class Bars>
+// The softmax role of one warp (both attention kernels).  SPLIT warps share
+// each TMEM lane quarter of a tile: warp h owns the keys
+// [h*KB/SPLIT, (h+1)*KB/SPLIT) of every block (and O columns
+// [h*DH/SPLIT, ...)); the warps of a row exchange the row extremum once per
+// block and the row sum once at the end.  With PAIR the P-ready arrivals go
+// to the even CTA of the pair.
+template <int KSUB, int NT, int SPLIT, bool PAIR, class Bars>
 __device__ __forceinline__ void softmax_role(Bars* bars, uint8_t* smem, int off_x, uint32_t tmem,
                                              uint32_t tile_cols, int warp, int lane,
                                              const AttnArgs& args, int nb, int jb0, int slot,
                                              int head, int q0, volatile int* abort_flag) {
   constexpr int KB = SUB * KSUB;
-  constexpr int SPLIT = 2;
   constexpr int kWhere = KID_ATTN * 16;
-  // SPLIT warps share each TMEM lane quarter of a tile: warp half h owns
-  // the keys [h*KB/SPLIT, (h+1)*KB/SPLIT) of every block (and O columns
-  // [h*DH/SPLIT, ...)); the two halves exchange the row extremum once per
-  // block and the row sum once at the end.
-  
   const int e = warp - 2;
   const int t = e / (4 * SPLIT);           // query tile
-  const int h = (e % (4 * SPLIT)) / 4;     // key half
+  const int h = (e % (4 * SPLIT)) / 4;     // key range
   const int q = warp & 3;                  // TMEM lane quarter
   const int row = q * 32 + lane;           // query row within the tile
   const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
   const uint32_t tS = tmem + (tile_cols * static_cast<uint32_t>(t)) + lane_off;
   const uint32_t tO = tmem + (tile_cols * static_cast<uint32_t>(t) + KB) + lane_off;
-  constexpr int NCH = KB / 32 / SPLIT;     // 32-key chunks of this half per block
-  const int ch0 = h * NCH;                 // first chunk of this half
+  constexpr int NCH = KB / 32 / SPLIT;     // 32-key chunks of this range per block
+  static_assert(NCH == 2, "each softmax warp owns 64 keys of a block");
+  const int ch0 = h * NCH;                 // first chunk of this range
   float* xbase = reinterpret_cast<float*>(smem + off_x);
   uint64_t* xb = &bars->xbar[t][q];
-  auto xslot = [&](int par, int half) { return xbase + ((par * NT + t) * SPLIT + half) * 128 + row; };
+  auto xslots = [&](int par) { return xbase + ((par * NT + t) * SPLIT) * 128 + row; };
   float m2 = -INFINITY;  // running max, log2 units
-  float l = 0.f;         // running sum of this half's weights
+  float l = 0.f;         // running sum of this range's weights
   bool ok = true;
   for (int j = 0; j < nb; ++j) {
     if (!mbar_wait(&bars->s_full[t], j & 1, abort_flag, args.timeout_ns)) {
@@ -164,8 +172,8 @@ __device__ __forceinline__ void softmax_role(Bars* bars, uint8_t* smem, int off_
       break;
     }
     tc_fence_after();
-    // pass 1: row extremum of this half's raw scores (max, or min for a
-    // negative scale), then the other half's through shared memory
+    // pass 1: row extremum of this range's raw scores (max, or min for a
+    // negative scale), then the other ranges' through shared memory
     const float c = args.scale_log2;  // scale * log2(e)
     const int kvalid = args.Nk - (jb0 + j) * KB;  // keys of this block that exist
     float ext = c >= 0.f ? -INFINITY : INFINITY;
@@ -187,31 +195,24 @@ __device__ __forceinline__ void softmax_role(Bars* bars, uint8_t* smem, int off_
             ext = c >= 0.f ? fmaxf(ext, __uint_as_float(r[i])) : fminf(ext, __uint_as_float(r[i]));
       }
     };
-    // the half's first two chunks stay in registers for pass 2
+    // the range's two chunks stay in registers for pass 2
     uint32_t ra[32], rb[32];
     tmem_ld_32x32b_x32(tS + ch0 * 32, ra);
     tmem_ld_32x32b_x32(tS + (ch0 + 1) * 32, rb);
     tmem_wait_ld();
     scan(ra, ch0 * 32);
     scan(rb, (ch0 + 1) * 32);
-#pragma unroll
-    for (int g = 2; g < NCH; g += 2) {
-      uint32_t rc[32], rd[32];
-      tmem_ld_32x32b_x32(tS + (ch0 + g) * 32, rc);
-      tmem_ld_32x32b_x32(tS + (ch0 + g + 1) * 32, rd);
-      tmem_wait_ld();
-      scan(rc, (ch0 + g) * 32);
-      scan(rd, (ch0 + g + 1) * 32);
-    }
-    float other;
-    if (!exchange(xslot(j & 1, h), xslot(j & 1, h ^ 1), ext, xb, j & 1, &other, abort_flag,
-                  args.timeout_ns)) {
+    float others[SPLIT];
+    if (!exchange<SPLIT>(xslots(j & 1), h, ext, xb, j & 1, others, abort_flag,
+                         args.timeout_ns)) {
       if (lane == 0) record_error(args.err, 1, kWhere + 6, j, t * 8 + h * 4 + q);
       bars->abort_flag = 1;
       ok = false;
       break;
     }
-    ext = c >= 0.f ? fmaxf(ext, other) : fminf(ext, other);
+#pragma unroll
+    for (int i = 0; i < SPLIT; ++i)
+      ext = c >= 0.f ? fmaxf(ext, others[i]) : fminf(ext, others[i]);
     // reference point of the exponents: moved only when the running max
     // exceeds it by more than 2^8 (the weights then stay below 2^8 and O is
     // rescaled rarely); z and l are scaled alike, so z / l is unchanged.
@@ -222,85 +223,32 @@ __device__ __forceinline__ void softmax_role(Bars* bars, uint8_t* smem, int off_
     const float eta = ex2_approx(m2 - m_new);  // 0 on the first block, 1 if unmoved
     // pass 2: p = 2^(s*c - m) with one FFMA; each chunk of 32 keys is
     // written back over its own 32 columns as 16 columns of p_hi pairs and
-    // 16 of p_lo pairs (keys 2i, 2i+1 share a column).  The next chunk's
-    // load is in flight while this chunk is processed.
-    // 256-key blocks (one tile per CTA, registers to spare): pairs of keys
-    // go through the SIMD2 FP32 instructions (the scaled exponent, the row
-    // sum as two partial sums, the p_lo residual); 128-key blocks keep
-    // scalar FP32, which measured faster within their 96 registers
+    // 16 of p_lo pairs (keys 2i, 2i+1 share a column).
     float rs = 0.f;
-    uint64_t rs2 = f2_pack(0.f, 0.f);
-    const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(-m_new, -m_new);
     auto expo = [&](const uint32_t (&r)[32], int cc) {
       float p[32];
       uint32_t hi[16], lo[16];
-      if constexpr (KSUB == 2) {
+      if (kvalid >= KB) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float e0, e1;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])),
-                           c2, nm2),
-                    e0, e1);
-          p[2 * i] = ex2_approx(e0);
-          p[2 * i + 1] = ex2_approx(e1);
-        }
-        if (kvalid < KB) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (cc * 32 + i >= kvalid) p[i] = 0.f;
-        }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const uint64_t pp = f2_pack(p[2 * i], p[2 * i + 1]);
-          rs2 = f2_add(rs2, pp);
-          hi[i] = pack_bf16x2(p[2 * i], p[2 * i + 1]);
-          float d0, d1;
-          f2_unpack(f2_sub(pp, f2_pack(bf16_lo(hi[i]), bf16_hi(hi[i]))), d0, d1);
-          lo[i] = pack_bf16x2(d0, d1);
-        }
+        for (int i = 0; i < 32; ++i)
+          p[i] = ex2_approx(fmaf(__uint_as_float(r[i]), c, -m_new));
       } else {
-        if (kvalid >= KB) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            p[i] = ex2_approx(fmaf(__uint_as_float(r[i]), c, -m_new));
-        } else {
+        for (int i = 0; i < 32; ++i)
+          p[i] = cc * 32 + i < kvalid ? ex2_approx(fmaf(__uint_as_float(r[i]), c, -m_new))
+                                      : 0.f;
+      }
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            p[i] = cc * 32 + i < kvalid ? ex2_approx(fmaf(__uint_as_float(r[i]), c, -m_new))
-                                        : 0.f;
-        }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          rs += p[2 * i] + p[2 * i + 1];
-          hi[i] = pack_bf16x2(p[2 * i], p[2 * i + 1]);
-          lo[i] = pack_bf16x2(p[2 * i] - bf16_lo(hi[i]), p[2 * i + 1] - bf16_hi(hi[i]));
-        }
+      for (int i = 0; i < 16; ++i) {
+        rs += p[2 * i] + p[2 * i + 1];
+        hi[i] = pack_bf16x2(p[2 * i], p[2 * i + 1]);
+        lo[i] = pack_bf16x2(p[2 * i] - bf16_lo(hi[i]), p[2 * i + 1] - bf16_hi(hi[i]));
       }
       tmem_st_32x32b_x16(tS + cc * 32, hi);
       tmem_st_32x32b_x16(tS + cc * 32 + 16, lo);
     };
     expo(ra, ch0);
     expo(rb, ch0 + 1);
-    if (NCH > 2) {
-      // further chunks (256-key blocks): reloaded, next load in flight
-      uint32_t r0[32], r1[32];
-      tmem_ld_32x32b_x32(tS + (ch0 + 2) * 32, r0);
-      tmem_wait_ld();
-#pragma unroll
-      for (int cc = 2; cc < NCH; cc += 2) {
-        tmem_ld_32x32b_x32(tS + (ch0 + cc + 1) * 32, r1);
-        expo(r0, ch0 + cc);
-        tmem_wait_ld();
-        if (cc + 2 < NCH) tmem_ld_32x32b_x32(tS + (ch0 + cc + 2) * 32, r0);
-        expo(r1, ch0 + cc + 1);
-        tmem_wait_ld();
-      }
-    }
-    if constexpr (KSUB == 2) {
-      float rs_a, rs_b;
-      f2_unpack(rs2, rs_a, rs_b);
-      rs = rs_a + rs_b;
-    }
     l = eta * l + rs;
     m2 = m_new;
     if (j > 0) {
@@ -313,21 +261,30 @@ __device__ __forceinline__ void softmax_role(Bars* bars, uint8_t* smem, int off_
       }
       tc_fence_after();
       if (__any_sync(0xffffffffu, eta != 1.0f)) {
-        // this half's O columns
+        // this range's O columns
         constexpr int OCH = DH / 32 / SPLIT;
-#pragma unroll 1
-        for (int cc = h * OCH; cc < (h + 1) * OCH; cc += 2) {
-          uint32_t ra[32], rb[32];
-          tmem_ld_32x32b_x32(tO + cc * 32, ra);
-          tmem_ld_32x32b_x32(tO + cc * 32 + 32, rb);
+        if constexpr (OCH == 1) {
+          uint32_t ra[32];
+          tmem_ld_32x32b_x32(tO + h * 32, ra);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            ra[i] = __float_as_uint(__uint_as_float(ra[i]) * eta);
-            rb[i] = __float_as_uint(__uint_as_float(rb[i]) * eta);
+          for (int i = 0; i < 32; ++i) ra[i] = __float_as_uint(__uint_as_float(ra[i]) * eta);
+          tmem_st_32x32b_x32(tO + h * 32, ra);
+        } else {
+#pragma unroll 1
+          for (int cc = h * OCH; cc < (h + 1) * OCH; cc += 2) {
+            uint32_t ra[32], rb[32];
+            tmem_ld_32x32b_x32(tO + cc * 32, ra);
+            tmem_ld_32x32b_x32(tO + cc * 32 + 32, rb);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              ra[i] = __float_as_uint(__uint_as_float(ra[i]) * eta);
+              rb[i] = __float_as_uint(__uint_as_float(rb[i]) * eta);
+            }
+            tmem_st_32x32b_x32(tO + cc * 32, ra);
+            tmem_st_32x32b_x32(tO + cc * 32 + 32, rb);
           }
-          tmem_st_32x32b_x32(tO + cc * 32, ra);
-          tmem_st_32x32b_x32(tO + cc * 32 + 32, rb);
         }
       }
     }
@@ -339,17 +296,19 @@ __device__ __forceinline__ void softmax_role(Bars* bars, uint8_t* smem, int off_
     mbar_arrive(&bars->p_full[t]);
   }
   if (ok && nb > 0) {
-    float l_other = 0.f;
+    float ls[SPLIT];
     if (!mbar_wait(&bars->pv_done[t], (nb - 1) & 1, abort_flag, args.timeout_ns)) {
       if (lane == 0) record_error(args.err, 1, kWhere + 3, nb, t * 8 + h * 4 + q);
       bars->abort_flag = 1;
-    } else if (!exchange(xslot(nb & 1, h), xslot(nb & 1, h ^ 1), l, xb, nb & 1, &l_other,
-                         abort_flag, args.timeout_ns)) {
+    } else if (!exchange<SPLIT>(xslots(nb & 1), h, l, xb, nb & 1, ls, abort_flag,
+                                args.timeout_ns)) {
       if (lane == 0) record_error(args.err, 1, kWhere + 6, nb, t * 8 + h * 4 + q);
       bars->abort_flag = 1;
     } else {
-      // both halves' sums, added in the same order in both warps
-      const float lt = h == 0 ? l + l_other : l_other + l;
+      // the ranges' sums, added in range order in every warp of the row
+      float lt = ls[0];
+#pragma unroll
+      for (int i = 1; i < SPLIT; ++i) lt += ls[i];
       tc_fence_after();
       const int tok = q0 + t * BQ + row;
       if (slot >= 0) {
@@ -609,7 +568,7 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
       }
     }
   } else {
-    softmax_role<KSUB, NT, false>(bars, smem, A::OFF_X, tmem, A::TILE_COLS, warp, lane, args, nb,
+    softmax_role<KSUB, NT, A::SPLIT, false>(bars, smem, A::OFF_X, tmem, A::TILE_COLS, warp, lane, args, nb,
                                   jb0, slot, head, q0, abort_flag);
   }
 
