@@ -310,21 +310,22 @@ class BlockWorkload(Workload):
 
     def phase_split(self, steps=5):
         """Per-operator time of a single block on the compute stream (ms):
-        QKV projection, attention, out-projection, FFN."""
+        QKV projection, attention, out-projection, FFN (median of steps)."""
         torch = self.torch
         if len(self.blocks) != 1 or self.X.dim() == 3:
             return None
         names = (["norm1", "qkv_rope", "attention", "out_proj", "norm2", "ffn"] if self.prenorm
                  else ["qkv", "attention", "out_proj", "ffn"])
-        tot = [0.0] * len(names)
+        per = [[] for _ in names]
         for _ in range(steps):
             marks = [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
             with torch.cuda.stream(self.stream):
                 self.step(marks=marks)
             marks[-1].synchronize()
             for i in range(len(names)):
-                tot[i] += marks[i].elapsed_time(marks[i + 1])
-        return {k: v / steps for k, v in zip(names, tot)}
+                per[i].append(marks[i].elapsed_time(marks[i + 1]))
+        # median per phase: one step delayed by the host does not skew it
+        return {k: sorted(v)[len(v) // 2] for k, v in zip(names, per)}
 
     def io(self):
         return self.X, self.Y
