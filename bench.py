@@ -308,14 +308,21 @@ class BlockWorkload(Workload):
         out["total"] = out["arena"] + out["live_state"] + out["workspace"]
         return out
 
+    @property
+    def phase_names(self):
+        """Operator phases one step marks (a single block without a journal)."""
+        if len(self.blocks) != 1 or self.X.dim() == 3 or self.journal is not None:
+            return None
+        return (["norm1", "qkv_rope", "attention", "out_proj", "norm2", "ffn"] if self.prenorm
+                else ["qkv", "attention", "out_proj", "ffn"])
+
     def phase_split(self, steps=5):
         """Per-operator time of a single block on the compute stream (ms):
         QKV projection, attention, out-projection, FFN (median of steps)."""
         torch = self.torch
-        if len(self.blocks) != 1 or self.X.dim() == 3:
+        names = self.phase_names
+        if names is None:
             return None
-        names = (["norm1", "qkv_rope", "attention", "out_proj", "norm2", "ffn"] if self.prenorm
-                 else ["qkv", "attention", "out_proj", "ffn"])
         per = [[] for _ in names]
         for _ in range(steps):
             marks = [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
@@ -639,6 +646,57 @@ def reference_arm(args):
 
 
 # ------------------------------------------------------------------- main --
+def write_trace(path, wl, arena, stream, flush, torch):
+    """Page timeline of two steps after the measured ones (not timed): one
+    record per page copy and page GEMM from the library, the operator phase
+    marks of each step where the workload has them, and per-step sums of
+    copy and GEMM busy time.  Written to `path`; nothing is printed."""
+    from weight_streamed_bf16_gb300 import psi
+    arena.sync()
+    psi.psi_arena_trace_begin(arena.handle, 1 << 14)
+    origin = torch.cuda.Event(enable_timing=True)
+    origin.record(stream)          # next to the library's origin event
+    names = getattr(wl, "phase_names", None)
+    marks = []
+    with torch.cuda.stream(stream):
+        for k in range(2):
+            flush.fill_(k & 0xFF)
+            if names:
+                m = [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
+                wl.step(marks=m)
+                marks.append(m)
+            else:
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                wl.step()
+                e1.record(stream)
+                marks.append([e0, e1])
+    arena.sync()
+    torch.cuda.synchronize()
+    rec = psi.psi_arena_trace_get(arena.handle)
+    psi.psi_arena_set_timing(arena.handle, False)
+    steps = []
+    for m in marks:
+        t = [origin.elapsed_time(e) for e in m]
+        lo, hi = t[0], t[-1]
+
+        def busy(kind):
+            iv = sorted((max(r["start_ms"], lo), min(r["end_ms"], hi)) for r in rec
+                        if r["kind"] == kind and r["end_ms"] > lo and r["start_ms"] < hi)
+            tot, end = 0.0, -1e300
+            for a, b in iv:
+                if b > end:
+                    tot += b - max(a, end)
+                    end = b
+            return tot
+        steps.append({"start_ms": lo, "end_ms": hi,
+                      "phases": ({n: [t[i], t[i + 1]] for i, n in enumerate(names)}
+                                 if names else None),
+                      "copy_busy_ms": busy("copy"), "gemm_busy_ms": busy("gemm")})
+    with open(path, "w") as f:
+        json.dump({"workload": wl.name, "steps": steps, "records": rec}, f)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -662,6 +720,9 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="stack workload: arena sweep 32/80/256 MiB + resident, bitwise control")
     ap.add_argument("--cpu-rows", type=int, default=1536)
+    ap.add_argument("--trace", default=None, metavar="PATH",
+                    help="after the measurements, write the page timeline of two more "
+                         "steps (copies, page GEMMs, phase marks) to PATH as JSON")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -812,6 +873,9 @@ def main():
     e2e_ms, _, e2e_value = aggregate_ranks(dist, dev, e2e_ms, wl.flops, args.steps, world)
     in_bytes = Xh.numel() * Xh.element_size()
     out_bytes = Yh.numel() * Yh.element_size()
+
+    if args.trace and arena is not None and rank == 0:
+        write_trace(args.trace, wl, arena, stream, flush, torch)
 
     # ------------------------------------------------ roofline (page GEMM) --
     digest = source_digest("page_gemm.cu", "page_gemm_pair.cu", "gemm_epilogue.cuh", "ptx.cuh")

@@ -151,6 +151,19 @@ typedef struct {
   double copy_busy_ms;       /* the same for the timed copies */
 } psi_stats;
 
+/* One record of the page timeline (psi_arena_trace_begin/get). */
+enum { PSI_TRACE_COPY = 0, PSI_TRACE_GEMM = 1 };
+typedef struct {
+  int32_t kind;     /* PSI_TRACE_COPY: H2D copy of a page; PSI_TRACE_GEMM: page GEMM */
+  int32_t slot;     /* arena slot of the page; -1: a resident page or no arena page */
+  int32_t stream;   /* 0 compute stream, 1 the arena's auxiliary stream, 2 copy stream */
+  int32_t pad_;
+  uint64_t seq;     /* copy: the page request's sequence number; GEMM: launch number */
+  double start_ms;  /* from the origin event of psi_arena_trace_begin */
+  double end_ms;
+  double work;      /* copy: bytes; GEMM: algorithmic FLOPs 2*M*N*K */
+} psi_trace_record;
+
 /* ---------------------------------------------------------------- misc -- */
 const char* psi_version(void);
 const char* psi_status_string(psi_status s);
@@ -228,6 +241,19 @@ psi_status psi_arena_reset_stats(psi_arena* arena);
  * (copy stream) with CUDA events; psi_arena_stats sums them (it waits for
  * the events).  Off by default. */
 psi_status psi_arena_set_timing(psi_arena* arena, int32_t enable);
+/* Page timeline (the lifecycle of section II-D made visible): turn timing on
+ * and keep one psi_trace_record per timed page copy and page GEMM, at most
+ * `capacity` of them (later ones are dropped), with times measured from an
+ * event recorded now on the compute stream.  Drops the records of an
+ * earlier trace.  PSI_ERR_INVALID_ARG for a null arena or capacity 0. */
+psi_status psi_arena_trace_begin(psi_arena* arena, size_t capacity);
+/* Wait for the events of the records taken so far (a host wait) and copy
+ * min(capacity, held) of them, ordered by start time, to `out` (host
+ * memory, may be null when capacity is 0); *count = records held.  The
+ * timing sums of psi_arena_stats include the same launches.
+ * PSI_ERR_INVALID_ARG without an active trace or for null arena/count. */
+psi_status psi_arena_trace_get(psi_arena* arena, psi_trace_record* out, size_t capacity,
+                               size_t* count);
 /* Test hook: the next psi_page_stream call on this arena fails with
  * PSI_ERR_CUDA before enqueuing anything (host-side fault injection). */
 psi_status psi_arena_fail_next_copy(psi_arena* arena);

@@ -138,3 +138,13 @@ def test_linear_rope_argument_checks_need_no_gpu(lib):
     assert r == psi.PSI_ERR_INVALID_ARG
     r = lib.psi_linear_rope_paged(1, 1, 1, 64, C.byref(W), 1, None, 1, 64, 0)
     assert r == psi.PSI_ERR_INVALID_ARG and "rope" in psi.psi_last_error()
+
+
+def test_trace_argument_checks_need_no_gpu(lib):
+    n = C.c_size_t(7)
+    assert lib.psi_arena_trace_begin(None, 16) == psi.PSI_ERR_INVALID_ARG
+    assert lib.psi_arena_trace_get(None, None, 0, C.byref(n)) == psi.PSI_ERR_INVALID_ARG
+    assert n.value == 7
+    assert C.sizeof(psi.psi_trace_record) == 48
+    text = open(os.path.join(ROOT, "include", "psi.h")).read()
+    assert "PSI_TRACE_COPY = 0, PSI_TRACE_GEMM = 1" in text

@@ -159,3 +159,40 @@ def test_no_device_allocation_by_the_library():
     free1, _ = torch.cuda.mem_get_info()
     assert free1 == free0
     a.close()
+
+
+def test_page_timeline_follows_the_lifecycle():
+    """Section II-D on the device clock: every page GEMM starts after the copy
+    into its slot ended, and a slot's next copy starts after the GEMM that
+    read the previous page ended (event timestamps of the page trace)."""
+    g = torch.Generator().manual_seed(11)
+    N, K, M, pr = 512, 512, 7 * 256, 256
+    X = torch.randn(N, K, generator=g).to(torch.bfloat16).cuda()
+    W = (torch.randn(M, K, generator=g) / 24).to(torch.bfloat16)
+    b = (torch.randn(M, generator=g) * 0.02).to(torch.bfloat16).cuda()
+    a = Arena(pr * K * 2, 2)
+    w = LinearWeight(W, pr * K * 2, page_rows=pr)
+    Y = torch.empty(N, M, dtype=torch.bfloat16, device="cuda")
+    psi.psi_arena_trace_begin(a.handle, 64)
+    for _ in range(2):
+        psi.psi_linear_paged(a.handle, X.data_ptr(), N, K, w.desc(), b.data_ptr(), None,
+                             Y.data_ptr(), M, 0)
+    a.sync()
+    rec = psi.psi_arena_trace_get(a.handle)
+    copies = [r for r in rec if r["kind"] == "copy"]
+    gemms = [r for r in rec if r["kind"] == "gemm"]
+    assert len(copies) == 14 and len(gemms) == 14
+    assert all(r["end_ms"] >= r["start_ms"] >= 0 for r in rec)
+    assert all(r["stream"] == 2 and r["work"] == pr * K * 2 for r in copies)
+    assert all(r["slot"] in (0, 1) and r["work"] == 2.0 * N * pr * K for r in gemms)
+    eps = 2e-3  # event timer resolution, ms
+    by_seq = sorted(copies, key=lambda r: r["seq"])
+    by_launch = sorted(gemms, key=lambda r: r["seq"])
+    for i, (c, gm) in enumerate(zip(by_seq, by_launch)):
+        assert gm["slot"] == c["slot"] == i % 2
+        assert gm["start_ms"] >= c["end_ms"] - eps          # ready before consumed
+        if i >= 2:
+            assert c["start_ms"] >= by_launch[i - 2]["end_ms"] - eps  # slot released first
+    st = a.stats()
+    assert st["timed_copies"] == 14 and st["timed_gemms"] == 14
+    a.close()

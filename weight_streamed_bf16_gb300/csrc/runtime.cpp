@@ -31,6 +31,10 @@ struct TimedLaunch {
   cudaEvent_t start;
   cudaEvent_t stop;
   double work;  // FLOPs for a GEMM, bytes for a copy
+  int32_t kind = PSI_TRACE_GEMM;
+  int32_t slot = -1;    // arena slot of the page, -1 if none
+  int32_t stream = 0;   // 0 compute, 1 auxiliary, 2 copy
+  uint64_t seq = 0;     // page request or launch number
 };
 
 }  // namespace
@@ -60,6 +64,12 @@ struct psi_arena {
   bool fail_next_copy = false;
   std::vector<TimedLaunch> gemm_t, copy_t;
   std::vector<cudaEvent_t> pool;
+  uint64_t gemm_seq = 0;  // page-GEMM launches while timing
+  // page timeline: records of the timed launches since psi_arena_trace_begin
+  bool tracing = false;
+  size_t trace_cap = 0;
+  cudaEvent_t trace_origin = nullptr;
+  std::vector<psi_trace_record> trace;
 };
 
 namespace psi {
@@ -124,6 +134,13 @@ psi_status arena_gemm(psi_arena* a, cudaStream_t sm, const void* X, int64_t ldx,
   a->stats.kernels_launched++;
   if (a->timing) {
     t.work = 2.0 * g.M * static_cast<double>(g.N) * g.K;
+    t.kind = PSI_TRACE_GEMM;
+    t.stream = sm == a->aux ? 1 : 0;
+    const char* pc = static_cast<const char*>(P);
+    t.slot = (pc >= a->base && pc < a->base + a->bytes)
+                 ? static_cast<int32_t>((pc - a->base) / static_cast<ptrdiff_t>(a->page_bytes))
+                 : -1;
+    t.seq = ++a->gemm_seq;
     return timed_end(a, sm, t, &a->gemm_t);
   }
   return PSI_OK;
@@ -310,6 +327,7 @@ psi_status psi_arena_destroy(psi_arena* a) {
     cudaEventDestroy(t.stop);
   }
   for (auto e : a->pool) cudaEventDestroy(e);
+  if (a->trace_origin) cudaEventDestroy(a->trace_origin);
   delete a;
   return PSI_OK;
 }
@@ -362,6 +380,10 @@ psi_status page_stream_to(psi_arena* a, const void* host_src, size_t bytes, uint
   }
   if (a->timing) {
     t.work = static_cast<double>(bytes);
+    t.kind = PSI_TRACE_COPY;
+    t.slot = s;
+    t.stream = sync_copy ? (cs == a->aux ? 1 : 0) : 2;
+    t.seq = a->seq + 1;  // the number this request gets below
     if ((st = timed_end(a, sync_copy ? cs : a->copy, t, &a->copy_t)) != PSI_OK) return st;
   }
   a->state[s] = SLOT_REQUESTED;
@@ -448,6 +470,21 @@ psi_status psi_arena_stats(const psi_arena* ca, psi_stats* out) {
       *ms += f;
       *work += t.work;
       iv.emplace_back(t0, t0 + f);
+      if (a->tracing && a->trace.size() < a->trace_cap) {
+        float ts = 0.f, te = 0.f;
+        e = cudaEventElapsedTime(&ts, a->trace_origin, t.start);
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&te, a->trace_origin, t.stop);
+        if (e != cudaSuccess) return cuda_error(e, "arena trace: elapsed");
+        psi_trace_record r{};
+        r.kind = t.kind;
+        r.slot = t.slot;
+        r.stream = t.stream;
+        r.seq = t.seq;
+        r.start_ms = ts;
+        r.end_ms = te;
+        r.work = t.work;
+        a->trace.push_back(r);
+      }
     }
     std::sort(iv.begin(), iv.end());
     double end = -1e300;
@@ -488,6 +525,43 @@ psi_status psi_arena_reset_stats(psi_arena* a) {
 psi_status psi_arena_set_timing(psi_arena* a, int32_t enable) {
   if (!a) return set_error(PSI_ERR_INVALID_ARG, "arena_set_timing: null arena");
   a->timing = enable != 0;
+  return PSI_OK;
+}
+
+psi_status psi_arena_trace_begin(psi_arena* a, size_t capacity) {
+  if (!a || capacity == 0)
+    return set_error(PSI_ERR_INVALID_ARG, "arena_trace_begin: null arena or capacity 0");
+  psi_stats tmp;
+  a->tracing = false;
+  psi_status st = psi_arena_stats(a, &tmp);  // launches before the origin stay out
+  if (st != PSI_OK) return st;
+  cudaError_t e = cudaSuccess;
+  if (!a->trace_origin) e = cudaEventCreate(&a->trace_origin);
+  if (e == cudaSuccess) e = cudaEventRecord(a->trace_origin, a->compute);
+  if (e != cudaSuccess) return cuda_error(e, "arena_trace_begin: origin event");
+  a->trace.clear();
+  a->trace.reserve(std::min<size_t>(capacity, 1 << 16));
+  a->trace_cap = capacity;
+  a->tracing = true;
+  a->timing = true;
+  return PSI_OK;
+}
+
+psi_status psi_arena_trace_get(psi_arena* a, psi_trace_record* out, size_t capacity,
+                               size_t* count) {
+  if (!a || !count || (capacity > 0 && !out))
+    return set_error(PSI_ERR_INVALID_ARG, "arena_trace_get: null argument");
+  if (!a->tracing) return set_error(PSI_ERR_INVALID_ARG, "arena_trace_get: no trace begun");
+  psi_stats tmp;
+  psi_status st = psi_arena_stats(a, &tmp);  // waits for and folds the pending launches
+  if (st != PSI_OK) return st;
+  std::stable_sort(a->trace.begin(), a->trace.end(),
+                   [](const psi_trace_record& x, const psi_trace_record& y) {
+                     return x.start_ms < y.start_ms;
+                   });
+  const size_t n = std::min(capacity, a->trace.size());
+  for (size_t i = 0; i < n; ++i) out[i] = a->trace[i];
+  *count = a->trace.size();
   return PSI_OK;
 }
 

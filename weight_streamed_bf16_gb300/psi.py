@@ -38,6 +38,7 @@ EXPORTS = [
     "psi_arena_create", "psi_arena_destroy", "psi_arena_slots",
     "psi_page_stream", "psi_page_release", "psi_sync", "psi_stream_wait",
     "psi_arena_stats", "psi_arena_reset_stats", "psi_arena_set_timing", "psi_kernel_launches",
+    "psi_arena_trace_begin", "psi_arena_trace_get",
     "psi_arena_fail_next_copy", "psi_debug_stall_next_gemm",
     "psi_linear_paged", "psi_linear_rope_paged", "psi_rmsnorm",
     "psi_ffn_paged", "psi_attn_partitioned", "psi_attn_partitioned_ws",
@@ -105,6 +106,21 @@ class psi_stats(C.Structure):
         return {k: getattr(self, k) for k, _ in self._fields_}
 
 
+PSI_TRACE_COPY = 0
+PSI_TRACE_GEMM = 1
+
+
+class psi_trace_record(C.Structure):
+    _fields_ = [("kind", C.c_int32), ("slot", C.c_int32), ("stream", C.c_int32),
+                ("pad_", C.c_int32), ("seq", C.c_uint64), ("start_ms", C.c_double),
+                ("end_ms", C.c_double), ("work", C.c_double)]
+
+    def as_dict(self):
+        return {"kind": "copy" if self.kind == PSI_TRACE_COPY else "gemm", "slot": self.slot,
+                "stream": self.stream, "seq": self.seq, "start_ms": self.start_ms,
+                "end_ms": self.end_ms, "work": self.work}
+
+
 _lib = None
 
 
@@ -145,6 +161,8 @@ def load(path: str = LIB_PATH) -> C.CDLL:
         "psi_kernel_launches": (C.c_uint64, []),
         "psi_arena_reset_stats": (st, [vp]),
         "psi_arena_set_timing": (st, [vp, i32]),
+        "psi_arena_trace_begin": (st, [vp, sz]),
+        "psi_arena_trace_get": (st, [vp, C.POINTER(psi_trace_record), sz, C.POINTER(sz)]),
         "psi_arena_fail_next_copy": (st, [vp]),
         "psi_debug_stall_next_gemm": (st, [C.c_uint64]),
         "psi_linear_paged": (st, [vp, vp, i64, i64, C.POINTER(psi_linear_weight), vp, vp,
@@ -264,6 +282,19 @@ def psi_arena_reset_stats(arena: int):
 
 def psi_arena_set_timing(arena: int, enable: bool):
     _check(load().psi_arena_set_timing(arena, 1 if enable else 0))
+
+
+def psi_arena_trace_begin(arena: int, capacity: int):
+    _check(load().psi_arena_trace_begin(arena, capacity))
+
+
+def psi_arena_trace_get(arena: int) -> list:
+    """The page timeline records held (ordered by start time) as dicts."""
+    n = C.c_size_t(0)
+    _check(load().psi_arena_trace_get(arena, None, 0, C.byref(n)))
+    buf = (psi_trace_record * max(n.value, 1))()
+    _check(load().psi_arena_trace_get(arena, buf, n.value, C.byref(n)))
+    return [buf[i].as_dict() for i in range(n.value)]
 
 
 def psi_arena_fail_next_copy(arena: int):
