@@ -358,6 +358,240 @@ __device__ __forceinline__ void softmax_role(Bars* bars, uint8_t* smem, int off_
   }
 }
 
+// The softmax role of one warp for 256-key blocks (one query tile, two
+// 128-key sub-tiles per block, four warps per TMEM lane quarter): warp h
+// owns chunk h of each sub-tile (keys 32h.. and 128 + 32h..) and O columns
+// [32h, 32h + 32).  Each sub-tile has its own S-ready and P-ready barrier,
+// and sub-tile 0's weights are published first, so its PV product (and the
+// next block's scores for it) run on the tensor core while sub-tile 1's
+// weights are formed.  The extremum and row-sum exchanges are those of the
+// 128-key role.
+template <int NT, int SPLIT, class Bars>
+__device__ __forceinline__ void softmax_role_sub(Bars* bars, uint8_t* smem, int off_x, uint32_t tmem,
+                                             uint32_t tile_cols, int warp, int lane,
+                                             const AttnArgs& args, int nb, int jb0, int slot,
+                                             int head, int q0, volatile int* abort_flag) {
+  constexpr int KB = 2 * SUB;
+  constexpr int kWhere = KID_ATTN * 16;
+  const int e = warp - 2;
+  constexpr int t = 0;                     // the query tile
+  const int h = e / 4;                     // key range
+  const int q = warp & 3;                  // TMEM lane quarter
+  const int row = q * 32 + lane;           // query row within the tile
+  const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+  const uint32_t tS = tmem + (tile_cols * static_cast<uint32_t>(t)) + lane_off;
+  const uint32_t tO = tmem + (tile_cols * static_cast<uint32_t>(t) + KB) + lane_off;
+  static_assert(NT == 1 && SPLIT == 4, "one tile, four warps per lane quarter");
+  const int c0 = h, c1 = 4 + h;            // this warp's chunks of a block
+  float* xbase = reinterpret_cast<float*>(smem + off_x);
+  uint64_t* xb = &bars->xbar[t][q];
+  auto xslots = [&](int par) { return xbase + ((par * NT + t) * SPLIT) * 128 + row; };
+  float m2 = -INFINITY;  // running max, log2 units
+  float l = 0.f;         // running sum of this range's weights
+  bool ok = true;
+  for (int j = 0; j < nb; ++j) {
+    if (!mbar_wait(&bars->s_full[0], j & 1, abort_flag, args.timeout_ns)) {
+      if (lane == 0) record_error(args.err, 1, kWhere + 2, j, h * 4 + q);
+      bars->abort_flag = 1;
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    // pass 1: row extremum of this range's raw scores (max, or min for a
+    // negative scale), then the other ranges' through shared memory
+    const float c = args.scale_log2;  // scale * log2(e)
+    const int kvalid = args.Nk - (jb0 + j) * KB;  // keys of this block that exist
+    float ext = c >= 0.f ? -INFINITY : INFINITY;
+    auto scan = [&](const uint32_t (&r)[32], int base) {
+      if (kvalid >= KB) {
+        if (c >= 0.f) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 2)
+            ext = max3f(ext, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; i += 2)
+            ext = min3f(ext, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (base + i < kvalid)
+            ext = c >= 0.f ? fmaxf(ext, __uint_as_float(r[i])) : fminf(ext, __uint_as_float(r[i]));
+      }
+    };
+    // the warp's two chunks stay in registers for pass 2; sub-tile 0 is
+    // scanned while sub-tile 1's scores are still being computed
+    uint32_t ra[32], rb[32];
+    tmem_ld_32x32b_x32(tS + c0 * 32, ra);
+    tmem_wait_ld();
+    scan(ra, c0 * 32);
+    if (!mbar_wait(&bars->s_full[1], j & 1, abort_flag, args.timeout_ns)) {
+      if (lane == 0) record_error(args.err, 1, kWhere + 2, j, 64 + h * 4 + q);
+      bars->abort_flag = 1;
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    tmem_ld_32x32b_x32(tS + c1 * 32, rb);
+    tmem_wait_ld();
+    scan(rb, c1 * 32);
+    float others[SPLIT];
+    if (!exchange<SPLIT>(xslots(j & 1), h, ext, xb, j & 1, others, abort_flag,
+                         args.timeout_ns)) {
+      if (lane == 0) record_error(args.err, 1, kWhere + 6, j, t * 8 + h * 4 + q);
+      bars->abort_flag = 1;
+      ok = false;
+      break;
+    }
+#pragma unroll
+    for (int i = 0; i < SPLIT; ++i)
+      ext = c >= 0.f ? fmaxf(ext, others[i]) : fminf(ext, others[i]);
+    // reference point of the exponents: moved only when the running max
+    // exceeds it by more than 2^8 (the weights then stay below 2^8 and O is
+    // rescaled rarely); z and l are scaled alike, so z / l is unchanged.
+    // The BF16-weights variant keeps the exact running max: its rounded
+    // weights depend on the reference point.
+    const float mx = fmaxf(m2, ext * c);
+    const float m_new = mx > m2 + (args.bf16_weights ? 0.f : 8.f) ? mx : m2;
+    const float eta = ex2_approx(m2 - m_new);  // 0 on the first block, 1 if unmoved
+    // pass 2: p = 2^(s*c - m) with one FFMA; each chunk of 32 keys is
+    // written back over its own 32 columns as 16 columns of p_hi pairs and
+    // 16 of p_lo pairs (keys 2i, 2i+1 share a column).
+    float rs = 0.f;
+    auto expo = [&](const uint32_t (&r)[32], int cc) {
+      float p[32];
+      uint32_t hi[16], lo[16];
+      if (kvalid >= KB) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          p[i] = ex2_approx(fmaf(__uint_as_float(r[i]), c, -m_new));
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          p[i] = cc * 32 + i < kvalid ? ex2_approx(fmaf(__uint_as_float(r[i]), c, -m_new))
+                                      : 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        rs += p[2 * i] + p[2 * i + 1];
+        hi[i] = pack_bf16x2(p[2 * i], p[2 * i + 1]);
+        lo[i] = pack_bf16x2(p[2 * i] - bf16_lo(hi[i]), p[2 * i + 1] - bf16_hi(hi[i]));
+      }
+      tmem_st_32x32b_x16(tS + cc * 32, hi);
+      tmem_st_32x32b_x16(tS + cc * 32 + 16, lo);
+    };
+    expo(ra, c0);
+    if (j > 0) {
+      // the previous PV of this tile has finished: O is stable
+      if (!mbar_wait(&bars->pv_done[t], (j - 1) & 1, abort_flag, args.timeout_ns)) {
+        if (lane == 0) record_error(args.err, 1, kWhere + 3, j, t * 8 + h * 4 + q);
+        bars->abort_flag = 1;
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (__any_sync(0xffffffffu, eta != 1.0f)) {
+        // this range's O columns
+        constexpr int OCH = DH / 32 / SPLIT;
+        if constexpr (OCH == 1) {
+          uint32_t ra[32];
+          tmem_ld_32x32b_x32(tO + h * 32, ra);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ra[i] = __float_as_uint(__uint_as_float(ra[i]) * eta);
+          tmem_st_32x32b_x32(tO + h * 32, ra);
+        } else {
+#pragma unroll 1
+          for (int cc = h * OCH; cc < (h + 1) * OCH; cc += 2) {
+            uint32_t ra[32], rb[32];
+            tmem_ld_32x32b_x32(tO + cc * 32, ra);
+            tmem_ld_32x32b_x32(tO + cc * 32 + 32, rb);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              ra[i] = __float_as_uint(__uint_as_float(ra[i]) * eta);
+              rb[i] = __float_as_uint(__uint_as_float(rb[i]) * eta);
+            }
+            tmem_st_32x32b_x32(tO + cc * 32, ra);
+            tmem_st_32x32b_x32(tO + cc * 32 + 32, rb);
+          }
+        }
+      }
+    }
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(&bars->p_full[0]);  // sub-tile 0's weights (and the rescaled O)
+    expo(rb, c1);
+    l = eta * l + rs;
+    m2 = m_new;
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(&bars->p_full[1]);
+  }
+  if (ok && nb > 0) {
+    float ls[SPLIT];
+    if (!mbar_wait(&bars->pv_done[t], (nb - 1) & 1, abort_flag, args.timeout_ns)) {
+      if (lane == 0) record_error(args.err, 1, kWhere + 3, nb, t * 8 + h * 4 + q);
+      bars->abort_flag = 1;
+    } else if (!exchange<SPLIT>(xslots(nb & 1), h, l, xb, nb & 1, ls, abort_flag,
+                                args.timeout_ns)) {
+      if (lane == 0) record_error(args.err, 1, kWhere + 6, nb, t * 8 + h * 4 + q);
+      bars->abort_flag = 1;
+    } else {
+      // the ranges' sums, added in range order in every warp of the row
+      float lt = ls[0];
+#pragma unroll
+      for (int i = 1; i < SPLIT; ++i) lt += ls[i];
+      tc_fence_after();
+      const int tok = q0 + t * BQ + row;
+      if (slot >= 0) {
+        // a key range of a split unit: unnormalised z, and (m, l), FP32
+        float* zs = args.part + static_cast<size_t>(slot) * PartSlot<NT>::FLOATS;
+        float* zr = zs + static_cast<size_t>(t * BQ + row) * DH;
+        constexpr int OCH = DH / 32 / SPLIT;
+#pragma unroll 1
+        for (int cc = h * OCH; cc < (h + 1) * OCH; ++cc) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tO + cc * 32, r);
+          tmem_wait_ld();
+          float4* z4 = reinterpret_cast<float4*>(zr + cc * 32);
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            z4[u] = make_float4(__uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1]),
+                                __uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3]));
+        }
+        if (h == 0) {
+          float* ml = zs + static_cast<size_t>(PartSlot<NT>::ROWS) * DH + 2 * (t * BQ + row);
+          ml[0] = m2;
+          ml[1] = lt;
+        }
+      } else {
+      uint16_t* orow =
+          args.O + head * args.o_ld_head + static_cast<int64_t>(tok) * args.o_ld_token;
+      constexpr int OCH = DH / 32 / SPLIT;
+#pragma unroll 1
+      for (int cc = h * OCH; cc < (h + 1) * OCH; ++cc) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tO + cc * 32, r);
+        tmem_wait_ld();
+        if (tok < args.Nq) {
+          uint4* o4 = reinterpret_cast<uint4*>(orow + cc * 32);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            float v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = __fdiv_rn(__uint_as_float(r[8 * u + i]), lt);
+            o4[u] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                               pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+          }
+        }
+      }
+      }
+    }
+  }
+}
+
 template <int KSUB>
 __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -397,6 +631,10 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
       mbar_init(&bars->k_empty[s], 1);
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->v_empty[s], 1);
+    }
+    if constexpr (KSUB == 2) {  // one tile: S-ready and P-ready per sub-tile
+      mbar_init(&bars->s_full[1], 1);
+      mbar_init(&bars->p_full[1], 128 * A::SPLIT);
     }
     for (int t = 0; t < NT; ++t) {
       mbar_init(&bars->s_full[t], 1);
@@ -516,6 +754,67 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
         mma_commit(&bars->s_full[t]);
       };
       if (!mbar_wait(&bars->q_full, 0, abort_flag, args.timeout_ns)) fail(-1, 2);
+      if constexpr (KSUB == 2) {
+        // one tile; per sub-tile u of block j: wait for its weights, O +=
+        // P_hi V + P_lo V over it, then the next block's scores for u (they
+        // overwrite its P after the PV MMAs, which the tensor core executes
+        // first)
+        auto issue_sub = [&](int j, int u) {
+          const int js = j * KSUB + u;
+          if (js0 + js < nsub) {
+            const int s = js & 1;
+            if (!mbar_wait(&bars->k_full[s], (js >> 1) & 1, abort_flag, args.timeout_ns)) {
+              fail(js, 0);
+              return;
+            }
+            tc_fence_after();
+            const uint32_t sQ = smem_u32(smem + A::OFF_Q);
+            const uint32_t sK = smem_u32(smem + A::OFF_K + s * 2 * TILE64);
+#pragma unroll
+            for (int kk = 0; kk < DH / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * TILE64 + (kk & 3) * 32;
+              mma_bf16_ss(tmem + A::tm_s(0) + SUB * u, sdesc_sw128(sQ + off, 16, 1024),
+                          sdesc_sw128(sK + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(&bars->k_empty[s]);
+            issued = true;
+          }
+          mma_commit(&bars->s_full[u]);  // also when the sub-tile is past the keys
+        };
+        for (int u = 0; u < KSUB && ok; ++u) issue_sub(0, u);
+        for (int j = 0; j < nb && ok; ++j) {
+          for (int u = 0; u < KSUB && ok; ++u) {
+            if (!mbar_wait(&bars->p_full[u], j & 1, abort_flag, args.timeout_ns)) {
+              fail(j, 3);
+              break;
+            }
+            tc_fence_after();
+            const int js = j * KSUB + u;
+            if (js0 + js < nsub) {
+              const int s = js & 1;
+              if (!mbar_wait(&bars->v_full[s], (js >> 1) & 1, abort_flag, args.timeout_ns)) {
+                fail(js, 4);
+                break;
+              }
+              tc_fence_after();
+              const uint32_t sV = smem_u32(smem + A::OFF_V + s * 2 * TILE64);
+              const int halves = args.bf16_weights ? 1 : 2;  // p_hi (and p_lo)
+              for (int half = 0; half < halves; ++half) {
+#pragma unroll
+                for (int kk = 0; kk < SUB / 16; ++kk) {
+                  const uint32_t pcol = SUB * u + 32 * (kk >> 1) + 8 * (kk & 1) + 16 * half;
+                  mma_bf16_ts(tmem + A::tm_o(0), tmem + A::tm_s(0) + pcol,
+                              sdesc_sw128(sV + kk * 2048, TILE64, 1024), idesc_o,
+                              (j | u | half | kk) != 0 ? 1u : 0u);
+                }
+              }
+              mma_commit(&bars->v_empty[s]);
+            }
+            if (u == KSUB - 1) mma_commit(&bars->pv_done[0]);
+            if (j + 1 < nb) issue_sub(j + 1, u);
+          }
+        }
+      } else {
       for (int t = 0; t < NT && ok; ++t) issue_s(0, t);
       for (int j = 0; j < nb && ok; ++j) {
         for (int t = 0; t < NT && ok; ++t) {
@@ -560,6 +859,7 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
         for (int u = 0; u < KSUB; ++u)
           if (js0 + j * KSUB + u < nsub) mma_commit(&bars->v_empty[(j * KSUB + u) & 1]);
       }
+      }
       if (issued) {
         mma_commit(&bars->drain);
         int dummy = 0;
@@ -568,7 +868,11 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
       }
     }
   } else {
-    softmax_role<KSUB, NT, A::SPLIT, false>(bars, smem, A::OFF_X, tmem, A::TILE_COLS, warp, lane, args, nb,
+    if constexpr (KSUB == 2)
+      softmax_role_sub<NT, A::SPLIT>(bars, smem, A::OFF_X, tmem, A::TILE_COLS, warp, lane, args,
+                                     nb, jb0, slot, head, q0, abort_flag);
+    else
+      softmax_role<KSUB, NT, A::SPLIT, false>(bars, smem, A::OFF_X, tmem, A::TILE_COLS, warp, lane, args, nb,
                                   jb0, slot, head, q0, abort_flag);
   }
 
