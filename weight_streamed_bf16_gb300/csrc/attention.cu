@@ -138,9 +138,8 @@ __device__ __forceinline__ bool exchange(float* slots, int h, float v, uint64_t*
 // each TMEM lane quarter of a tile: warp h owns the keys
 // [h*KB/SPLIT, (h+1)*KB/SPLIT) of every block (and O columns
 // [h*DH/SPLIT, ...)); the warps of a row exchange the row extremum once per
-// block and the row sum once at the end.  With PAIR the P-ready arrivals go
-// to the even CTA of the pair.
-template <int KSUB, int NT, int SPLIT, bool PAIR, class Bars>
+// block and the row sum once at the end.
+template <int KSUB, int NT, int SPLIT, class Bars>
 __device__ __forceinline__ void softmax_role(Bars* bars, uint8_t* smem, int off_x, uint32_t tmem,
                                              uint32_t tile_cols, int warp, int lane,
                                              const AttnArgs& args, int nb, int jb0, int slot,
@@ -290,9 +289,6 @@ __device__ __forceinline__ void softmax_role(Bars* bars, uint8_t* smem, int off_
     }
     tmem_wait_st();
     tc_fence_before();
-    if constexpr (PAIR)  // the even CTA of the pair issues the MMAs
-    mbar_arrive_cluster(mapa_shared(smem_u32(&bars->p_full[t]), 0));
-  else
     mbar_arrive(&bars->p_full[t]);
   }
   if (ok && nb > 0) {
@@ -872,8 +868,8 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
       softmax_role_sub<NT, A::SPLIT>(bars, smem, A::OFF_X, tmem, A::TILE_COLS, warp, lane, args,
                                      nb, jb0, slot, head, q0, abort_flag);
     else
-      softmax_role<KSUB, NT, A::SPLIT, false>(bars, smem, A::OFF_X, tmem, A::TILE_COLS, warp, lane, args, nb,
-                                  jb0, slot, head, q0, abort_flag);
+      softmax_role<KSUB, NT, A::SPLIT>(bars, smem, A::OFF_X, tmem, A::TILE_COLS, warp, lane,
+                                       args, nb, jb0, slot, head, q0, abort_flag);
   }
 
   tc_fence_before();
