@@ -76,6 +76,8 @@ struct AShape {
   __device__ static uint32_t tm_s(int t) { return TILE_COLS * t; }
   __device__ static uint32_t tm_o(int t) { return TILE_COLS * t + KB; }
 };
+// 256-key blocks keep sub-tile 0's P in the columns after O
+static_assert(AShape<2>::TILE_COLS + SUB <= AShape<2>::TM_COLS, "tensor memory");
 
 // Workspace slot of one tail-split CTA: z [NT*128 rows x 128] then (m, l)
 // per row, FP32.
@@ -358,10 +360,10 @@ __device__ __forceinline__ void softmax_role(Bars* bars, uint8_t* smem, int off_
 // 128-key sub-tiles per block, four warps per TMEM lane quarter): warp h
 // owns chunk h of each sub-tile (keys 32h.. and 128 + 32h..) and O columns
 // [32h, 32h + 32).  Each sub-tile has its own S-ready and P-ready barrier,
-// and sub-tile 0's weights are published first, so its PV product (and the
-// next block's scores for it) run on the tensor core while sub-tile 1's
-// weights are formed.  The extremum and row-sum exchanges are those of the
-// 128-key role.
+// and sub-tile 0's weights (in the columns after O) are published first, so
+// its PV product (and the next block's scores for it) run on the tensor
+// core while sub-tile 1's weights are formed.  The extremum and row-sum
+// exchanges are those of the 128-key role.
 template <int NT, int SPLIT, class Bars>
 __device__ __forceinline__ void softmax_role_sub(Bars* bars, uint8_t* smem, int off_x, uint32_t tmem,
                                              uint32_t tile_cols, int warp, int lane,
@@ -385,6 +387,10 @@ __device__ __forceinline__ void softmax_role_sub(Bars* bars, uint8_t* smem, int 
   float m2 = -INFINITY;  // running max, log2 units
   float l = 0.f;         // running sum of this range's weights
   bool ok = true;
+  // P of sub-tile 0 goes to the 128 columns after O, so that S of sub-tile
+  // 0 stays readable until the block's reference point is known
+  const uint32_t tP0 = tmem + tile_cols + lane_off;
+  const float c = args.scale_log2;  // scale * log2(e)
   for (int j = 0; j < nb; ++j) {
     if (!mbar_wait(&bars->s_full[0], j & 1, abort_flag, args.timeout_ns)) {
       if (lane == 0) record_error(args.err, 1, kWhere + 2, j, h * 4 + q);
@@ -393,10 +399,9 @@ __device__ __forceinline__ void softmax_role_sub(Bars* bars, uint8_t* smem, int 
       break;
     }
     tc_fence_after();
+    const int kvalid = args.Nk - (jb0 + j) * KB;  // keys of this block that exist
     // pass 1: row extremum of this range's raw scores (max, or min for a
     // negative scale), then the other ranges' through shared memory
-    const float c = args.scale_log2;  // scale * log2(e)
-    const int kvalid = args.Nk - (jb0 + j) * KB;  // keys of this block that exist
     float ext = c >= 0.f ? -INFINITY : INFINITY;
     auto scan = [&](const uint32_t (&r)[32], int base) {
       if (kvalid >= KB) {
@@ -416,12 +421,43 @@ __device__ __forceinline__ void softmax_role_sub(Bars* bars, uint8_t* smem, int 
             ext = c >= 0.f ? fmaxf(ext, __uint_as_float(r[i])) : fminf(ext, __uint_as_float(r[i]));
       }
     };
-    // the warp's two chunks stay in registers for pass 2; sub-tile 0 is
-    // scanned while sub-tile 1's scores are still being computed
-    uint32_t ra[32], rb[32];
-    tmem_ld_32x32b_x32(tS + c0 * 32, ra);
-    tmem_wait_ld();
-    scan(ra, c0 * 32);
+    // pass 2: p = 2^(s*c - m) with one FFMA; each chunk of 32 keys goes to
+    // 32 columns at `dst` as 16 columns of p_hi pairs and 16 of p_lo pairs
+    // (keys 2i, 2i+1 share a column); `rs` gets the chunk's sum
+    auto expo = [&](const uint32_t (&r)[32], int cc, uint32_t dst, float m, float& rs) {
+      float p[32];
+      uint32_t hi[16], lo[16];
+      if (kvalid >= KB) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) p[i] = ex2_approx(fmaf(__uint_as_float(r[i]), c, -m));
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          p[i] = cc * 32 + i < kvalid ? ex2_approx(fmaf(__uint_as_float(r[i]), c, -m)) : 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        rs += p[2 * i] + p[2 * i + 1];
+        hi[i] = pack_bf16x2(p[2 * i], p[2 * i + 1]);
+        lo[i] = pack_bf16x2(p[2 * i] - bf16_lo(hi[i]), p[2 * i + 1] - bf16_hi(hi[i]));
+      }
+      tmem_st_32x32b_x16(dst, hi);
+      tmem_st_32x32b_x16(dst + 16, lo);
+    };
+    // Sub-tile 0 is scanned while sub-tile 1's scores are computed.  With
+    // the lagging reference point (below) the reference rarely moves after
+    // the first block, so sub-tile 0's weights are formed against the
+    // current one meanwhile and the row exchange only confirms them; where
+    // it moves a row of the warp, the warp forms them again from S.
+    const bool speculate = j > 0 && !args.bf16_weights;
+    float rs0 = 0.f, rs1 = 0.f;
+    {
+      uint32_t ra[32];
+      tmem_ld_32x32b_x32(tS + c0 * 32, ra);
+      tmem_wait_ld();
+      scan(ra, c0 * 32);
+      if (speculate) expo(ra, c0, tP0 + c0 * 32, m2, rs0);
+    }
     if (!mbar_wait(&bars->s_full[1], j & 1, abort_flag, args.timeout_ns)) {
       if (lane == 0) record_error(args.err, 1, kWhere + 2, j, 64 + h * 4 + q);
       bars->abort_flag = 1;
@@ -429,13 +465,14 @@ __device__ __forceinline__ void softmax_role_sub(Bars* bars, uint8_t* smem, int 
       break;
     }
     tc_fence_after();
+    uint32_t rb[32];
     tmem_ld_32x32b_x32(tS + c1 * 32, rb);
     tmem_wait_ld();
     scan(rb, c1 * 32);
     float others[SPLIT];
     if (!exchange<SPLIT>(xslots(j & 1), h, ext, xb, j & 1, others, abort_flag,
                          args.timeout_ns)) {
-      if (lane == 0) record_error(args.err, 1, kWhere + 6, j, t * 8 + h * 4 + q);
+      if (lane == 0) record_error(args.err, 1, kWhere + 6, j, h * 4 + q);
       bars->abort_flag = 1;
       ok = false;
       break;
@@ -451,75 +488,37 @@ __device__ __forceinline__ void softmax_role_sub(Bars* bars, uint8_t* smem, int 
     const float mx = fmaxf(m2, ext * c);
     const float m_new = mx > m2 + (args.bf16_weights ? 0.f : 8.f) ? mx : m2;
     const float eta = ex2_approx(m2 - m_new);  // 0 on the first block, 1 if unmoved
-    // pass 2: p = 2^(s*c - m) with one FFMA; each chunk of 32 keys is
-    // written back over its own 32 columns as 16 columns of p_hi pairs and
-    // 16 of p_lo pairs (keys 2i, 2i+1 share a column).
-    float rs = 0.f;
-    auto expo = [&](const uint32_t (&r)[32], int cc) {
-      float p[32];
-      uint32_t hi[16], lo[16];
-      if (kvalid >= KB) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          p[i] = ex2_approx(fmaf(__uint_as_float(r[i]), c, -m_new));
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          p[i] = cc * 32 + i < kvalid ? ex2_approx(fmaf(__uint_as_float(r[i]), c, -m_new))
-                                      : 0.f;
-      }
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        rs += p[2 * i] + p[2 * i + 1];
-        hi[i] = pack_bf16x2(p[2 * i], p[2 * i + 1]);
-        lo[i] = pack_bf16x2(p[2 * i] - bf16_lo(hi[i]), p[2 * i + 1] - bf16_hi(hi[i]));
-      }
-      tmem_st_32x32b_x16(tS + cc * 32, hi);
-      tmem_st_32x32b_x16(tS + cc * 32 + 16, lo);
-    };
-    expo(ra, c0);
+    if (!speculate || __any_sync(0xffffffffu, m_new != m2)) {
+      if (speculate) tmem_wait_st();  // the first stores land before they are replaced
+      uint32_t ra[32];
+      tmem_ld_32x32b_x32(tS + c0 * 32, ra);
+      tmem_wait_ld();
+      rs0 = 0.f;
+      expo(ra, c0, tP0 + c0 * 32, m_new, rs0);
+    }
     if (j > 0) {
-      // the previous PV of this tile has finished: O is stable
-      if (!mbar_wait(&bars->pv_done[t], (j - 1) & 1, abort_flag, args.timeout_ns)) {
-        if (lane == 0) record_error(args.err, 1, kWhere + 3, j, t * 8 + h * 4 + q);
+      // the previous PV has finished: O is stable
+      if (!mbar_wait(&bars->pv_done[0], (j - 1) & 1, abort_flag, args.timeout_ns)) {
+        if (lane == 0) record_error(args.err, 1, kWhere + 3, j, h * 4 + q);
         bars->abort_flag = 1;
         ok = false;
         break;
       }
       tc_fence_after();
-      if (__any_sync(0xffffffffu, eta != 1.0f)) {
-        // this range's O columns
-        constexpr int OCH = DH / 32 / SPLIT;
-        if constexpr (OCH == 1) {
-          uint32_t ra[32];
-          tmem_ld_32x32b_x32(tO + h * 32, ra);
-          tmem_wait_ld();
+      if (__any_sync(0xffffffffu, eta != 1.0f)) {  // this range's O columns
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tO + h * 32, r);
+        tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) ra[i] = __float_as_uint(__uint_as_float(ra[i]) * eta);
-          tmem_st_32x32b_x32(tO + h * 32, ra);
-        } else {
-#pragma unroll 1
-          for (int cc = h * OCH; cc < (h + 1) * OCH; cc += 2) {
-            uint32_t ra[32], rb[32];
-            tmem_ld_32x32b_x32(tO + cc * 32, ra);
-            tmem_ld_32x32b_x32(tO + cc * 32 + 32, rb);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              ra[i] = __float_as_uint(__uint_as_float(ra[i]) * eta);
-              rb[i] = __float_as_uint(__uint_as_float(rb[i]) * eta);
-            }
-            tmem_st_32x32b_x32(tO + cc * 32, ra);
-            tmem_st_32x32b_x32(tO + cc * 32 + 32, rb);
-          }
-        }
+        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * eta);
+        tmem_st_32x32b_x32(tO + h * 32, r);
       }
     }
     tmem_wait_st();
     tc_fence_before();
     mbar_arrive(&bars->p_full[0]);  // sub-tile 0's weights (and the rescaled O)
-    expo(rb, c1);
-    l = eta * l + rs;
+    expo(rb, c1, tS + c1 * 32, m_new, rs1);  // over sub-tile 1's S
+    l = eta * l + (rs0 + rs1);
     m2 = m_new;
     tmem_wait_st();
     tc_fence_before();
@@ -798,8 +797,10 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
               for (int half = 0; half < halves; ++half) {
 #pragma unroll
                 for (int kk = 0; kk < SUB / 16; ++kk) {
-                  const uint32_t pcol = SUB * u + 32 * (kk >> 1) + 8 * (kk & 1) + 16 * half;
-                  mma_bf16_ts(tmem + A::tm_o(0), tmem + A::tm_s(0) + pcol,
+                  // sub-tile 0's P is in the columns after O, sub-tile 1's over its S
+                  const uint32_t pcol = (u == 0 ? A::TILE_COLS : SUB) + 32 * (kk >> 1) +
+                                        8 * (kk & 1) + 16 * half;
+                  mma_bf16_ts(tmem + A::tm_o(0), tmem + pcol,
                               sdesc_sw128(sV + kk * 2048, TILE64, 1024), idesc_o,
                               (j | u | half | kk) != 0 ? 1u : 0u);
                 }
