@@ -188,3 +188,30 @@ def test_attention_workspace_too_small():
                                     heads_view(V.cuda()), heads_view(O), 1, 8, 8, 128, 0.1, 128,
                                     ws.data_ptr(), 64, torch.cuda.current_stream().cuda_stream)
     assert e.value.status == psi.PSI_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("key_block", [128, 256])
+@pytest.mark.parametrize("sign", [1, -1])
+@pytest.mark.parametrize("flags", [0, psi.PSI_ATTN_BF16_WEIGHTS])
+def test_attention_reference_moves_in_later_blocks(key_block, sign, flags):
+    """Scores that grow by about 13 (log2 units) every 256 keys move the
+    reference point of the exponents after the first block (reading of
+    Eq.(4) with a lagging reference): O is rescaled in tensor memory, and
+    with 256-key blocks sub-tile 0's weights, formed ahead against the old
+    reference, are formed again.  A negative scale turns the extremum into a
+    minimum."""
+    g = torch.Generator().manual_seed(21 + key_block + sign)
+    H, Nq, Nk, dh = 2, 256, 1024, 128
+    Q = (1.0 + 0.01 * torch.randn(H, Nq, dh, generator=g)).to(torch.bfloat16)
+    level = (torch.arange(Nk) // 256).to(torch.float32) * (100.0 / dh) * sign
+    K = (level[None, :, None] + 0.05 * torch.randn(H, Nk, dh, generator=g)).to(torch.bfloat16)
+    V = torch.randn(H, Nk, dh, generator=g).to(torch.bfloat16)
+    scale = sign / math.sqrt(dh)
+    O = run_attention(Q.cuda(), K.cuda(), V.cuda(), scale, key_block=key_block, flags=flags).cpu()
+    what = f"moving reference, kb {key_block}, sign {sign}, flags {flags}"
+    if flags & psi.PSI_ATTN_BF16_WEIGHTS:
+        for h in range(H):
+            check(O[h], ops.attention_bf16_weights(f64(Q)[h], f64(K)[h], f64(V)[h], scale,
+                                                   key_block), what=f"{what}, head {h}")
+    else:
+        check(O, ops.attention_heads(f64(Q), f64(K), f64(V), scale), what=what)
