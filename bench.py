@@ -646,6 +646,19 @@ def reference_arm(args):
 
 
 # ------------------------------------------------------------------- main --
+def busy_ms(records, kind, lo, hi):
+    """Length of the union of the `kind` records' intervals clipped to
+    [lo, hi] (records of the page trace, times in ms)."""
+    iv = sorted((max(r["start_ms"], lo), min(r["end_ms"], hi)) for r in records
+                if r["kind"] == kind and r["end_ms"] > lo and r["start_ms"] < hi)
+    tot, end = 0.0, -1e300
+    for a, b in iv:
+        if b > end:
+            tot += b - max(a, end)
+            end = b
+    return tot
+
+
 def write_trace(path, wl, arena, stream, flush, torch):
     """Page timeline of two steps after the measured ones (not timed): one
     record per page copy and page GEMM from the library, the operator phase
@@ -680,19 +693,11 @@ def write_trace(path, wl, arena, stream, flush, torch):
         t = [origin.elapsed_time(e) for e in m]
         lo, hi = t[0], t[-1]
 
-        def busy(kind):
-            iv = sorted((max(r["start_ms"], lo), min(r["end_ms"], hi)) for r in rec
-                        if r["kind"] == kind and r["end_ms"] > lo and r["start_ms"] < hi)
-            tot, end = 0.0, -1e300
-            for a, b in iv:
-                if b > end:
-                    tot += b - max(a, end)
-                    end = b
-            return tot
         steps.append({"start_ms": lo, "end_ms": hi,
                       "phases": ({n: [t[i], t[i + 1]] for i, n in enumerate(names)}
                                  if names else None),
-                      "copy_busy_ms": busy("copy"), "gemm_busy_ms": busy("gemm")})
+                      "copy_busy_ms": busy_ms(rec, "copy", lo, hi),
+                      "gemm_busy_ms": busy_ms(rec, "gemm", lo, hi)})
     with open(path, "w") as f:
         json.dump({"workload": wl.name, "steps": steps, "records": rec}, f)
 

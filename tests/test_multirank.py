@@ -48,3 +48,18 @@ def test_single_rank_needs_no_process_group():
     total, per_step, value = bench.aggregate_ranks(None, torch.device("cpu"), 8.0, 1e12, 4, 1)
     assert (total, per_step) == (8.0, 2.0)
     assert value == pytest.approx(1e12 / 2e-3 / 1e12)
+
+
+def test_trace_busy_time_is_the_union_of_intervals():
+    """The page-timeline summary counts overlapping records once and clips
+    them to the step."""
+    import bench
+    rec = [{"kind": "copy", "start_ms": 0.0, "end_ms": 1.0},
+           {"kind": "copy", "start_ms": 0.5, "end_ms": 1.5},    # overlaps the first
+           {"kind": "copy", "start_ms": 2.0, "end_ms": 2.25},
+           {"kind": "gemm", "start_ms": 0.0, "end_ms": 9.0},
+           {"kind": "copy", "start_ms": 2.9, "end_ms": 3.4}]    # clipped at 3.0
+    assert abs(bench.busy_ms(rec, "copy", 0.0, 3.0) - 1.85) < 1e-12
+    assert abs(bench.busy_ms(rec, "copy", 0.75, 3.0) - (0.75 + 0.25 + 0.1)) < 1e-12
+    assert bench.busy_ms(rec, "gemm", 1.0, 2.0) == 1.0
+    assert bench.busy_ms(rec, "copy", 5.0, 6.0) == 0.0
