@@ -16,7 +16,8 @@ Where the operator has an inner BF16 write boundary (the FFN hidden slice),
 a correct FP32 evaluation may round an inner value the other way when the
 exact value lies within the FP32 error bound of a rounding boundary; the
 oracle's ``slack`` is the largest effect such flips can have on each output
-and is subtracted from |y - y_oracle| before grading.
+and is subtracted from |y - y_oracle| before grading.  ``n_pass_by_slack``
+counts the elements that are within tolerance only because of it.
 
 The tolerance is ``graded <= 2`` for every element; raw violations are listed
 with their condition number A / |y64|.  Normwise errors: max|dy| / max|y| and
@@ -55,6 +56,17 @@ def _slack_used(y, ref, res) -> int:
     return int(np.count_nonzero((np.abs(y - ref) > 0) & (slack > 0)))
 
 
+def _pass_by_slack(y, res, tol) -> int:
+    """Elements within tolerance only because of the slack: graded above
+    ``tol`` without it and at most ``tol`` with it."""
+    slack = getattr(res, "slack", None)
+    if slack is None:
+        return 0
+    with_s = graded_ulps(y, res.y, res.y64, res.A, slack)
+    without = graded_ulps(y, res.y, res.y64, res.A)
+    return int(np.count_nonzero((without > tol) & (with_s <= tol)))
+
+
 def report(y, res, tol_ulps: float = 2.0) -> dict:
     """Compare BF16 values ``y`` (float64 array) with an oracle ``Result``."""
     y = np.asarray(y, np.float64)
@@ -75,6 +87,7 @@ def report(y, res, tol_ulps: float = 2.0) -> dict:
         "all_finite": bool(finite.all()),
         "max_graded_ulps": float(g.max()) if g.size else 0.0,
         "n_slack_used": _slack_used(y, ref, res),
+        "n_pass_by_slack": _pass_by_slack(np.where(finite, y, 0.0), res, tol_ulps),
         "max_raw_ulps": int(r.max()) if r.size else 0,
         "n_raw_gt_tol": int(len(bad)),
         "n_differing": int(np.count_nonzero(r)),

@@ -368,6 +368,89 @@ def test_attention_bf16_weights_definition():
     assert 1e-5 < d < 2.0 ** -6
 
 
+def _bf16_weights_closed_form(Q, K, V, sc, kb, mp):
+    """The numerator/denominator of the BF16-weights recurrence unrolled: a
+    key j of block t gets the weight B(e^{s_j - m_t}) relative to the running
+    max m_t after block t, and the later rescales multiply it by e^{m_t - M}
+    (M the final max), so z = sum_j e^{m_t - M} B(e^{s_j - m_t}) v_j and
+    l = sum_j e^{s_j - M}.  Scores are exact rationals, exponentials are
+    taken at 60 significant digits, each weight is rounded to BF16 by the
+    rational rounder of this file.  Returns o = z/l (mpf), whether every
+    weight is at least 2^-40 (relative) away from a BF16 rounding boundary,
+    and the outputs with the weights rounded against the final max instead."""
+    def mpf(fr):
+        return mp.mpf(fr.numerator) / fr.denominator
+
+    def frac(x):
+        sign, man, ex, _ = mp.mpf(x)._mpf_      # value = (-1)^sign * man * 2^ex
+        return (-1) ** sign * Fraction(man) * Fraction(2) ** ex
+
+    n, nk = Q.shape[0], K.shape[0]
+    s = [[Fraction(sc) * sum(Fraction(float(Q[i, c])) * Fraction(float(K[j, c]))
+                             for c in range(Q.shape[1])) for j in range(nk)] for i in range(n)]
+    blocks = [range(t0, min(t0 + kb, nk)) for t0 in range(0, nk, kb)]
+    o, o_final, clear = [], [], True
+    eps = Fraction(1, 2 ** 40)
+    for i in range(n):
+        run, ms = None, []
+        for blk in blocks:
+            bm = max(s[i][j] for j in blk)
+            run = bm if run is None else max(run, bm)
+            ms.append(run)
+        M = ms[-1]
+        z = [mp.mpf(0)] * V.shape[1]
+        zf = [mp.mpf(0)] * V.shape[1]
+        den = mp.mpf(0)
+        for t, blk in enumerate(blocks):
+            resc = mp.exp(mpf(ms[t] - M))
+            for j in blk:
+                p = frac(mp.exp(mpf(s[i][j] - ms[t])))
+                w = _round_rational(p)
+                clear = clear and _round_rational(p * (1 - eps)) == _round_rational(p * (1 + eps))
+                pf = mp.exp(mpf(s[i][j] - M))
+                wf = _round_rational(frac(pf))
+                den += pf
+                for c in range(V.shape[1]):
+                    z[c] += resc * w * float(V[j, c])
+                    zf[c] += wf * float(V[j, c])
+        o.append([zc / den for zc in z])
+        o_final.append([zc / den for zc in zf])
+    return o, clear, o_final, frac
+
+
+def test_attention_bf16_weights_several_blocks_running_max_moves():
+    """Four key blocks (the last one partial) whose scores grow from block to
+    block in every row, so the running max moves at each block and every
+    earlier block's weights are rescaled: the oracle's recurrence against
+    the unrolled closed form evaluated independently in high precision.  The
+    same inputs with the weights rounded against the final max give other
+    BF16 outputs, so a recurrence that rounded against the wrong max, or
+    skipped or inverted a rescale, fails here."""
+    mp = pytest.importorskip("mpmath")
+    mp.mp.dps = 60
+    rng = np.random.default_rng(31)
+    dh, kb, nk = 8, 5, 17
+    u = np.full(dh, 0.5)
+    Q = bf16.round_bf16(u + 0.25 * rng.standard_normal((4, dh)))
+    K = bf16.round_bf16(0.5 * rng.standard_normal((nk, dh))
+                        + np.repeat(np.arange(4), kb)[:nk, None] * 1.5 * u)
+    V = _rand_bf16(rng, (nk, dh))
+    sc = 0.5
+    S = sc * Q @ K.T
+    bmax = np.stack([S[:, t0:t0 + kb].max(axis=1) for t0 in range(0, nk, kb)], axis=1)
+    assert np.all(np.diff(bmax, axis=1) > 0)       # the max moves at every block
+    r = ops.attention_bf16_weights(Q, K, V, sc, key_block=kb)
+    o, clear, o_final, frac = _bf16_weights_closed_form(Q, K, V, sc, kb, mp)
+    assert clear                       # no weight within 2^-40 of a rounding boundary
+    want64 = np.array([[float(x) for x in row] for row in o])
+    assert np.allclose(r.y64, want64, rtol=1e-13, atol=0)
+    want = np.array([[_round_rational(frac(x)) for x in row] for row in o])
+    assert np.array_equal(r.y, want)
+    assert np.all(r.slack == 0)        # no ambiguous weight, so no slack
+    wrong = np.array([[_round_rational(frac(x)) for x in row] for row in o_final])
+    assert not np.array_equal(wrong, want)
+
+
 # ------------------------------------------------- RMSNorm and split RoPE --
 def _round_rational(v: Fraction) -> float:
     """RNE to 8 significant bits of any rational (normal range), by exact
