@@ -134,21 +134,115 @@ class ClockSampler:
                 "samples": len(rows), "reasons": reasons}
 
 
-def h2d_probe(torch, dev, nbytes=1 << 30, reps=3):
-    """Host-to-device bandwidth of one large pinned cudaMemcpyAsync (GB/s)."""
+def h2d_probe(torch, dev, nbytes=1 << 30, reps=3, streams=1):
+    """Host-to-device bandwidth (GB/s, best of `reps`) of `nbytes` of pinned
+    host memory copied by `streams` concurrent cudaMemcpyAsync calls, one
+    per stream on equal parts; the interval runs from an event before the
+    first copy to the join of the last."""
     src = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
     dst = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     s = torch.cuda.current_stream()
+    side = [torch.cuda.Stream(dev) for _ in range(streams)]
+    part = nbytes // streams
     best = 0.0
     for _ in range(reps):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(s)
-        dst.copy_(src, non_blocking=True)
+        done = []
+        for i, ss in enumerate(side):
+            ss.wait_event(e0)
+            with torch.cuda.stream(ss):
+                dst[i * part:(i + 1) * part].copy_(src[i * part:(i + 1) * part],
+                                                   non_blocking=True)
+            e = torch.cuda.Event()
+            e.record(ss)
+            done.append(e)
+        for e in done:
+            s.wait_event(e)
         e1.record(s)
         e1.synchronize()
-        best = max(best, nbytes / (e0.elapsed_time(e1) * 1e-3) / 1e9)
+        best = max(best, part * streams / (e0.elapsed_time(e1) * 1e-3) / 1e9)
     del src, dst
     return best
+
+
+def gemm_alone(torch, dev, wl, peaks, flush, launches=20):
+    """The page GEMM where it is compute-bound: the block's first QKV page
+    (2048 x 4096, resident) against X [6144 x 4096], one launch per event
+    pair on the compute stream, L2 flushed before each launch; and the whole
+    resident QKV projection (6 pages on the compute and auxiliary streams)
+    timed the same way.  Algorithmic FLOPs 2*M*N*K over the event time,
+    against the burst peak (a kernel timed alone)."""
+    from weight_streamed_bf16_gb300 import psi
+    from weight_streamed_bf16_gb300.torch_io import Arena
+    bw = wl.blocks[0]
+    X = wl.X if wl.X.dim() == 2 else wl.X[0]
+    N, K = X.shape
+    rows = bw.qkv.page_rows
+    Wp = bw.qkv.host[:rows].to(dev)
+    Wall = bw.qkv.host.to(dev)
+    Y = torch.empty(N, bw.qkv.rows, dtype=torch.bfloat16, device=dev)
+    arena = Arena(wl.shape.page_bytes, 1, device=dev)
+    s = arena.compute
+    page = psi.psi_linear_weight(0, Wp.data_ptr(), rows, K, rows)
+    full = psi.psi_linear_weight(0, Wall.data_ptr(), bw.qkv.rows, K, rows)
+    out = {}
+    for name, desc, m in (("page", page, rows), ("qkv_resident", full, bw.qkv.rows)):
+        def run():
+            psi.psi_linear_paged(arena.handle, X.data_ptr(), N, K, desc, bw.bqkv.data_ptr(), None,
+                                 Y.data_ptr(), bw.qkv.rows, psi.PSI_RESIDENT)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(launches)]
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                run()
+            for e0, e1 in ev:
+                flush.fill_(7)
+                e0.record(s)
+                run()
+                e1.record(s)
+        arena.sync()
+        ms = sorted(a.elapsed_time(b) for a, b in ev)
+        med = ms[len(ms) // 2]
+        fl = 2.0 * N * m * K
+        ach = fl / (med * 1e-3) / 1e12
+        out[name] = {"ms": med, "flops": fl, "achieved": ach,
+                     "frac": ach / peaks["bf16_tflops"]}
+    arena.close()
+    del Wp, Wall, Y
+    return out
+
+
+def ingest_alone(torch, dev, link_gbs, flush, steps=20):
+    """Page ingest where it is transfer-bound: the streamed FFN configuration
+    (8 pages of 8 MiB through a 4-slot arena, 68.7 GFLOP of page GEMMs, so
+    the 67.1 MB of copies bound it), one step per event pair, L2 flushed
+    before each and every copy of the step after its start event; weight
+    bytes over the step time (median) against the H2D probe."""
+    wl = FfnWorkload(torch, dev)
+    s = wl.stream
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            wl.step()
+        for e0, e1 in ev:
+            flush.fill_(5)
+            e0.record(s)
+            # the step's page copies start after its start event (none runs
+            # ahead into the flush), so the interval holds all of its bytes
+            wl.arena.copy.wait_event(e0)
+            wl.step()
+            e1.record(s)
+    wl.arena.sync()
+    ms = sorted(a.elapsed_time(b) for a, b in ev)
+    med = ms[len(ms) // 2]
+    gbs = wl.weight_h2d / (med * 1e-3) / 1e9
+    out = {"workload": wl.name, "ms_per_step": med, "bytes_per_step": wl.weight_h2d,
+           "achieved_gbs": gbs, "link_probe_gbs": link_gbs, "frac_of_link": gbs / link_gbs,
+           "tflops": wl.flops / (med * 1e-3) / 1e12}
+    wl.arena.close()
+    return out
 
 
 def aggregate_ranks(dist, device, total_ms: float, flops_per_step: float, steps: int,
@@ -753,6 +847,8 @@ def main():
 
     peaks = load_peaks()
     link_gbs = h2d_probe(torch, dev)
+    link2_gbs = h2d_probe(torch, dev, streams=2)
+    link4_gbs = h2d_probe(torch, dev, streams=4)
     wl = make_workload(torch, dev, args)
     stream = wl.stream
     arena = getattr(wl, "arena", None)
@@ -764,17 +860,37 @@ def main():
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            wl.step()
-    if arena is not None:
-        arena.sync()
-        psi.psi_arena_reset_stats(arena.handle)
-        psi.psi_arena_set_timing(arena.handle, True)
+    def timed_loop(n, ev, loop0=None, loop1=None):
+        """n steps, each after an L2 flush (a write larger than L2) and
+        bracketed by its own event pair; loop0/loop1 span the whole loop."""
+        with torch.cuda.stream(stream):
+            if loop0 is not None:
+                loop0.record(stream)
+            for i in range(n):
+                flush.fill_(i & 0xFF)
+                ev[i][0].record(stream)
+                wl.step()
+                ev[i][1].record(stream)
+            if loop1 is not None:
+                loop1.record(stream)
+
+    # warm-up: the timed loop's own body (the first pass through it is
+    # slower on the host than the ones after it)
+    warm = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(args.warmup)]
+    timed_loop(args.warmup, warm)
+    barrier()
     j0 = wl.journal.stats() if getattr(wl, "journal", None) is not None else None
     k0 = psi.psi_kernel_launches()
 
     # ------------------------------------------------ device-timed region --
+    # One event pair spans the whole loop, the L2 flushes between steps
+    # included: ms_per_step = that time / steps, so every copy and kernel of
+    # every step is inside the interval (a step's first page copies can
+    # start during the flush before it).  The per-step pairs give the sum
+    # without the flushes.  No per-launch timing inside the library here
+    # (its event pairs around every page GEMM and copy cost about 5 % of the
+    # step); it is taken in a separate pass below.
     try:
         gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
     except Exception:
@@ -782,28 +898,33 @@ def main():
     clocks = ClockSampler(gpu_id)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
+    loop0, loop1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     clocks.start()
     t_wall = time.perf_counter()
-    with torch.cuda.stream(stream):
-        for i in range(args.steps):
-            flush.fill_(i & 0xFF)             # write > L2 between steps (not timed)
-            ev[i][0].record(stream)
-            wl.step()
-            ev[i][1].record(stream)
+    timed_loop(args.steps, ev, loop0, loop1)
     barrier()
     k1 = psi.psi_kernel_launches()
     t_wall = time.perf_counter() - t_wall
     clk = clocks.stop()
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    total_ms = sum(step_ms)
+    step_sum_ms = sum(step_ms)
+    loop_ms = loop0.elapsed_time(loop1)
+    total_ms = loop_ms
+    # the same steps again with the library's per-launch event pairs, for the
+    # in-step page-GEMM and copy figures (not for `value`)
+    st = None
+    timed_ms = None
     if arena is not None:
+        psi.psi_arena_reset_stats(arena.handle)
+        psi.psi_arena_set_timing(arena.handle, True)
+        ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        timed_loop(args.steps, ev2)
+        barrier()
+        timed_ms = sum(a.elapsed_time(b) for a, b in ev2) / args.steps
         st = psi.psi_arena_stats(arena.handle)
         psi.psi_arena_set_timing(arena.handle, False)
-        if st["pages_streamed"] or st["resident_pages"]:
-            pass
-    else:
-        st = None
     jst = None
     if getattr(wl, "journal", None) is not None:
         js = wl.journal.stats()
@@ -869,7 +990,7 @@ def main():
             d2h_s.wait_event(step_done[-1])
             t1.record(d2h_s)
 
-    e2e_run(2)
+    e2e_run(max(3, args.warmup))
     barrier()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_run(args.steps, t0, t1)
@@ -885,22 +1006,41 @@ def main():
     # ------------------------------------------------ roofline (page GEMM) --
     digest = source_digest("page_gemm.cu", "page_gemm_pair.cu", "gemm_epilogue.cuh", "ptx.cuh")
     roof = None
-    peak_t = peaks["bf16_tflops"] if wl.timed_alone else peaks["bf16_tflops_sustained"]
+    peak_s = peaks["bf16_tflops_sustained"]
     if st and st["timed_gemms"]:
         avg_ms = st["gemm_ms"] / st["timed_gemms"]
         fl_launch = st["gemm_flops"] / st["timed_gemms"]
         ach = fl_launch / (avg_ms * 1e-3) / 1e12
         busy = st["gemm_flops"] / (st["gemm_busy_ms"] * 1e-3) / 1e12 if st["gemm_busy_ms"] else None
+        in_step = {
+            "achieved": ach, "peak": peak_s, "unit": "TFLOP/s", "frac": ach / peak_s,
+            "peak_kind": f"sustained bf16, of {peaks['source']}",
+            "launches": st["timed_gemms"], "avg_launch_ms": avg_ms,
+            "flops_per_launch": fl_launch,
+            # consecutive page GEMMs overlap on two streams, which stretches
+            # each launch's event interval; FLOPs over the union of the
+            # intervals is the throughput while any page GEMM runs
+            "achieved_busy": busy, "frac_busy": busy / peak_s if busy else None,
+            "ms_per_step_with_launch_events": timed_ms}
         roof = {"kernel": "page_gemm (tcgen05, all epilogues)", "bound": "tensor",
-                "achieved": ach, "peak": peak_t, "unit": "TFLOP/s", "frac": ach / peak_t,
-                "peak_kind": ("burst" if wl.timed_alone else "sustained") + f" bf16, of {peaks['source']}",
-                "launches": st["timed_gemms"], "avg_launch_ms": avg_ms,
-                "flops_per_launch": fl_launch,
-                # consecutive page GEMMs overlap on two streams, which stretches
-                # each launch's event interval; FLOPs over the union of the
-                # intervals is the throughput while any page GEMM runs
-                "achieved_busy": busy, "frac_busy": busy / peak_t if busy else None,
-                "traffic": profile_traffic("page_gemm_block_traffic.txt", digest)}
+                "in_step": in_step}
+        if isinstance(wl, BlockWorkload):
+            # the compute-bound figure: one resident QKV page timed alone
+            ga = gemm_alone(torch, dev, wl, peaks, flush)
+            pg = ga["page"]
+            roof.update({"achieved": pg["achieved"], "peak": peaks["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": pg["frac"],
+                         "peak_kind": f"burst bf16, of {peaks['source']}",
+                         "measured": "one resident 6144x2048x4096 QKV page launch per event "
+                                     "pair, L2 flushed before each (median of 20)",
+                         "avg_launch_ms": pg["ms"], "flops_per_launch": pg["flops"],
+                         "qkv_resident": ga["qkv_resident"],
+                         "traffic": profile_traffic("page_gemm_block_traffic.txt", digest)})
+        else:
+            roof.update({k: in_step[k] for k in ("achieved", "peak", "unit", "frac",
+                                                 "peak_kind", "avg_launch_ms",
+                                                 "flops_per_launch")})
+            roof["traffic"] = None
     elif isinstance(wl, AttentionWorkload):
         ach = wl.flops / (ms_per_step * 1e-3) / 1e12
         roof = {"kernel": "attn_partitioned (tcgen05)", "bound": "tensor", "achieved": ach,
@@ -966,8 +1106,13 @@ def main():
         ingest = {"unit": "GB/s", "copy_engine_gbs": ce, "copy_busy_gbs": ce_busy,
                   "effective_gbs": eff,
                   "link_probe_gbs": link_gbs, "copy_frac_of_link": ce / link_gbs,
+                  "link_probe_two_streams_gbs": link2_gbs,
+                  "link_probe_four_streams_gbs": link4_gbs,
                   "weight_bytes_per_step": wl.weight_h2d,
                   "pages_per_step": st["pages_streamed"] / args.steps}
+        if isinstance(wl, BlockWorkload):
+            # the transfer-bound figure: the streamed FFN configuration
+            ingest["transfer_bound"] = ingest_alone(torch, dev, link_gbs, flush)
     step_bound_ms = max(wl.flops / (peaks["bf16_tflops_sustained"] * 1e12),
                         wl.weight_h2d / (link_gbs * 1e9)) * 1e3
 
@@ -986,6 +1131,11 @@ def main():
             "config": {"workload": wl.name, "l2": "flushed between steps (256 MiB write)",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "flops_per_step": wl.flops, "wall_s_timed": t_wall,
+                       # ms_per_step is the whole timed loop (one event pair,
+                       # the L2 flushes between steps included) over the
+                       # steps; this is the sum of the per-step event pairs,
+                       # flushes excluded
+                       "step_sum_ms_per_step": step_sum_ms / args.steps,
                        "step_roofline_ms": step_bound_ms,
                        "phase_ms": phases, "rmsnorm_roofline": norm_roof,
                        "managed_device_bytes": (wl.managed_bytes()

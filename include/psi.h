@@ -51,7 +51,8 @@ typedef enum {
   PSI_ERR_DEVICE = 7        /* a kernel recorded an error (bounded wait expired) */
 } psi_status;
 
-/* flags (bitwise or) */
+/* flags (bitwise or).  Each entry point lists the flags it honours; a call
+ * given any other bit fails with PSI_ERR_UNSUPPORTED and enqueues nothing. */
 #define PSI_RESIDENT              0x1u /* weights read from dev_resident: no copies */
 #define PSI_SYNC_COPY             0x2u /* H2D page copies on the compute stream */
 #define PSI_BOUNDARY_PREGELU_BF16 0x4u /* FFN: extra BF16 write of the biased
@@ -217,7 +218,7 @@ int32_t psi_arena_slots(const psi_arena* arena);
  * last release (its previous consumers); the compute stream then waits for
  * the copy.  With PSI_SYNC_COPY the copy is enqueued on the compute stream
  * instead.  PSI_ERR_PAGE_BUSY if that slot still has an unreleased request,
- * PSI_ERR_CAPACITY if bytes > page_bytes. */
+ * PSI_ERR_CAPACITY if bytes > page_bytes.  Flags: PSI_SYNC_COPY. */
 psi_status psi_page_stream(psi_arena* arena, const void* host_src, size_t bytes,
                            uint32_t flags, psi_page* out);
 /* End a request: records the slot's consumed event on the compute stream
@@ -278,7 +279,8 @@ psi_status psi_debug_stall_next_gemm(uint64_t timeout_ns);
  * PSI_RESIDENT); page GEMMs alternate between the compute stream and the
  * arena's auxiliary stream (disjoint output columns), so one page's tail
  * overlaps the next page's start.  The per-element arithmetic is the same in
- * every mode, so resident and streamed results are bitwise equal. */
+ * every mode, so resident and streamed results are bitwise equal.
+ * Flags: PSI_RESIDENT, PSI_SYNC_COPY, PSI_BIAS_AFTER_BF16. */
 psi_status psi_linear_paged(psi_arena* arena, const void* X, int64_t N, int64_t K,
                             const psi_linear_weight* W, const void* bias,
                             const void* residual, void* Y, int64_t ldy,
@@ -321,7 +323,9 @@ psi_status psi_rmsnorm(const void* X, int64_t ldx, int64_t N, int64_t d, const v
  * A streamed FFN needs an arena of at least G slots (PSI_ERR_CAPACITY).
  *   X [N x d], residual and Y [N x r] (row stride r), a [h], b [r]: dev BF16
  *   hidden_ws, acc_ws: dev workspace of psi_ffn_workspace sizes (16-byte
- *   aligned); the full [N x h] hidden tensor is never formed. */
+ *   aligned); the full [N x h] hidden tensor is never formed.
+ * Flags: PSI_RESIDENT, PSI_SYNC_COPY, PSI_BOUNDARY_PREGELU_BF16,
+ * PSI_BIAS_AFTER_BF16. */
 psi_status psi_ffn_paged(psi_arena* arena, const void* X, int64_t N,
                          const psi_ffn_weight* W, const void* a, const void* b,
                          void* hidden_ws, void* acc_ws, const void* residual,
@@ -336,7 +340,8 @@ psi_status psi_ffn_paged(psi_arena* arena, const void* X, int64_t N,
  *   key_block: 128 or 256 keys per online-softmax update (the kernel reads
  *   K and V in 128-key sub-tiles; with 256 a CTA holds one 128-query tile,
  *   with 128 two).
- * Enqueued on `stream` (cudaStream_t).  No arena: inputs are resident. */
+ * Enqueued on `stream` (cudaStream_t).  No arena: inputs are resident.
+ * Flags: PSI_ATTN_BF16_WEIGHTS. */
 psi_status psi_attn_partitioned(const psi_heads* Q, const psi_heads* K,
                                 const psi_heads* V, const psi_heads* O,
                                 int32_t heads, int64_t Nq, int64_t Nk, int32_t dh,
@@ -439,18 +444,23 @@ psi_status psi_journal_fail_next_copy(psi_journal* j);
 /* The paper has no counterpart of this entry point; it serves callers that
  * cannot allocate device memory (code running inside another framework's
  * memory pool or a fixed budget handed out at start-up, plug-ins given
- * device pointers but no allocator).  It computes exactly what
- * psi_ffn_paged computes with PSI_RESIDENT (same kernels, same slice
- * grouping, so the same bytes), on `stream` (cudaStream_t), with weights
- * read in place from W->dev_resident (the packed page image, W->host is not
- * used) and no arena.
+ * device pointers but no allocator).  It computes what psi_ffn_paged
+ * computes with PSI_RESIDENT: the same slice grouping G, the same FP32
+ * accumulation order and the same per-element epilogue arithmetic, so the
+ * same bytes (the up projections of a group are launched one slice at a
+ * time rather than merged).  It runs on `stream` (cudaStream_t), with
+ * weights read in place from W->dev_resident (the packed page image,
+ * W->host is not used) and no arena.
  *   X [N x d], residual (or NULL) and Y [N x r] (row stride r), a [h],
- *   b [r]: device BF16, 16-byte aligned; flags: PSI_BOUNDARY_PREGELU_BF16.
- * Workspace: the hidden slices of one group (N*2*slice*2 bytes, rounded up
- * to 256) and the FP32 accumulator (N*r*4 bytes) live in one fixed 16 MiB
- * device array inside the library, held on every GPU that loads it until
- * the process exits.  Larger problems fail with PSI_ERR_CAPACITY before
- * anything is enqueued.  The call makes no cudaMalloc or cudaFree and
+ *   b [r]: device BF16, 16-byte aligned.
+ *   flags: PSI_BOUNDARY_PREGELU_BF16, PSI_BIAS_AFTER_BF16 (as for
+ *   psi_ffn_paged); PSI_RESIDENT is accepted and implied; any other bit
+ *   gives PSI_ERR_UNSUPPORTED.
+ * Workspace: the hidden slices of one group (N*G*slice*2 bytes, rounded up
+ * to 256, with G as for psi_ffn_paged) and the FP32 accumulator (N*r*4
+ * bytes) live in one fixed 16 MiB device array inside the library, held on
+ * every GPU that loads it until the process exits.  Larger problems fail
+ * with PSI_ERR_CAPACITY before anything is enqueued.  The call makes no cudaMalloc or cudaFree and
  * calls no allocating library routine.
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress); make that first call before any stream capture.

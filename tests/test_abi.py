@@ -148,3 +148,69 @@ def test_trace_argument_checks_need_no_gpu(lib):
     assert C.sizeof(psi.psi_trace_record) == 48
     text = open(os.path.join(ROOT, "include", "psi.h")).read()
     assert "PSI_TRACE_COPY = 0, PSI_TRACE_GEMM = 1" in text
+
+
+def test_unknown_and_unhonoured_flags_are_refused_without_a_gpu(lib):
+    """Every operator entry point refuses a flag bit it does not honour with
+    PSI_ERR_UNSUPPORTED, before it looks at any other argument or makes any
+    CUDA call (null pointers everywhere: nothing is dereferenced)."""
+    UNS = psi.PSI_ERR_UNSUPPORTED
+    unknown = 0x1000
+    W = psi.psi_linear_weight(None, None, 64, 64, 64)
+    FW = psi.psi_ffn_weight(None, None, 64, 128, 64, 64)
+    rope = psi.psi_rope(1 << 20, 1 << 21, 64, 64, 128, 0)
+    q = psi.psi_heads(None, 128, 0)
+    pg = psi.psi_page()
+
+    def linear(f):
+        return lib.psi_linear_paged(None, None, 1, 64, C.byref(W), None, None, None, 64, f)
+
+    def linear_rope(f):
+        return lib.psi_linear_rope_paged(None, None, 1, 64, C.byref(W), None, C.byref(rope),
+                                         None, 64, f)
+
+    def ffn(f):
+        return lib.psi_ffn_paged(None, None, 1, C.byref(FW), None, None, None, None, None,
+                                 None, f)
+
+    def attn(f):
+        return lib.psi_attn_partitioned(C.byref(q), C.byref(q), C.byref(q), C.byref(q), 1, 1,
+                                        1, 128, 0.1, 128, None, f)
+
+    def attn_ws(f):
+        return lib.psi_attn_partitioned_ws(C.byref(q), C.byref(q), C.byref(q), C.byref(q), 1,
+                                           1, 1, 128, 0.1, 128, None, 0, None, f)
+
+    def noalloc(f):
+        return lib.psi_ffn_resident_noalloc(None, 1, C.byref(FW), None, None, None, None, None,
+                                            f)
+
+    def page_stream(f):
+        return lib.psi_page_stream(None, None, 0, f, C.byref(pg))
+
+    honoured = {
+        linear: psi.PSI_RESIDENT | psi.PSI_SYNC_COPY | psi.PSI_BIAS_AFTER_BF16,
+        linear_rope: (psi.PSI_RESIDENT | psi.PSI_SYNC_COPY | psi.PSI_BIAS_AFTER_BF16
+                      | psi.PSI_ROPE_AFTER_BF16),
+        ffn: (psi.PSI_RESIDENT | psi.PSI_SYNC_COPY | psi.PSI_BOUNDARY_PREGELU_BF16
+              | psi.PSI_BIAS_AFTER_BF16),
+        attn: psi.PSI_ATTN_BF16_WEIGHTS,
+        attn_ws: psi.PSI_ATTN_BF16_WEIGHTS,
+        noalloc: psi.PSI_RESIDENT | psi.PSI_BOUNDARY_PREGELU_BF16 | psi.PSI_BIAS_AFTER_BF16,
+        page_stream: psi.PSI_SYNC_COPY,
+    }
+    every = (psi.PSI_RESIDENT | psi.PSI_SYNC_COPY | psi.PSI_BOUNDARY_PREGELU_BF16
+             | psi.PSI_BIAS_AFTER_BF16 | psi.PSI_ATTN_BF16_WEIGHTS | psi.PSI_ROPE_AFTER_BF16)
+    for call, ok in honoured.items():
+        name = call.__name__
+        assert call(unknown) == UNS, name
+        assert "0x1000" in psi.psi_last_error(), name
+        for bit in range(6):
+            f = 1 << bit
+            r = call(f)
+            if f & ok:
+                assert r != UNS, (name, hex(f))   # refused later, for the null pointers
+            else:
+                assert r == UNS, (name, hex(f))
+        assert call(ok) != UNS, name
+        assert every & ~ok and call(every) == UNS, name

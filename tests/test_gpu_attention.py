@@ -67,23 +67,38 @@ def test_attention_key_block_partitions_agree():
     assert d <= 2 ** -6
 
 
-def test_attention_config_sampled_rows():
+@pytest.fixture(scope="module")
+def attn_config_run():
     """Q, K, V [32 x 4096 x 128], scale 1/sqrt(128), key blocks of 256: the
-    GPU runs the full configuration; the oracle checks every head on sampled
-    query rows."""
+    full configuration on the GPU, once for the tests below."""
     cfg = psi_synth.ATTN
     Q, K, V = psi_synth.attn_inputs(cfg)
     O = run_attention(Q.cuda(), K.cuda(), V.cuda(), cfg.scale, key_block=cfg.key_block).cpu()
+    return cfg, f64(Q), f64(K), f64(V), O
+
+
+def test_attention_config_sampled_rows(attn_config_run):
+    """Every head of the attention configuration on sampled query rows."""
+    cfg, Qf, Kf, Vf, O = attn_config_run
     rows = np.array([0, 1, 127, 128, 2047, 2048, 4000, 4095])
-    Of = f64(O)
-    Qf, Kf, Vf = f64(Q), f64(K), f64(V)
     worst = 0.0
     for h in range(cfg.heads):
         res = ops.attention(Qf[h], Kf[h], Vf[h], cfg.scale, rows=rows)
         rep = check(O[h][rows], res, what=f"head {h}")
         worst = max(worst, rep["max_rel_err"])
     assert worst <= 1e-2
-    assert np.isfinite(Of).all()
+    assert np.isfinite(f64(O)).all()
+
+
+@pytest.mark.parametrize("head", [0, 15, 31])
+def test_attention_config_full_rows(attn_config_run, head):
+    """All 4096 query rows of a head of the attention configuration (the
+    first, a middle and the last head), element by element against the dense
+    float64 softmax of Eq.(3)."""
+    cfg, Qf, Kf, Vf, O = attn_config_run
+    res = ops.attention(Qf[head], Kf[head], Vf[head], cfg.scale)
+    rep = check(O[head], res, what=f"head {head}, all rows")
+    assert rep["n"] == cfg.N * cfg.dh
 
 
 @pytest.mark.parametrize("key_block", [128, 256])

@@ -82,6 +82,25 @@ def test_block_attention_probe(block_run):
         check(att[ROWS, hd * dh:(hd + 1) * dh], res, what=f"attention head {hd}")
 
 
+@pytest.mark.parametrize("hd", [0, 31])
+def test_block_attention_full_rows(block_run, hd):
+    """All 6144 query rows of a head of the block's attention (key blocks of
+    128, heads read in place from the fused QKV output), against the dense
+    float64 softmax: head 0 runs in whole units, head 31 holds the partial
+    last wave, whose units the kernel cuts into key ranges and merges by the
+    Eq.(4) update (768 units on 152 SMs leave 8 for the tail split: head 31's
+    query rows 4096..6143)."""
+    r = block_run
+    H, dh = CFG.heads, CFG.dh
+    h = f64(r["h"])
+    q = h[:, hd * dh:(hd + 1) * dh]
+    k = h[:, H * dh + hd * dh:H * dh + (hd + 1) * dh]
+    v = h[:, 2 * H * dh + hd * dh:2 * H * dh + (hd + 1) * dh]
+    res = ops.attention(q, k, v, 1 / math.sqrt(dh))
+    rep = check(r["att"][:, hd * dh:(hd + 1) * dh], res, what=f"block attention head {hd}")
+    assert rep["n"] == CFG.N * dh
+
+
 def test_block_out_proj_probe(block_run):
     r, w = block_run, block_run["w"]
     res = ops.linear(f64(r["att"][ROWS]), f64(w["Wo"]), f64(w["bo"]),

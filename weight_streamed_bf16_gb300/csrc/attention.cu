@@ -961,14 +961,10 @@ psi_status launch_k(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensor
                     const View& vq, const View& vk, const View& vv, const AttnArgs& a,
                     cudaStream_t stream) {
   using A = AShape<KSUB>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_kernel<KSUB>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         A::SMEM_BYTES);
-    if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute(attn)");
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  psi_status st = ensure_smem_attr(&attr_done, reinterpret_cast<const void*>(attn_kernel<KSUB>),
+                                   A::SMEM_BYTES, "cudaFuncSetAttribute(attn)");
+  if (st != PSI_OK) return st;
   const int q_blocks = (a.Nq + A::NT * BQ - 1) / (A::NT * BQ);
   const long long units = static_cast<long long>(q_blocks) * a.heads;
   if (units <= 0) return PSI_OK;

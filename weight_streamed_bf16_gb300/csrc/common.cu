@@ -39,6 +39,15 @@ psi_status cuda_error(cudaError_t e, const char* what) {
 
 const char* last_error_cstr() { return t_last_error.c_str(); }
 
+psi_status check_flags(uint32_t flags, uint32_t allowed, const char* what) {
+  const uint32_t bad = flags & ~allowed;
+  if (!bad) return PSI_OK;
+  char buf[160];
+  snprintf(buf, sizeof buf, "%s: flag bits 0x%x are not honoured by this entry point", what,
+           static_cast<unsigned>(bad));
+  return set_error(PSI_ERR_UNSUPPORTED, buf);
+}
+
 DevError* dev_error_ptr() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
@@ -73,6 +82,22 @@ int num_sms() {
     g_sms[dev] = n > 0 ? n : 1;
   }
   return g_sms[dev];
+}
+
+psi_status ensure_smem_attr(std::atomic<uint64_t>* done, const void* fn, int bytes,
+                            const char* what) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_error(e, what);
+  if (dev < 0 || dev >= kMaxDevices)
+    return set_error(PSI_ERR_UNSUPPORTED, std::string(what) + ": device index above 63");
+  const uint64_t bit = 1ull << dev;
+  if (done->load(std::memory_order_acquire) & bit) return PSI_OK;
+  // setting the attribute twice (two threads racing here) is harmless
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return cuda_error(e, what);
+  done->fetch_or(bit, std::memory_order_release);
+  return PSI_OK;
 }
 
 static psi_status get_encoder() {

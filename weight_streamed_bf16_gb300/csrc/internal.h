@@ -1,5 +1,6 @@
 // internal.h -- declarations shared by the translation units of libpsi.
 #pragma once
+#include <atomic>
 #include <cstdint>
 #include <cstddef>
 #include <string>
@@ -29,6 +30,25 @@ cudaError_t dev_error_take(DevError* out);
 psi_status set_error(psi_status s, const std::string& msg);
 psi_status cuda_error(cudaError_t e, const char* what);
 
+// The flags each entry point honours; any other bit is refused with
+// PSI_ERR_UNSUPPORTED before anything is enqueued.
+constexpr uint32_t kFlagsPageStream = PSI_SYNC_COPY;
+constexpr uint32_t kFlagsLinear = PSI_RESIDENT | PSI_SYNC_COPY | PSI_BIAS_AFTER_BF16;
+constexpr uint32_t kFlagsLinearRope = kFlagsLinear | PSI_ROPE_AFTER_BF16;
+constexpr uint32_t kFlagsFfn =
+    PSI_RESIDENT | PSI_SYNC_COPY | PSI_BOUNDARY_PREGELU_BF16 | PSI_BIAS_AFTER_BF16;
+constexpr uint32_t kFlagsFfnNoAlloc = PSI_RESIDENT | PSI_BOUNDARY_PREGELU_BF16 | PSI_BIAS_AFTER_BF16;
+constexpr uint32_t kFlagsAttn = PSI_ATTN_BF16_WEIGHTS;
+psi_status check_flags(uint32_t flags, uint32_t allowed, const char* what);
+
+// Hidden slices per FFN down-projection pass (psi_ffn_paged): two slices
+// share one FP32 accumulator read-modify-write when there are at least two
+// and the slice is a whole number of 64-deep k-blocks, else one.  Fixed by
+// the shape, never by the arena, so every FFN entry point sums in the same
+// order.
+constexpr int64_t kFfnGroupMax = 2;
+inline int64_t ffn_group(int64_t S, int64_t sl) { return (S >= 2 && sl % 64 == 0) ? 2 : 1; }
+
 // Tensor maps (driver entry point obtained through the runtime).
 // 2-D BF16 tensor [rows x cols] with row stride ld (elements), box
 // {box_cols, box_rows}, 128-byte swizzle.
@@ -42,6 +62,13 @@ psi_status make_tmap_2d_ex(CUtensorMap* m, const void* base, uint64_t rows, uint
 int num_sms();
 // Count one kernel launch (psi_kernel_launches).
 void count_launch();
+// Raise `fn`'s dynamic shared-memory limit to `bytes` on the current device,
+// once per device (the attribute belongs to the device context, so a
+// process that drives several GPUs sets it on each).  `done` is the call
+// site's per-device record (bit d: device d done); safe to call from
+// several host threads.
+psi_status ensure_smem_attr(std::atomic<uint64_t>* done, const void* fn, int bytes,
+                            const char* what);
 
 // ------------------------------------------------------------ page GEMM --
 enum Epilogue : int {

@@ -55,6 +55,8 @@ extern "C" psi_status psi_ffn_resident_noalloc(const void* X, int64_t N, const p
                                                const void* av, const void* bv,
                                                const void* residual, void* Y, void* stream,
                                                uint32_t flags) {
+  psi_status fs = check_flags(flags, kFlagsFfnNoAlloc, "ffn_resident_noalloc");
+  if (fs != PSI_OK) return fs;
   if (!X || !W || !W->dev_resident || !av || !bv || !Y)
     return set_error(PSI_ERR_INVALID_ARG, "ffn_resident_noalloc: null argument");
   const int64_t d = W->d, h = W->h, r = W->r, sl = W->slice;
@@ -71,15 +73,17 @@ extern "C" psi_status psi_ffn_resident_noalloc(const void* X, int64_t N, const p
   if (N > 0x7FFFFFFF || d > 0x7FFFFFFF || h > 0x7FFFFFFF || r > 0x7FFFFFFF)
     return set_error(PSI_ERR_UNSUPPORTED, "ffn_resident_noalloc: dimension above 2^31");
   if (N == 0) return PSI_OK;
-  // the same slice grouping as psi_ffn_paged, so both give the same bytes
+  // the slice grouping of psi_ffn_paged (the same function), so both sum the
+  // down projections in the same order and give the same bytes
   const int64_t S = h / sl;
-  const int64_t G = (S >= 2 && sl % 64 == 0) ? 2 : 1;
+  const int64_t G = ffn_group(S, sl);
   const size_t hid_bytes = round256(static_cast<size_t>(N) * G * sl * 2);
   const size_t acc_bytes = static_cast<size_t>(N) * r * 4;
   if (hid_bytes + acc_bytes > kNoAllocScratchBytes)
     return set_error(PSI_ERR_CAPACITY,
                      "ffn_resident_noalloc: needs " + std::to_string(hid_bytes + acc_bytes) +
-                         " bytes of workspace (N*2*slice*2 + N*r*4), the fixed array holds " +
+                         " bytes of workspace (N*G*slice*2 rounded up to 256, plus N*r*4), "
+                         "the fixed array holds " +
                          std::to_string(kNoAllocScratchBytes));
   void* base = nullptr;
   psi_status st = scratch_address(&base);
@@ -92,8 +96,12 @@ extern "C" psi_status psi_ffn_resident_noalloc(const void* X, int64_t N, const p
   const char* src = static_cast<const char*>(W->dev_resident);
   const size_t pb = psi_ffn_page_bytes(d, r, sl);
   const uint16_t* a16 = static_cast<const uint16_t*>(av);
+  const int32_t bias_after = (flags & PSI_BIAS_AFTER_BF16) ? 1 : 0;
   for (int64_t J0 = 0; J0 < S; J0 += G) {
     const int64_t gs = (S - J0) < G ? (S - J0) : G;
+    // one up-projection launch per slice (psi_ffn_paged merges a group's two
+    // slices into one launch when slice % 256 == 0); the per-element
+    // arithmetic of the epilogue is the same either way
     for (int64_t u = 0; u < gs; ++u) {
       const int64_t J = J0 + u;
       GemmArgs up{};
@@ -102,6 +110,7 @@ extern "C" psi_status psi_ffn_resident_noalloc(const void* X, int64_t N, const p
       up.K = static_cast<int32_t>(d);
       up.epi = EPI_GELU;
       up.pregelu = (flags & PSI_BOUNDARY_PREGELU_BF16) ? 1 : 0;
+      up.bias_after_bf16 = bias_after;
       up.bias = a16 + J * sl;
       up.out = Hg + u * sl;
       up.ldo = G * sl;
@@ -121,6 +130,7 @@ extern "C" psi_status psi_ffn_resident_noalloc(const void* X, int64_t N, const p
     dn.ldacc = r;
     dn.err = err;
     dn.timeout_ns = kWaitLimitNs;
+    dn.bias_after_bf16 = bias_after;
     const bool first = J0 == 0, last = J0 + gs >= S;
     if (last) {
       dn.epi = first ? EPI_LINEAR : EPI_ACC_FINAL;

@@ -244,14 +244,10 @@ psi_status launch_rmsnorm(const void* X, int64_t ldx, int64_t N, int64_t d, cons
   if (a.stages <= kConsumerWarps)
     return set_error(PSI_ERR_UNSUPPORTED, "rmsnorm: row too wide for the shared-memory ring");
   const int smem = stage_bytes * (1 + a.stages);
-  static bool attr_set = false;  // per process; one device per process
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(rmsnorm_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kStageBudget);
-    if (e != cudaSuccess) return cuda_error(e, "rmsnorm: shared-memory attribute");
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  psi_status st = ensure_smem_attr(&attr_done, reinterpret_cast<const void*>(rmsnorm_kernel),
+                                   kStageBudget, "rmsnorm: shared-memory attribute");
+  if (st != PSI_OK) return st;
   const int grid = static_cast<int>(std::min<int64_t>(N, num_sms()));
   if (d <= 4096) {
     const int g2 = static_cast<int>(std::min<int64_t>((N + kRegWarps - 1) / kRegWarps, num_sms()));

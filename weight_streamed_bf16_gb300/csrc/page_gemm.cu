@@ -266,14 +266,10 @@ template <int BN>
 psi_status launch_bn(const CUtensorMap& tx, const CUtensorMap& tp, const CUtensorMap& tp2,
                      const CUtensorMap& to, const GemmArgs& a, cudaStream_t s) {
   using C = Cfg<BN>;
-  static bool attr_set = false;  // per process; one device per process
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(page_gemm_kernel<BN>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::SMEM_BYTES);
-    if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute(page_gemm)");
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  psi_status st = ensure_smem_attr(&attr_done, reinterpret_cast<const void*>(page_gemm_kernel<BN>),
+                                   C::SMEM_BYTES, "cudaFuncSetAttribute(page_gemm)");
+  if (st != PSI_OK) return st;
   const int tiles = ((a.M + BM - 1) / BM) * ((a.N + BN - 1) / BN);
   const int grid = tiles < num_sms() ? tiles : num_sms();
   page_gemm_kernel<BN><<<grid, kThreads, C::SMEM_BYTES, s>>>(tx, tp, tp2, to, a);

@@ -264,13 +264,10 @@ bool gemm_use_pair(int64_t M, int64_t N) { return M >= 256 && N >= 256; }
 psi_status launch_page_gemm_pair(const CUtensorMap& tx, const CUtensorMap& tp,
                                  const CUtensorMap& tp2, const CUtensorMap& to, const GemmArgs& a,
                                  cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(page_gemm_pair_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, PSMEM_BYTES);
-    if (e != cudaSuccess) return cuda_error(e, "cudaFuncSetAttribute(page_gemm_pair)");
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  psi_status st = ensure_smem_attr(&attr_done, reinterpret_cast<const void*>(page_gemm_pair_kernel),
+                                   PSMEM_BYTES, "cudaFuncSetAttribute(page_gemm_pair)");
+  if (st != PSI_OK) return st;
   const int tiles = ((a.M + 2 * BM - 1) / (2 * BM)) * ((a.N + PTILE_N - 1) / PTILE_N);
   const int max_pairs = num_sms() / 2;
   const int pairs = tiles < max_pairs ? tiles : max_pairs;

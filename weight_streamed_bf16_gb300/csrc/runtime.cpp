@@ -82,12 +82,6 @@ namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-// Hidden slices per down-projection pass.  Two slices share one FP32
-// accumulator read-modify-write (half the accumulator traffic of one slice
-// per pass); the group depends on the slice shape only, never on the arena.
-constexpr int64_t kFfnGroupMax = 2;
-int64_t ffn_group(int64_t S, int64_t sl) { return (S >= 2 && sl % 64 == 0) ? 2 : 1; }
-
 cudaEvent_t pool_get(psi_arena* a) {
   if (!a->pool.empty()) {
     cudaEvent_t e = a->pool.back();
@@ -423,6 +417,8 @@ extern "C" {
 
 psi_status psi_page_stream(psi_arena* a, const void* host_src, size_t bytes, uint32_t flags,
                            psi_page* out) {
+  psi_status fs = check_flags(flags, kFlagsPageStream, "page_stream");
+  if (fs != PSI_OK) return fs;
   if (!a) return set_error(PSI_ERR_INVALID_ARG, "page_stream: null arena");
   return page_stream_to(a, host_src, bytes, flags, a->compute, out);
 }
@@ -583,6 +579,11 @@ static psi_status linear_paged(psi_arena* a, const void* X, int64_t N, int64_t K
                                const psi_linear_weight* W, const void* bias,
                                const void* residual, void* Y, int64_t ldy, uint32_t flags,
                                const psi_rope* rope) {
+  {
+    psi_status fs = rope ? check_flags(flags, kFlagsLinearRope, "linear_rope_paged")
+                         : check_flags(flags, kFlagsLinear, "linear_paged");
+    if (fs != PSI_OK) return fs;
+  }
   if (!a || !X || !W || !bias || !Y)
     return set_error(PSI_ERR_INVALID_ARG, "linear_paged: null argument");
   if (N < 0 || K <= 0 || W->cols != K || W->rows <= 0 || W->page_rows <= 0)
@@ -705,6 +706,8 @@ psi_status psi_rmsnorm(const void* X, int64_t ldx, int64_t N, int64_t d, const v
 psi_status psi_ffn_paged(psi_arena* a, const void* X, int64_t N, const psi_ffn_weight* W,
                          const void* av, const void* bv, void* hidden_ws, void* acc_ws,
                          const void* residual, void* Y, uint32_t flags) {
+  psi_status fs = check_flags(flags, kFlagsFfn, "ffn_paged");
+  if (fs != PSI_OK) return fs;
   if (!a || !X || !W || !av || !bv || !hidden_ws || !acc_ws || !Y)
     return set_error(PSI_ERR_INVALID_ARG, "ffn_paged: null argument");
   const int64_t d = W->d, h = W->h, r = W->r, sl = W->slice;
@@ -840,6 +843,8 @@ psi_status psi_attn_partitioned_ws(const psi_heads* Q, const psi_heads* K, const
                                    const psi_heads* O, int32_t heads, int64_t Nq, int64_t Nk,
                                    int32_t dh, float scale, int32_t key_block, void* workspace,
                                    size_t workspace_bytes, void* stream, uint32_t flags) {
+  psi_status fs = check_flags(flags, kFlagsAttn, "attn");
+  if (fs != PSI_OK) return fs;
   if (!Q || !K || !V || !O || !O->ptr)
     return set_error(PSI_ERR_INVALID_ARG, "attn: null argument");
   if (heads <= 0 || Nq < 0 || Nk < 1)
