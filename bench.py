@@ -246,18 +246,20 @@ def ingest_alone(torch, dev, link_gbs, flush, steps=20):
 
 
 def aggregate_ranks(dist, device, total_ms: float, flops_per_step: float, steps: int,
-                    world: int):
-    """Whole-job figures of a replicas run: the slowest rank's time (max over
-    ranks) bounds the job; every rank processed `steps` steps of its own
-    workload, so value = world * flops_per_step * steps / max_time.  No
-    data-path collective: only this one max-reduction of the timing."""
+                    world: int, work_ranks: int | None = None):
+    """Whole-job figures: the slowest rank's time (max over ranks) bounds the
+    job.  In a replicas run every rank processed `steps` steps of its own
+    workload, so value = world * flops_per_step * steps / max_time; a run
+    whose ranks share one workload per step (work_ranks = 1) counts it once.
+    No data-path collective: only this one max-reduction of the timing."""
     import torch
     if dist is not None and world > 1:
         t = torch.tensor([total_ms], dtype=torch.float64, device=device)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_ms = float(t.item())
     ms_per_step = total_ms / steps
-    return total_ms, ms_per_step, flops_per_step * world / (ms_per_step * 1e-3) / 1e12
+    n = world if work_ranks is None else work_ranks
+    return total_ms, ms_per_step, flops_per_step * n / (ms_per_step * 1e-3) / 1e12
 
 
 # -------------------------------------------------------------- workloads --
@@ -280,6 +282,14 @@ def workload_name(args) -> str:
 
     import psi_synth
     w = args.workload
+    if getattr(args, "shard", False) and w == "block":
+        cfg = psi_synth.BLOCK
+        return (f"synthetic transformer block x1 split by output columns over {args.gpus} "
+                f"GPU(s): d_model {cfg.d}, {cfg.N} tokens, {cfg.heads} heads x {cfg.dh}, "
+                f"QKV {cfg.qkv_rows}x{cfg.d} + out {cfg.d}x{cfg.d} + FFN "
+                f"{cfg.d}->{cfg.hidden}->{cfg.d} tanh-GELU, {cfg.page_bytes // MiB} MiB pages, "
+                f"{args.arena_mib} MiB arena per GPU, weights streamed from pinned host, "
+                f"columns all-gathered between phases")
     if w in ("block", "stack"):
         cfg = psi_synth.BLOCK
         blocks = 1 if w == "block" else args.blocks
@@ -427,6 +437,64 @@ class BlockWorkload(Workload):
                 per[i].append(marks[i].elapsed_time(marks[i + 1]))
         # median per phase: one step delayed by the host does not skew it
         return {k: sorted(v)[len(v) // 2] for k, v in zip(names, per)}
+
+    def io(self):
+        return self.X, self.Y
+
+
+class ShardedBlockWorkload(Workload):
+    """The block split by output columns over the job's ranks (one part per
+    GPU): each rank streams its own pages (its heads' Q, K, V rows, its rows
+    of Wo, all of U with its rows of V) through its own 80 MiB arena, and
+    the attention output, x1 and y are all-gathered by columns between the
+    phases (NCCL).  One step is one block forward of the whole job, so the
+    algorithmic FLOPs per step are one block's (strong scaling)."""
+
+    def __init__(self, torch, dev, arena_mib=80, dist=None):
+        import psi_synth
+        from weight_streamed_bf16_gb300.block import BlockShape
+        from weight_streamed_bf16_gb300.shard import (ShardBuffers, ShardPlan, ShardRunner,
+                                                      ShardWeights)
+        from weight_streamed_bf16_gb300.torch_io import Arena
+        cfg = psi_synth.BLOCK
+        self.torch, self.dist = torch, dist
+        world = dist.get_world_size() if dist is not None else 1
+        rank = dist.get_rank() if dist is not None else 0
+        self.shape = BlockShape(d=cfg.d, N=cfg.N, heads=cfg.heads, dh=cfg.dh,
+                                hidden=cfg.hidden, slice=cfg.slice, page_bytes=cfg.page_bytes)
+        self.plan = ShardPlan(self.shape, world, rank)
+        w = psi_synth.block_weights(cfg, block=0, device=dev)
+        w = {k: v.cpu() for k, v in w.items()}
+        self.w = ShardWeights(w, self.plan, device=dev)
+        del w
+        self.arena = Arena(cfg.page_bytes, arena_mib * MiB // cfg.page_bytes, device=dev)
+        self.bufs = ShardBuffers(self.shape, device=dev)
+        self.runner = ShardRunner(self.plan, self.arena, self.bufs, device=dev,
+                                  attn_tail_split=True)
+        self.X = psi_synth.block_input(cfg, device=dev)
+        self.Y = torch.empty_like(self.X)
+        self.flops = float(cfg.flops)
+        self.world_factor = 1            # the job does one block per step in total
+        self.weight_h2d = self.w.host_bytes
+        self.name = (f"synthetic transformer block x1 split by output columns over {world} "
+                     f"GPU(s): d_model {cfg.d}, {cfg.N} tokens, {cfg.heads} heads x {cfg.dh}, "
+                     f"QKV {cfg.qkv_rows}x{cfg.d} + out {cfg.d}x{cfg.d} + FFN "
+                     f"{cfg.d}->{cfg.hidden}->{cfg.d} tanh-GELU, {cfg.page_bytes // MiB} MiB "
+                     f"pages, {arena_mib} MiB arena per GPU, weights streamed from pinned host, "
+                     f"columns all-gathered between phases")
+
+    @property
+    def stream(self):
+        return self.arena.compute
+
+    def step(self, X=None, Y=None):
+        from weight_streamed_bf16_gb300.shard import forward_parts_in_turn, forward_sharded
+        X = self.X if X is None else X
+        Y = self.Y if Y is None else Y
+        if self.dist is not None:
+            forward_sharded(self.runner, X, self.w, Y, 0)
+        else:
+            forward_parts_in_turn([self.runner], X, [self.w], Y, 0)
 
     def io(self):
         return self.X, self.Y
@@ -610,7 +678,11 @@ def psi_weight_bytes():
     return psi_synth.BLOCK.weight_bytes
 
 
-def make_workload(torch, dev, args):
+def make_workload(torch, dev, args, dist=None):
+    if args.shard:
+        if args.workload != "block":
+            raise SystemExit("--shard applies to the block workload")
+        return ShardedBlockWorkload(torch, dev, args.arena_mib, dist)
     if args.workload == "block":
         return BlockWorkload(torch, dev, 1, args.arena_mib, args.resident, args.prenorm)
     if args.workload == "stack":
@@ -819,6 +891,10 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="stack workload: arena sweep 32/80/256 MiB + resident, bitwise control")
     ap.add_argument("--cpu-rows", type=int, default=1536)
+    ap.add_argument("--shard", action="store_true",
+                    help="block: split every operator by output columns over the ranks "
+                         "(NCCL column gathers between phases; strong scaling) instead of "
+                         "running one independent block per rank")
     ap.add_argument("--trace", default=None, metavar="PATH",
                     help="after the measurements, write the page timeline of two more "
                          "steps (copies, page GEMMs, phase marks) to PATH as JSON")
@@ -849,7 +925,7 @@ def main():
     link_gbs = h2d_probe(torch, dev)
     link2_gbs = h2d_probe(torch, dev, streams=2)
     link4_gbs = h2d_probe(torch, dev, streams=4)
-    wl = make_workload(torch, dev, args)
+    wl = make_workload(torch, dev, args, dist)
     stream = wl.stream
     arena = getattr(wl, "arena", None)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -910,7 +986,12 @@ def main():
     step_ms = [a.elapsed_time(b) for a, b in ev]
     step_sum_ms = sum(step_ms)
     loop_ms = loop0.elapsed_time(loop1)
-    total_ms = loop_ms
+    # with streamed weights a step's first page copies may start before its
+    # start event (during the flush), so the whole loop is the honest time;
+    # without a copy stream every operation of a step lies between its two
+    # events and the per-step sum leaves out only the flushes
+    timing = "whole loop" if wl.weight_h2d else "sum of steps"
+    total_ms = loop_ms if wl.weight_h2d else step_sum_ms
     # the same steps again with the library's per-launch event pairs, for the
     # in-step page-GEMM and copy figures (not for `value`)
     st = None
@@ -937,8 +1018,9 @@ def main():
         jst["h2d_gbs_per_step_time"] = js["h2d_bytes"] / (total_ms * 1e-3) / 1e9
     # the library's own count of the kernels it launched in the timed region
     gpu_launches = k1 - k0
+    wf = getattr(wl, "world_factor", world)  # ranks whose work a step counts
     total_ms, ms_per_step, value = aggregate_ranks(dist, dev, total_ms, wl.flops, args.steps,
-                                                   world)
+                                                   world, wf)
 
     phases = wl.phase_split() if hasattr(wl, "phase_split") else None
 
@@ -996,7 +1078,7 @@ def main():
     e2e_run(args.steps, t0, t1)
     barrier()
     e2e_ms = t0.elapsed_time(t1)
-    e2e_ms, _, e2e_value = aggregate_ranks(dist, dev, e2e_ms, wl.flops, args.steps, world)
+    e2e_ms, _, e2e_value = aggregate_ranks(dist, dev, e2e_ms, wl.flops, args.steps, world, wf)
     in_bytes = Xh.numel() * Xh.element_size()
     out_bytes = Yh.numel() * Yh.element_size()
 
@@ -1126,16 +1208,19 @@ def main():
         out = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "higher_is_better": True, "scaling": "strong" if args.shard else "weak",
+            "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic (seeded, N(0,1/fan_in) weights)",
             "config": {"workload": wl.name, "l2": "flushed between steps (256 MiB write)",
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "parallelism": (f"output columns x{world}" if args.shard else
+                                       f"replicas x{world}" if world > 1 else "single GPU"),
                        "flops_per_step": wl.flops, "wall_s_timed": t_wall,
-                       # ms_per_step is the whole timed loop (one event pair,
-                       # the L2 flushes between steps included) over the
-                       # steps; this is the sum of the per-step event pairs,
-                       # flushes excluded
+                       # the sum of the per-step event pairs (flushes
+                       # excluded) and the whole timed loop (one event pair,
+                       # flushes included), each over the steps
                        "step_sum_ms_per_step": step_sum_ms / args.steps,
+                       "loop_ms_per_step": loop_ms / args.steps,
+                       "ms_per_step_from": timing,
                        "step_roofline_ms": step_bound_ms,
                        "phase_ms": phases, "rmsnorm_roofline": norm_roof,
                        "managed_device_bytes": (wl.managed_bytes()

@@ -180,6 +180,19 @@ const char* psi_last_error(void);
 psi_status psi_plan_linear(int64_t rows, int64_t cols, size_t page_bytes,
                            int64_t* page_rows);
 
+/* Output-column partition for sharding an operator over `parts` devices
+ * (the column-partition invariant of section II-B: every output entry still
+ * receives its complete dot product from one device, so the gathered
+ * columns equal the unpartitioned result bit for bit).  Part `part` of
+ * `parts` gets the contiguous columns [*c0, *c1) of [0, cols): boundaries
+ * are multiples of `align` (the last part ends at cols), and the parts'
+ * widths differ by at most `align`, earlier parts taking the larger ones.
+ * A part may be empty (c0 == c1) when cols < parts * align.
+ * PSI_ERR_INVALID_ARG for cols < 0, align < 1, parts < 1 or part outside
+ * [0, parts).  Host arithmetic only, no CUDA call. */
+psi_status psi_plan_columns(int64_t cols, int64_t align, int32_t parts, int32_t part,
+                            int64_t* c0, int64_t* c1);
+
 /* Bytes of one FFN page: slice*d*2 + r*slice*2. */
 size_t psi_ffn_page_bytes(int64_t d, int64_t r, int64_t slice);
 
@@ -330,6 +343,17 @@ psi_status psi_ffn_paged(psi_arena* arena, const void* X, int64_t N,
                          const psi_ffn_weight* W, const void* a, const void* b,
                          void* hidden_ws, void* acc_ws, const void* residual,
                          void* Y, uint32_t flags);
+
+/* psi_ffn_paged with Y and the residual at row stride ldy (elements; ldy >=
+ * W->r, a multiple of 8), so an FFN over a range of output columns (the
+ * rows [c0, c1) of V, packed into their own page image) can write straight
+ * into those columns of a wider activation, e.g. Y = y + c0 with ldy = the
+ * full width.  The accumulator workspace stays [N x r].  Same flags;
+ * psi_ffn_paged is this call with ldy = W->r. */
+psi_status psi_ffn_paged_strided(psi_arena* arena, const void* X, int64_t N,
+                                 const psi_ffn_weight* W, const void* a, const void* b,
+                                 void* hidden_ws, void* acc_ws, const void* residual,
+                                 void* Y, int64_t ldy, uint32_t flags);
 
 /* Partitioned attention, Eqs.(3)-(4): for every head and query row,
  * s_j = scale * q.k_j in FP32; keys are visited in blocks of key_block and

@@ -78,12 +78,17 @@ class BlockWeights:
 class BlockRunner:
     """Activation buffers and the arena for running blocks on one device."""
 
-    def __init__(self, shape: BlockShape, arena: Arena, device="cuda", rope=None):
+    def __init__(self, shape: BlockShape, arena: Arena, device="cuda", rope=None,
+                 attn_tail_split: bool = True):
         """``rope``: (cos, sin) FP32 tables [N x dh/2] (any device), required
-        for a pre-norm block."""
+        for a pre-norm block.  ``attn_tail_split``: give attention its
+        workspace, so the units of a partial last wave are cut into key
+        ranges (psi_attn_partitioned_ws); off, every (head, query tile) unit
+        is computed whole, the same way at any grid size."""
         s = shape
         self.s = s
         self.arena = arena
+        self.attn_tail_split = attn_tail_split
         self.xn = None
         if s.prenorm:
             if rope is None:
@@ -139,9 +144,13 @@ class BlockRunner:
         k = self._heads(self.h, H * dh, s.qkv)
         v = self._heads(self.h, 2 * H * dh, s.qkv)
         o = self._heads(self.att, 0, H * dh)
-        psi.psi_attn_partitioned_ws(q, k, v, o, H, N, N, dh, 1.0 / math.sqrt(dh), s.key_block,
-                                    self.attn_ws.data_ptr(), self.attn_ws.numel() * 4,
-                                    cs.cuda_stream, 0)
+        if self.attn_tail_split:
+            psi.psi_attn_partitioned_ws(q, k, v, o, H, N, N, dh, 1.0 / math.sqrt(dh),
+                                        s.key_block, self.attn_ws.data_ptr(),
+                                        self.attn_ws.numel() * 4, cs.cuda_stream, 0)
+        else:
+            psi.psi_attn_partitioned(q, k, v, o, H, N, N, dh, 1.0 / math.sqrt(dh), s.key_block,
+                                     cs.cuda_stream, 0)
         mark(2 + pn)
         psi.psi_linear_paged(A, self.att.data_ptr(), N, H * dh, W.out.desc(), W.bo.data_ptr(),
                              X.data_ptr(), self.x1.data_ptr(), s.d, flags)

@@ -204,6 +204,21 @@ psi_status psi_plan_linear(int64_t rows, int64_t cols, size_t page_bytes, int64_
   return PSI_OK;
 }
 
+psi_status psi_plan_columns(int64_t cols, int64_t align, int32_t parts, int32_t part,
+                            int64_t* c0, int64_t* c1) {
+  if (!c0 || !c1 || cols < 0 || align < 1 || parts < 1 || part < 0 || part >= parts)
+    return set_error(PSI_ERR_INVALID_ARG, "plan_columns: bad arguments");
+  // units of `align` columns (the last unit may be short), dealt out as
+  // evenly as possible, the remainder to the first parts
+  const int64_t units = (cols + align - 1) / align;
+  const int64_t base = units / parts, extra = units % parts;
+  const int64_t u0 = part * base + std::min<int64_t>(part, extra);
+  const int64_t u1 = u0 + base + (part < extra ? 1 : 0);
+  *c0 = std::min(u0 * align, cols);
+  *c1 = std::min(u1 * align, cols);
+  return PSI_OK;
+}
+
 size_t psi_ffn_page_bytes(int64_t d, int64_t r, int64_t slice) {
   if (d <= 0 || r <= 0 || slice <= 0) return 0;
   return static_cast<size_t>(slice) * static_cast<size_t>(d) * 2 +
@@ -706,6 +721,13 @@ psi_status psi_rmsnorm(const void* X, int64_t ldx, int64_t N, int64_t d, const v
 psi_status psi_ffn_paged(psi_arena* a, const void* X, int64_t N, const psi_ffn_weight* W,
                          const void* av, const void* bv, void* hidden_ws, void* acc_ws,
                          const void* residual, void* Y, uint32_t flags) {
+  return psi_ffn_paged_strided(a, X, N, W, av, bv, hidden_ws, acc_ws, residual, Y,
+                               W ? W->r : 0, flags);
+}
+
+psi_status psi_ffn_paged_strided(psi_arena* a, const void* X, int64_t N, const psi_ffn_weight* W,
+                                 const void* av, const void* bv, void* hidden_ws, void* acc_ws,
+                                 const void* residual, void* Y, int64_t ldy, uint32_t flags) {
   psi_status fs = check_flags(flags, kFlagsFfn, "ffn_paged");
   if (fs != PSI_OK) return fs;
   if (!a || !X || !W || !av || !bv || !hidden_ws || !acc_ws || !Y)
@@ -715,6 +737,8 @@ psi_status psi_ffn_paged(psi_arena* a, const void* X, int64_t N, const psi_ffn_w
     return set_error(PSI_ERR_INVALID_ARG, "ffn_paged: bad shape (h must be a multiple of slice)");
   if (d % 8 || r % 8 || sl % 16)
     return set_error(PSI_ERR_INVALID_ARG, "ffn_paged: d, r must be multiples of 8, slice of 16");
+  if (ldy < r || ldy % 8)
+    return set_error(PSI_ERR_INVALID_ARG, "ffn_paged: ldy must be >= r and a multiple of 8");
   if (!aligned16(X) || !aligned16(Y) || !aligned16(av) || !aligned16(bv) ||
       !aligned16(hidden_ws) || !aligned16(acc_ws) || (residual && !aligned16(residual)))
     return set_error(PSI_ERR_INVALID_ARG, "ffn_paged: pointers must be 16-byte aligned");
@@ -806,7 +830,7 @@ psi_status psi_ffn_paged(psi_arena* a, const void* X, int64_t N, const psi_ffn_w
       dn.bias = static_cast<const uint16_t*>(bv);
       dn.resid = static_cast<const uint16_t*>(residual);
       dn.out = static_cast<uint16_t*>(Y);
-      dn.ldo = r;
+      dn.ldo = ldy;
     } else {
       dn.epi = first ? EPI_ACC_STORE : EPI_ACC_ADD;
     }

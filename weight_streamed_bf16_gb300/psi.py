@@ -34,14 +34,14 @@ PSI_ROPE_AFTER_BF16 = 0x20
 # every entry point include/psi.h declares
 EXPORTS = [
     "psi_version", "psi_status_string", "psi_last_error",
-    "psi_plan_linear", "psi_ffn_page_bytes", "psi_ffn_pack", "psi_ffn_workspace",
+    "psi_plan_linear", "psi_plan_columns", "psi_ffn_page_bytes", "psi_ffn_pack", "psi_ffn_workspace",
     "psi_arena_create", "psi_arena_destroy", "psi_arena_slots",
     "psi_page_stream", "psi_page_release", "psi_sync", "psi_stream_wait",
     "psi_arena_stats", "psi_arena_reset_stats", "psi_arena_set_timing", "psi_kernel_launches",
     "psi_arena_trace_begin", "psi_arena_trace_get",
     "psi_arena_fail_next_copy", "psi_debug_stall_next_gemm",
     "psi_linear_paged", "psi_linear_rope_paged", "psi_rmsnorm",
-    "psi_ffn_paged", "psi_attn_partitioned", "psi_attn_partitioned_ws",
+    "psi_ffn_paged", "psi_ffn_paged_strided", "psi_attn_partitioned", "psi_attn_partitioned_ws",
     "psi_attn_workspace_size",
     "psi_ffn_resident_noalloc",
     "psi_journal_create", "psi_journal_destroy", "psi_journal_commit", "psi_journal_reload",
@@ -147,6 +147,7 @@ def load(path: str = LIB_PATH) -> C.CDLL:
         "psi_status_string": (C.c_char_p, [st]),
         "psi_last_error": (C.c_char_p, []),
         "psi_plan_linear": (st, [i64, i64, sz, C.POINTER(i64)]),
+        "psi_plan_columns": (st, [i64, i64, i32, i32, C.POINTER(i64), C.POINTER(i64)]),
         "psi_ffn_page_bytes": (sz, [i64, i64, i64]),
         "psi_ffn_pack": (st, [vp, vp, i64, i64, i64, i64, vp]),
         "psi_ffn_workspace": (st, [i64, i64, i64, C.POINTER(sz), C.POINTER(sz)]),
@@ -172,6 +173,8 @@ def load(path: str = LIB_PATH) -> C.CDLL:
         "psi_rmsnorm": (st, [vp, i64, i64, i64, vp, C.c_float, vp, i64, vp]),
         "psi_ffn_paged": (st, [vp, vp, i64, C.POINTER(psi_ffn_weight), vp, vp, vp, vp, vp,
                                vp, u32]),
+        "psi_ffn_paged_strided": (st, [vp, vp, i64, C.POINTER(psi_ffn_weight), vp, vp, vp, vp, vp,
+                                       vp, i64, u32]),
         "psi_attn_partitioned": (st, [C.POINTER(psi_heads)] * 4 +
                                  [i32, i64, i64, i32, C.c_float, i32, vp, u32]),
         "psi_attn_partitioned_ws": (st, [C.POINTER(psi_heads)] * 4 +
@@ -220,6 +223,12 @@ def psi_plan_linear(rows: int, cols: int, page_bytes: int) -> int:
     out = C.c_int64()
     _check(load().psi_plan_linear(rows, cols, page_bytes, C.byref(out)))
     return out.value
+
+
+def psi_plan_columns(cols: int, align: int, parts: int, part: int) -> tuple[int, int]:
+    c0, c1 = C.c_int64(), C.c_int64()
+    _check(load().psi_plan_columns(cols, align, parts, part, C.byref(c0), C.byref(c1)))
+    return c0.value, c1.value
 
 
 def psi_ffn_page_bytes(d: int, r: int, slice_: int) -> int:
@@ -331,6 +340,13 @@ def psi_ffn_paged(arena: int, X: int, N: int, W: psi_ffn_weight, a: int, b: int,
                   hidden_ws: int, acc_ws: int, residual: int | None, Y: int, flags: int = 0):
     _check(load().psi_ffn_paged(arena, X, N, C.byref(W), a, b, hidden_ws, acc_ws,
                                 residual or None, Y, flags))
+
+
+def psi_ffn_paged_strided(arena: int, X: int, N: int, W: psi_ffn_weight, a: int, b: int,
+                          hidden_ws: int, acc_ws: int, residual: int | None, Y: int, ldy: int,
+                          flags: int = 0):
+    _check(load().psi_ffn_paged_strided(arena, X, N, C.byref(W), a, b, hidden_ws, acc_ws,
+                                        residual or None, Y, ldy, flags))
 
 
 def psi_attn_partitioned(Q: psi_heads, K: psi_heads, V: psi_heads, O: psi_heads, heads: int,
