@@ -33,7 +33,7 @@ def _worker(rank, world, port, out):
 
 def test_two_ranks_max_time_and_weak_scaling_value():
     port = _free_port()
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()
     out = mgr.dict()
     mp.spawn(_worker, args=(2, port, out), nprocs=2, join=True)
     for r in range(2):

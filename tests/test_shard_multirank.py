@@ -135,7 +135,7 @@ def _worker(rank, world, port, out):
 
 def test_two_ranks_gathered_columns_equal_unsharded(lib):
     port = _free_port()
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()
     out = mgr.dict()
     mp.spawn(_worker, args=(2, port, out), nprocs=2, join=True)
     assert out[0]["cols"] == (0, 256, 0, 2) and out[1]["cols"] == (256, 512, 2, 4)
