@@ -890,7 +890,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true",
                     help="stack workload: arena sweep 32/80/256 MiB + resident, bitwise control")
-    ap.add_argument("--cpu-rows", type=int, default=1536)
+    ap.add_argument("--cpu-rows", type=int, default=1024,
+                    help="token (query) rows of the oracle sample for cpu_baseline "
+                         "(the block sample holds 1024)")
     ap.add_argument("--shard", action="store_true",
                     help="block: split every operator by output columns over the ranks "
                          "(NCCL column gathers between phases; strong scaling) instead of "
