@@ -9,7 +9,11 @@ paged out-projection (+ residual), paged FFN (+ residual).
 
 Printed: one JSON line (rank 0).  value = algorithmic block TFLOP/s
 (3.092 TFLOP per block per GPU, summed over ranks); page ingest GB/s and
-the roofline of the dominant kernel (the page GEMM) are reported beside it.
+the roofline of the dominant kernel (the page GEMM) are reported beside it,
+and, after the headline's timed region, `configs` holds the other
+configurations of the study (single paged linear, paged FFN, partitioned
+attention with key blocks of 256, and the 48-block stack's arena sweep with
+its bitwise transport control).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl psi|reference]
                     [--workload block|ffn|linear|attention|stack]
@@ -606,30 +610,24 @@ class AttentionWorkload(Workload):
         return self.Q, self.O
 
 
-def stack_sweep(args):
-    """The stack configuration's transport control: one 48-block stack (weights
-    in pinned host memory, plus a device-resident copy) run streamed through
-    arenas of several sizes and resident; step times and a bitwise
-    comparison of the outputs."""
-    import torch
-    from weight_streamed_bf16_gb300 import build, psi
+def stack_sweep_runs(torch, dev, blocks: int, steps: int):
+    """The stack configuration's transport control: one stack of `blocks`
+    blocks (weights in pinned host memory, plus a device-resident copy) run
+    streamed through arenas of 32, 80 and 256 MiB, resident, and streamed
+    with the copies on the compute stream (no prefetch: the scheduling
+    comparison of Table IV); the arena sweep is the Table V analog.  Each
+    run times `steps` stacks after one warm-up stack with one event pair
+    over all of them (a stack moves 19 GB of weights, far more than L2),
+    and compares its output with the first run's bit for bit."""
+    from weight_streamed_bf16_gb300 import psi
     from weight_streamed_bf16_gb300.block import BlockRunner
     from weight_streamed_bf16_gb300.torch_io import Arena
-    build.build()
-    psi.load()
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
-    peaks = load_peaks()
-    link_gbs = h2d_probe(torch, dev)
     t0 = time.perf_counter()
-    wl = BlockWorkload(torch, dev, args.blocks, 80, resident=True)
+    wl = BlockWorkload(torch, dev, blocks, 80, resident=True)
     setup_s = time.perf_counter() - t0
     wl.arena.close()
     runs = []
     ref = None
-    # the arena sweep (Table V analog), the resident control, and the
-    # synchronous-transport control (copies on the compute stream, no
-    # prefetch: the scheduling comparison of Table IV)
     for mib, flags in [(32, 0), (80, 0), (256, 0), (80, psi.PSI_RESIDENT),
                        (80, psi.PSI_SYNC_COPY)]:
         arena = Arena(wl.shape.page_bytes, mib * MiB // wl.shape.page_bytes, device=dev)
@@ -639,15 +637,14 @@ def stack_sweep(args):
         with torch.cuda.stream(arena.compute):
             runner.stack(wl.X, wl.blocks, Y, tmp, flags)           # warm-up
         arena.sync(600000)
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(arena.compute):
-            for a, b in ev:
-                a.record(arena.compute)
+            e0.record(arena.compute)
+            for _ in range(steps):
                 runner.stack(wl.X, wl.blocks, Y, tmp, flags)
-                b.record(arena.compute)
+            e1.record(arena.compute)
         arena.sync(600000)
-        ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+        ms = e0.elapsed_time(e1) / steps
         st = arena.stats()
         same = None
         if ref is None:
@@ -664,13 +661,85 @@ def stack_sweep(args):
                      "bitwise_equal_to_first": same, "pages": st["pages_streamed"]})
         arena.close()
         del runner, Y, tmp
-    print(json.dumps({
-        "metric": METRIC, "workload": f"stack of {args.blocks} synthetic blocks, transport control",
-        "steps": args.steps, "unit": "TFLOP/s", "runs": runs, "setup_s": setup_s,
-        "link_probe_gbs": link_gbs, "peaks": peaks,
-        "all_bitwise_equal": all(r["bitwise_equal_to_first"] in (None, True) for r in runs),
-    }))
+    out = {"workload": f"stack of {blocks} synthetic blocks ({len(wl.blocks) * psi_weight_bytes()} "
+                       f"bytes of weights in pinned host memory), transport control",
+           "stacks_per_run": steps, "runs": runs, "setup_s": setup_s,
+           "all_bitwise_equal": all(r["bitwise_equal_to_first"] in (None, True) for r in runs)}
+    del wl
+    torch.cuda.empty_cache()
+    return out
+
+
+def stack_sweep(args):
+    """--sweep: the stack transport control alone, as its own JSON line."""
+    import torch
+    from weight_streamed_bf16_gb300 import build, psi
+    build.build()
+    psi.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peaks = load_peaks()
+    link_gbs = h2d_probe(torch, dev)
+    out = stack_sweep_runs(torch, dev, args.blocks, args.steps)
+    out.update({"metric": METRIC, "unit": "TFLOP/s", "steps": args.steps,
+                "link_probe_gbs": link_gbs, "peaks": peaks})
+    print(json.dumps(out))
     return 0
+
+
+def time_config(torch, wl, flush, steps: int, warmup: int = 3):
+    """One of the other configurations timed as the headline is: warm-up
+    iterations of the timed body, then `steps` steps each after an L2 flush,
+    one event pair over the loop and one per step; the whole loop when the
+    workload streams weights, else the sum of the steps."""
+    s = wl.stream
+    n = warmup + steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n)]
+    l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        for i in range(n):
+            if i == warmup:
+                l0.record(s)
+            flush.fill_(i & 0xFF)
+            ev[i][0].record(s)
+            wl.step()
+            ev[i][1].record(s)
+        l1.record(s)
+    torch.cuda.synchronize()
+    step_sum = sum(a.elapsed_time(b) for a, b in ev[warmup:]) / steps
+    loop = l0.elapsed_time(l1) / steps
+    ms = loop if wl.weight_h2d else step_sum
+    return {"workload": wl.name, "ms_per_step": ms,
+            "ms_per_step_from": "whole loop" if wl.weight_h2d else "sum of steps",
+            "tflops": wl.flops / (ms * 1e-3) / 1e12,
+            "weight_gbs": wl.weight_h2d / (ms * 1e-3) / 1e9 if wl.weight_h2d else 0.0}
+
+
+def other_configs(torch, dev, flush, peaks, link_gbs, steps: int, stack_blocks: int):
+    """The other four configurations of the study, for the same JSON line:
+    the single paged linear (latency-bound), the paged FFN (bound by its
+    weight copies), partitioned attention with key blocks of 256 (tensor
+    cores, burst peak) and the stack's transport control."""
+    out = {}
+    lw = LinearWorkload(torch, dev)
+    out["linear"] = time_config(torch, lw, flush, steps)
+    out["linear"]["bound"] = "latency (8 page launches, 8 copies of 64 KiB)"
+    lw.arena.close()
+    fw = FfnWorkload(torch, dev)
+    r = time_config(torch, fw, flush, steps)
+    r.update({"bound": "host link", "frac_of_link": r["weight_gbs"] / link_gbs,
+              "link_probe_gbs": link_gbs})
+    out["ffn"] = r
+    fw.arena.close()
+    aw = AttentionWorkload(torch, dev)
+    r = time_config(torch, aw, flush, steps)
+    r.update({"bound": "tensor", "frac_of_burst_peak": r["tflops"] / peaks["bf16_tflops"]})
+    out["attention"] = r
+    del aw
+    if stack_blocks > 0:
+        out["stack"] = stack_sweep_runs(torch, dev, stack_blocks, 1)
+    return out
 
 
 def psi_weight_bytes():
@@ -893,6 +962,12 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=1024,
                     help="token (query) rows of the oracle sample for cpu_baseline "
                          "(the block sample holds 1024)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="block: skip the other configurations (linear, FFN, attention, "
+                         "stack transport control) after the headline measurement")
+    ap.add_argument("--stack-blocks", type=int, default=48,
+                    help="blocks of the stack in the default line's transport control "
+                         "(0: none)")
     ap.add_argument("--shard", action="store_true",
                     help="block: split every operator by output columns over the ranks "
                          "(NCCL column gathers between phases; strong scaling) instead of "
@@ -1200,6 +1275,13 @@ def main():
     step_bound_ms = max(wl.flops / (peaks["bf16_tflops_sustained"] * 1e12),
                         wl.weight_h2d / (link_gbs * 1e9)) * 1e3
 
+    configs = None
+    if (rank == 0 and world == 1 and args.workload == "block" and not args.shard and
+            not args.prenorm and not args.resident and not args.no_configs):
+        # the study's other configurations, measured after the headline's
+        # timed region (they do not enter `value`)
+        configs = other_configs(torch, dev, flush, peaks, link_gbs, 10, args.stack_blocks)
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         fl, sec, desc = OracleSample(args.workload).run(args.cpu_rows)
@@ -1233,7 +1315,7 @@ def main():
                     in_bytes + wl.weight_h2d, "d2h_bytes_per_step": out_bytes,
                     "ms_per_step": e2e_ms / args.steps},
             "gpu_launches": gpu_launches, "clocks": clk,
-            "peaks": peaks,
+            "peaks": peaks, "configs": configs,
         }
         print(json.dumps(out))
     if dist is not None:
