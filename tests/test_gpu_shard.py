@@ -177,3 +177,40 @@ def test_block_one_part_is_the_block():
     arena.close()
     del bw, sw
     assert torch.equal(_bits(Y), _bits(ref))
+
+
+def test_forward_sharded_one_rank_nccl():
+    """forward_sharded on a one-rank NCCL group (its phases on the arena's
+    stream, the column gathers as NCCL all-gathers on torch's stream)
+    equals the unsharded block with the attention tail split off."""
+    import os
+    import socket
+
+    import torch.distributed as dist
+    from weight_streamed_bf16_gb300.shard import forward_sharded
+    shape, w, rope, X = _block_case(False)
+    arena = Arena(CFG.page_bytes, 5)
+    ref_runner = BlockRunner(shape, arena, attn_tail_split=False)
+    bw = BlockWeights(w, shape)
+    ref = torch.empty_like(X)
+    ref_runner.forward(X, bw, ref, 0)
+    arena.sync()
+    sk = socket.socket()
+    sk.bind(("127.0.0.1", 0))
+    port = sk.getsockname()[1]
+    sk.close()
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("nccl", rank=0, world_size=1)
+    try:
+        p = ShardPlan(shape, 1, 0)
+        sw = ShardWeights(w, p)
+        runner = ShardRunner(p, arena, ShardBuffers(shape))
+        Y = torch.full_like(X, float("nan"))
+        forward_sharded(runner, X, sw, Y, 0)
+        torch.cuda.synchronize()
+        arena.sync()
+    finally:
+        dist.destroy_process_group()
+        arena.close()
+    del bw, sw
+    assert torch.equal(_bits(Y), _bits(ref))

@@ -143,6 +143,111 @@ def test_two_ranks_gathered_columns_equal_unsharded(lib):
         assert out[r]["x1"] and out[r]["y"] and out[r]["att"], out[r]
 
 
+class _OracleRunner:
+    """A part of the block computed by the oracle on the host, with the
+    interface forward_sharded drives (the GPU runner's phases, with float64
+    tensors in place of device buffers and no streams)."""
+
+    def __init__(self, plan, w, ops):
+        s = plan.shape
+        self.plan, self.s, self.w, self.ops = plan, s, w, ops
+        self.h = torch.full((s.N, s.qkv), float("nan"), dtype=torch.float64)
+        self.att = torch.full((s.N, s.heads * s.dh), float("nan"), dtype=torch.float64)
+        self.x1 = torch.full((s.N, s.d), float("nan"), dtype=torch.float64)
+
+    def gathered(self, Y):
+        return {"att": self.att, "x1": self.x1, "y": Y}
+
+    def before_collective(self):
+        pass
+
+    def after_collective(self):
+        pass
+
+    def run_phase(self, name, X, W, Y, flags=0):
+        s, w, ops, p = self.s, self.w, self.ops, self.plan
+        Xn = X.numpy()
+        if name == "qkv":
+            for r0, r1 in p.qkv_rows:
+                self.h[:, r0:r1] = torch.from_numpy(
+                    ops.linear(Xn, w["Wqkv"][r0:r1], w["bqkv"][r0:r1]).y)
+        elif name == "attention":
+            h0, h1 = p.heads
+            Hd = s.heads * s.dh
+            hn = self.h.numpy()
+            for hd in range(h0, h1):
+                c = slice(hd * s.dh, (hd + 1) * s.dh)
+                q = hn[:, hd * s.dh:(hd + 1) * s.dh]
+                k = hn[:, Hd + hd * s.dh:Hd + (hd + 1) * s.dh]
+                v = hn[:, 2 * Hd + hd * s.dh:2 * Hd + (hd + 1) * s.dh]
+                self.att[:, c] = torch.from_numpy(ops.attention(q, k, v, s.dh ** -0.5).y)
+        elif name == "out_proj":
+            c0, c1 = p.out_cols
+            self.x1[:, c0:c1] = torch.from_numpy(
+                ops.linear(self.att.numpy(), w["Wo"][c0:c1], w["bo"][c0:c1],
+                           residual=Xn[:, c0:c1]).y)
+        elif name == "ffn":
+            c0, c1 = p.out_cols
+            x1 = self.x1.numpy()
+            Y[:, c0:c1] = torch.from_numpy(
+                ops.ffn(x1, w["W1"], w["W2"][c0:c1], w["a1"], w["b1"][c0:c1],
+                        residual=x1[:, c0:c1]).y)
+
+
+def _block_worker(rank, world, port, out):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        from oracle import bf16, ops
+        from weight_streamed_bf16_gb300 import build as b, psi as p
+        from weight_streamed_bf16_gb300.block import BlockShape
+        from weight_streamed_bf16_gb300.shard import ShardPlan, forward_sharded
+        b.build()
+        p.load()
+        rng = np.random.default_rng(9)             # the same draws on every rank
+
+        def rb(shape, sd=1.0):
+            return bf16.round_bf16(rng.standard_normal(shape) * sd)
+
+        s = BlockShape(d=512, N=10, heads=4, dh=128, hidden=512, slice=256)
+        Hd = s.heads * s.dh
+        w = {"Wqkv": rb((s.qkv, s.d), s.d ** -0.5), "bqkv": rb((s.qkv,), 0.02),
+             "Wo": rb((s.d, Hd), Hd ** -0.5), "bo": rb((s.d,), 0.02),
+             "W1": rb((s.hidden, s.d), s.d ** -0.5), "a1": rb((s.hidden,), 0.02),
+             "W2": rb((s.d, s.hidden), s.hidden ** -0.5), "b1": rb((s.d,), 0.02)}
+        X = torch.from_numpy(rb((s.N, s.d)))
+        runner = _OracleRunner(ShardPlan(s, world, rank), w, ops)
+        Y = torch.full((s.N, s.d), float("nan"), dtype=torch.float64)
+        forward_sharded(runner, X, None, Y)
+        # the unsharded block, one operator after the other
+        Xn = X.numpy()
+        h = ops.linear(Xn, w["Wqkv"], w["bqkv"]).y
+        att = np.concatenate([ops.attention(h[:, i * s.dh:(i + 1) * s.dh],
+                                            h[:, Hd + i * s.dh:Hd + (i + 1) * s.dh],
+                                            h[:, 2 * Hd + i * s.dh:2 * Hd + (i + 1) * s.dh],
+                                            s.dh ** -0.5).y for i in range(s.heads)], axis=1)
+        x1 = ops.linear(att, w["Wo"], w["bo"], residual=Xn).y
+        y = ops.ffn(x1, w["W1"], w["W2"], w["a1"], w["b1"], residual=x1).y
+        out[rank] = (np.array_equal(runner.att.numpy(), att),
+                     np.array_equal(runner.x1.numpy(), x1), np.array_equal(Y.numpy(), y))
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_ranks_sharded_block_forward_equals_unsharded(lib):
+    """forward_sharded (the phases and the column gathers between them) over
+    two gloo ranks, each part computed by the oracle: the gathered attention
+    output, x1 and block output equal the unsharded block bit for bit."""
+    port = _free_port()
+    mgr = mp.get_context("spawn").Manager()
+    out = mgr.dict()
+    mp.spawn(_block_worker, args=(2, port, out), nprocs=2, join=True)
+    for r in range(2):
+        assert out[r] == (True, True, True), (r, out[r])
+
+
 def test_gather_rejects_unequal_blocks():
     from weight_streamed_bf16_gb300.shard import gather_columns
     with pytest.raises(ValueError):

@@ -142,7 +142,6 @@ class ShardRunner:
         nws = psi.psi_attn_workspace_size(s.key_block)
         self.attn_ws = (torch.empty(nws // 4, dtype=torch.float32, device=device)
                         if attn_tail_split else None)
-        self.rope_tab = None
         if s.prenorm:
             if rope is None:
                 raise ValueError("a pre-norm block needs the RoPE tables")
@@ -151,6 +150,23 @@ class ShardRunner:
 
     def _heads(self, t: torch.Tensor, col0: int, ld: int) -> psi.psi_heads:
         return psi.psi_heads(t.data_ptr() + 2 * col0, ld, self.s.dh)
+
+    def gathered(self, Y: torch.Tensor) -> dict:
+        """The tensors gathered after the phases: attention output, x1, y."""
+        return {"att": self.b.att, "x1": self.b.x1, "y": Y}
+
+    def run_phase(self, name: str, X, W, Y, flags: int = 0):
+        """Enqueue a phase on the arena's compute stream."""
+        with torch.cuda.stream(self.arena.compute):
+            self.phase(name, X, W, Y, flags)
+
+    def before_collective(self):
+        """The collective's stream (torch's current one) waits for the phase."""
+        torch.cuda.current_stream().wait_stream(self.arena.compute)
+
+    def after_collective(self):
+        """The compute stream waits for the gathered columns."""
+        self.arena.compute.wait_stream(torch.cuda.current_stream())
 
     def phase(self, name: str, X: torch.Tensor, W: ShardWeights, Y: torch.Tensor,
               flags: int = 0):
@@ -234,27 +250,27 @@ def gather_columns(T: torch.Tensor, ranges: list[tuple[int, int]], rank: int, gr
             T[:, a:b].copy_(parts[q])
 
 
-def forward_sharded(runner: ShardRunner, X: torch.Tensor, W: ShardWeights, Y: torch.Tensor,
-                    flags: int = 0, group=None):
+def forward_sharded(runner, X: torch.Tensor, W, Y: torch.Tensor, flags: int = 0, group=None):
     """One block forward of this rank's part, with the column gathers
-    between phases (torch.distributed, one process per device).  The
-    compute stream is synchronised before each gather, whose collective runs
-    on torch's current stream of the device."""
+    between phases (torch.distributed, one process per device): after the
+    attention phase the attention output, after the out-projection x1, after
+    the FFN y.  ``runner`` is a ShardRunner (or any object with its
+    ``plan``, ``run_phase``, ``gathered``, ``before_collective`` and
+    ``after_collective``); the collective runs on torch's current stream,
+    ordered after the phase and before the next one by the runner's hooks."""
     import torch.distributed as dist
     rank = dist.get_rank(group)
     plan = runner.plan
     ranges = {"att": plan.all("att_cols"), "x1": plan.all("out_cols"),
               "y": plan.all("out_cols")}
-    bufs = {"att": runner.b.att, "x1": runner.b.x1, "y": Y}
-    cs = runner.arena.compute
+    bufs = runner.gathered(Y)
     for name in ShardRunner.PHASES:
-        with torch.cuda.stream(cs):
-            runner.phase(name, X, W, Y, flags)
+        runner.run_phase(name, X, W, Y, flags)
         g = ShardRunner.GATHERED.get(name)
         if g is not None:
-            torch.cuda.current_stream().wait_stream(cs)
+            runner.before_collective()
             gather_columns(bufs[g], ranges[g], rank, group)
-            cs.wait_stream(torch.cuda.current_stream())
+            runner.after_collective()
 
 
 def forward_parts_in_turn(runners: list[ShardRunner], X: torch.Tensor, weights: list,
