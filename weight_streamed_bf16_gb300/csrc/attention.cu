@@ -722,9 +722,17 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
         bars->abort_flag = 1;
         ok = false;
       };
+      // Shared-memory descriptors are formed once: the start-address field
+      // holds address / 16 in its low 14 bits, and every operand lies below
+      // 256 KB, so the descriptor of base + off is the base's descriptor +
+      // off / 16.  The tensor core queues about one instruction, so the
+      // issue loops keep only that addition between MMAs.
+      const uint64_t dq0 = sdesc_sw128(smem_u32(smem + A::OFF_Q), 16, 1024);
+      const uint64_t dk0 = sdesc_sw128(smem_u32(smem + A::OFF_K), 16, 1024);
+      const uint64_t dv0 = sdesc_sw128(smem_u32(smem + A::OFF_V), TILE64, 1024);
       // S_t = Q_t K^T for the sub-tiles of key block j, into tile t's S columns
       auto issue_s = [&](int j, int t) {
-        const uint32_t sQ = smem_u32(smem + A::OFF_Q + t * 2 * TILE64);
+        const uint64_t dq = dq0 + static_cast<uint64_t>((t * 2 * TILE64) >> 4);
         for (int u = 0; u < KSUB; ++u) {
           const int js = j * KSUB + u;
           if (js0 + js >= nsub) break;
@@ -736,12 +744,12 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
             }
             tc_fence_after();
           }
-          const uint32_t sK = smem_u32(smem + A::OFF_K + s * 2 * TILE64);
+          const uint64_t dk = dk0 + static_cast<uint64_t>((s * 2 * TILE64) >> 4);
+          const uint32_t d_tm = tmem + A::tm_s(t) + SUB * u;
 #pragma unroll
           for (int kk = 0; kk < DH / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * TILE64 + (kk & 3) * 32;
-            mma_bf16_ss(tmem + A::tm_s(t) + SUB * u, sdesc_sw128(sQ + off, 16, 1024),
-                        sdesc_sw128(sK + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+            const uint32_t off = ((kk >> 2) * TILE64 + (kk & 3) * 32) >> 4;
+            mma_bf16_ss(d_tm, dq + off, dk + off, idesc_s, kk > 0 ? 1u : 0u);
           }
           if (t == NT - 1) mma_commit(&bars->k_empty[s]);  // every tile has read it
           issued = true;
@@ -763,13 +771,12 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
               return;
             }
             tc_fence_after();
-            const uint32_t sQ = smem_u32(smem + A::OFF_Q);
-            const uint32_t sK = smem_u32(smem + A::OFF_K + s * 2 * TILE64);
+            const uint64_t dk = dk0 + static_cast<uint64_t>((s * 2 * TILE64) >> 4);
+            const uint32_t d_tm = tmem + A::tm_s(0) + SUB * u;
 #pragma unroll
             for (int kk = 0; kk < DH / 16; ++kk) {
-              const uint32_t off = (kk >> 2) * TILE64 + (kk & 3) * 32;
-              mma_bf16_ss(tmem + A::tm_s(0) + SUB * u, sdesc_sw128(sQ + off, 16, 1024),
-                          sdesc_sw128(sK + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+              const uint32_t off = ((kk >> 2) * TILE64 + (kk & 3) * 32) >> 4;
+              mma_bf16_ss(d_tm, dq0 + off, dk + off, idesc_s, kk > 0 ? 1u : 0u);
             }
             mma_commit(&bars->k_empty[s]);
             issued = true;
@@ -792,17 +799,18 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
                 break;
               }
               tc_fence_after();
-              const uint32_t sV = smem_u32(smem + A::OFF_V + s * 2 * TILE64);
+              const uint64_t dv = dv0 + static_cast<uint64_t>((s * 2 * TILE64) >> 4);
               const int halves = args.bf16_weights ? 1 : 2;  // p_hi (and p_lo)
+              // sub-tile 0's P is in the columns after O, sub-tile 1's over its S
+              const uint32_t pbase = tmem + (u == 0 ? A::TILE_COLS : SUB);
+              const uint32_t o_tm = tmem + A::tm_o(0);
+              const uint32_t first = (j | u) != 0 ? 1u : 0u;
               for (int half = 0; half < halves; ++half) {
 #pragma unroll
                 for (int kk = 0; kk < SUB / 16; ++kk) {
-                  // sub-tile 0's P is in the columns after O, sub-tile 1's over its S
-                  const uint32_t pcol = (u == 0 ? A::TILE_COLS : SUB) + 32 * (kk >> 1) +
-                                        8 * (kk & 1) + 16 * half;
-                  mma_bf16_ts(tmem + A::tm_o(0), tmem + pcol,
-                              sdesc_sw128(sV + kk * 2048, TILE64, 1024), idesc_o,
-                              (j | u | half | kk) != 0 ? 1u : 0u);
+                  const uint32_t pcol = 32 * (kk >> 1) + 8 * (kk & 1) + 16 * half;
+                  mma_bf16_ts(o_tm, pbase + pcol, dv + ((kk * 2048) >> 4), idesc_o,
+                              (half | kk) != 0 ? 1u : first);
                 }
               }
               mma_commit(&bars->v_empty[s]);
@@ -834,15 +842,17 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
               }
               tc_fence_after();
             }
-            const uint32_t sV = smem_u32(smem + A::OFF_V + s * 2 * TILE64);
+            const uint64_t dv = dv0 + static_cast<uint64_t>((s * 2 * TILE64) >> 4);
             const int halves = args.bf16_weights ? 1 : 2;  // p_hi (and p_lo)
+            const uint32_t pbase = tmem + A::tm_s(t) + SUB * u;
+            const uint32_t o_tm = tmem + A::tm_o(t);
+            const uint32_t first = (j | u) != 0 ? 1u : 0u;
             for (int half = 0; half < halves; ++half) {
 #pragma unroll
               for (int kk = 0; kk < SUB / 16; ++kk) {
-                const uint32_t pcol = SUB * u + 32 * (kk >> 1) + 8 * (kk & 1) + 16 * half;
-                mma_bf16_ts(tmem + A::tm_o(t), tmem + A::tm_s(t) + pcol,
-                            sdesc_sw128(sV + kk * 2048, TILE64, 1024), idesc_o,
-                            (j | u | half | kk) != 0 ? 1u : 0u);
+                const uint32_t pcol = 32 * (kk >> 1) + 8 * (kk & 1) + 16 * half;
+                mma_bf16_ts(o_tm, pbase + pcol, dv + ((kk * 2048) >> 4), idesc_o,
+                            (half | kk) != 0 ? 1u : first);
               }
             }
           }
