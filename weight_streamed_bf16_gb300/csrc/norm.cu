@@ -3,9 +3,10 @@
 // from the global sum of squares s.
 //
 // HBM-bound: one read of X and one BF16 write of Y.  Rows of up to 4096
-// elements: 16 warps per SM each normalise whole rows from registers (16
-// vectors of 16 bytes per lane), so 16 rows are in flight per SM; gamma is
-// staged in shared memory once per CTA.  Wider rows: a persistent CTA per SM
+// elements: 12 to 16 warps per SM (chosen per launch from the row count)
+// each normalise whole rows from registers (16 vectors of 16 bytes per
+// lane), so that many rows are in flight per SM; gamma is staged in shared
+// memory once per CTA.  Wider rows: a persistent CTA per SM
 // stages whole rows in shared memory with untiled bulk copies (one producer
 // thread keeps a ring of up to 24 rows in flight), consumer warps normalise
 // a row in place, and a bulk store writes it back.  (The bulk-copy form is
@@ -16,6 +17,7 @@
 // vectors (the width partitions), then a butterfly over the 32 lanes
 // combines them: one fixed order, one denominator per row.
 #include <algorithm>
+#include <utility>
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -171,9 +173,12 @@ __global__ void __launch_bounds__(kNormThreads, 1) rmsnorm_kernel(NormArgs a) {
 }
 
 
-// Rows of up to 4096 elements, whole rows per warp from registers.
-constexpr int kRegWarps = 16;
-__global__ void __launch_bounds__(32 * kRegWarps, 1) rmsnorm_reg_kernel(NormArgs a) {
+// Rows of up to 4096 elements, whole rows per warp from registers; W warps
+// per CTA, one CTA per SM (the launch picks W so that the rows fill the
+// warps' last round as fully as possible).
+template <int W>
+__global__ void __launch_bounds__(32 * W, 1) rmsnorm_reg_kernel(NormArgs a) {
+  constexpr int kRegWarps = W;
   __shared__ __align__(16) uint4 g4s[512];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nv = a.d >> 3;
@@ -223,6 +228,18 @@ __global__ void __launch_bounds__(32 * kRegWarps, 1) rmsnorm_reg_kernel(NormArgs
   }
 }
 
+constexpr int kMinRegWarps = 12;
+constexpr int kMaxRegWarps = 16;
+using RegKernel = void (*)(NormArgs);
+template <int... Ws>
+const RegKernel* reg_kernel_table(std::integer_sequence<int, Ws...>) {
+  static const RegKernel table[] = {&rmsnorm_reg_kernel<kMinRegWarps + Ws>...};
+  return table;
+}
+const RegKernel* reg_kernels() {
+  return reg_kernel_table(std::make_integer_sequence<int, kMaxRegWarps - kMinRegWarps + 1>{});
+}
+
 }  // namespace
 
 psi_status launch_rmsnorm(const void* X, int64_t ldx, int64_t N, int64_t d, const void* gamma,
@@ -250,8 +267,22 @@ psi_status launch_rmsnorm(const void* X, int64_t ldx, int64_t N, int64_t d, cons
   if (st != PSI_OK) return st;
   const int grid = static_cast<int>(std::min<int64_t>(N, num_sms()));
   if (d <= 4096) {
-    const int g2 = static_cast<int>(std::min<int64_t>((N + kRegWarps - 1) / kRegWarps, num_sms()));
-    rmsnorm_reg_kernel<<<g2, 32 * kRegWarps, 0, stream>>>(a);
+    // warps per CTA: each warp takes whole rows in rounds of sms * W rows;
+    // choose W in [kMinRegWarps, kMaxRegWarps] with the fewest idle warp
+    // slots in the last round (ties: fewer warps)
+    const int64_t sms = num_sms();
+    int best_w = kMinRegWarps;
+    int64_t best_idle = -1;
+    for (int w = kMinRegWarps; w <= kMaxRegWarps; ++w) {
+      const int64_t slots = sms * w;
+      const int64_t idle = (N + slots - 1) / slots * slots - N;
+      if (best_idle < 0 || idle < best_idle) {
+        best_idle = idle;
+        best_w = w;
+      }
+    }
+    const int g2 = static_cast<int>(std::min<int64_t>((N + best_w - 1) / best_w, sms));
+    reg_kernels()[best_w - kMinRegWarps]<<<g2, 32 * best_w, 0, stream>>>(a);
   } else {
     rmsnorm_kernel<<<grid, kNormThreads, smem, stream>>>(a);
   }
