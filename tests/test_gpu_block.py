@@ -101,6 +101,59 @@ def test_block_attention_full_rows(block_run, hd):
     assert rep["n"] == CFG.N * dh
 
 
+# 256 token rows spread over all 6144 (every 24th, first and last included)
+WIDE = np.unique(np.concatenate([np.arange(0, CFG.N, 24), [CFG.N - 1]]))
+
+
+def test_block_projection_probes_wide(block_run):
+    """The block's QKV projection, out-projection and FFN on 257 token rows
+    spread over the whole sequence, each fed the GPU's own BF16 inputs to the
+    operator (the same-input probes of section IV-B), element by element."""
+    r, w = block_run, block_run["w"]
+    res = ops.linear(f64(r["X"][WIDE]), f64(w["Wqkv"]), f64(w["bqkv"]))
+    check(r["h"][WIDE], res, what="qkv, 257 rows")
+    res = ops.linear(f64(r["att"][WIDE]), f64(w["Wo"]), f64(w["bo"]),
+                     residual=f64(r["X"][WIDE]))
+    check(r["x1"][WIDE], res, what="out-proj, 257 rows")
+    x1 = f64(r["x1"][WIDE])
+    res = ops.ffn(x1, f64(w["W1"]), f64(w["W2"]), f64(w["a1"]), f64(w["b1"]), residual=x1)
+    check(r["Y"][WIDE], res, what="ffn, 257 rows")
+
+
+def test_stack_last_block_probes():
+    """A 4-block stack streamed through the 80 MiB arena: the last block's
+    operators against the oracle on its own GPU inputs (QKV, attention of
+    two heads, out-projection and FFN on sampled rows), so accuracy holds
+    after the residual stream has passed three blocks."""
+    ws = [_weights(b, resident=False) for b in range(4)]
+    X = psi_synth.block_input(CFG, device="cuda")
+    arena = Arena(CFG.page_bytes, 5)
+    runner = BlockRunner(_shape(), arena)
+    Y, tmp = torch.empty_like(X), torch.empty_like(X)
+    runner.stack(X, [bw for _, bw in ws], Y, tmp, 0)   # block 3 reads tmp, writes Y
+    arena.sync()
+    w = ws[3][0]
+    x_in, h, att, x1, y = (t.cpu() for t in (tmp, runner.h, runner.att, runner.x1, Y))
+    arena.close()
+    rows = WIDE[::4]
+    check(h[rows], ops.linear(f64(x_in[rows]), f64(w["Wqkv"]), f64(w["bqkv"])),
+          what="stack block 3 qkv")
+    H, dh = CFG.heads, CFG.dh
+    hf = f64(h)
+    for hd in (5, 30):
+        q = hf[rows, hd * dh:(hd + 1) * dh]
+        k = hf[:, H * dh + hd * dh:H * dh + (hd + 1) * dh]
+        v = hf[:, 2 * H * dh + hd * dh:2 * H * dh + (hd + 1) * dh]
+        check(att[rows, hd * dh:(hd + 1) * dh], ops.attention(q, k, v, 1 / math.sqrt(dh)),
+              what=f"stack block 3 attention head {hd}")
+    check(x1[rows], ops.linear(f64(att[rows]), f64(w["Wo"]), f64(w["bo"]),
+                               residual=f64(x_in[rows])), what="stack block 3 out-proj")
+    x1r = f64(x1[rows])
+    check(y[rows], ops.ffn(x1r, f64(w["W1"]), f64(w["W2"]), f64(w["a1"]), f64(w["b1"]),
+                           residual=x1r), what="stack block 3 ffn")
+    assert torch.isfinite(y.float()).all()
+
+
 def test_block_out_proj_probe(block_run):
     r, w = block_run, block_run["w"]
     res = ops.linear(f64(r["att"][ROWS]), f64(w["Wo"]), f64(w["bo"]),
