@@ -213,6 +213,28 @@ def gemm_alone(torch, dev, wl, peaks, flush, launches=20):
         out[name] = {"ms": med, "flops": fl, "achieved": ach,
                      "frac": ach / peaks["bf16_tflops"]}
     arena.close()
+    # The same two products through cuBLAS (torch.matmul), timed the same
+    # way: a reference point for the kernel on this shape, not part of the
+    # product path (which never calls a library GEMM).
+    lib = {}
+    for name, W, m in (("page", Wp, rows), ("qkv_resident", Wall, bw.qkv.rows)):
+        Yl = torch.empty(N, m, dtype=torch.bfloat16, device=dev)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(launches)]
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                torch.matmul(X, W.t(), out=Yl)
+            for e0, e1 in ev:
+                flush.fill_(7)
+                e0.record(s)
+                torch.matmul(X, W.t(), out=Yl)
+                e1.record(s)
+        torch.cuda.synchronize()
+        ms = sorted(a.elapsed_time(b) for a, b in ev)
+        med = ms[len(ms) // 2]
+        lib[name] = {"ms": med, "achieved": 2.0 * N * m * K / (med * 1e-3) / 1e12}
+        del Yl
+    out["cublas_same_shape"] = lib
     del Wp, Wall, Y
     return out
 
@@ -1194,6 +1216,7 @@ def main():
                                      "pair, L2 flushed before each (median of 20)",
                          "avg_launch_ms": pg["ms"], "flops_per_launch": pg["flops"],
                          "qkv_resident": ga["qkv_resident"],
+                         "cublas_same_shape": ga["cublas_same_shape"],
                          "traffic": profile_traffic("page_gemm_block_traffic.txt", digest)})
         else:
             roof.update({k: in_step[k] for k in ("achieved", "peak", "unit", "frac",

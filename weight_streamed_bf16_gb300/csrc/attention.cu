@@ -10,7 +10,9 @@
 // block), read as 128-key K/V sub-tiles.  A CTA holds NT query tiles of 128
 // (NT = 2 for 128-key blocks, 1 for 256-key blocks):
 //   warp 0      TMA producer: Q once, then per block its K sub-tiles and its
-//               V sub-tiles into 2-stage rings
+//               V sub-tiles into 2-stage rings (with 128-key blocks, V of
+//               block j and K of block j + 1 complete one barrier, so the
+//               MMA issuer waits once per block for its copies)
 //   warp 1      TMEM owner and MMA issuer:
 //                 S_t = Q_t K^T            (M=128, N=128 per sub-tile, K=128)
 //                                          into the S/P columns of tile t
@@ -668,6 +670,39 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
           tma_load_2d(smem + A::OFF_Q + (t * 2 + cb) * TILE64, &tmQ, &bars->q_full,
                       head * vq.hx + cb * 64, head * vq.hy + q0 + t * BQ);
       bool ok = true;
+      if constexpr (KSUB == 1) {
+        // K(0) on k_full[0]; then per block j, V(j) and K(j+1) together on
+        // v_full[j & 1], so the MMA issuer waits once per block for both
+        auto load_kv = [&](const CUtensorMap* m, const View& vw, int off, int stage, int j,
+                           uint64_t* full) {
+          uint8_t* dst = smem + off + stage * 2 * TILE64;
+          const int key0 = (js0 + j) * SUB;
+          tma_load_2d(dst, m, full, head * vw.hx, head * vw.hy + key0);
+          tma_load_2d(dst + TILE64, m, full, head * vw.hx + 64, head * vw.hy + key0);
+        };
+        if (nb > 0) {
+          mbar_arrive_expect_tx(&bars->k_full[0], 2 * TILE64);
+          load_kv(&tmK, vk, A::OFF_K, 0, 0, &bars->k_full[0]);
+          k_cnt[0] = 1;
+        }
+        for (int j = 0; j < nb && ok; ++j) {
+          const int sv = j & 1, sk = (j + 1) & 1;
+          const bool knext = j + 1 < nb;
+          if (!mbar_wait(&bars->v_empty[sv], ((j >> 1) & 1) ^ 1, abort_flag, args.timeout_ns) ||
+              (knext && !mbar_wait(&bars->k_empty[sk], (((j + 1) >> 1) & 1) ^ 1, abort_flag,
+                                   args.timeout_ns))) {
+            record_error(args.err, 1, kWhere + 0, j, 2);
+            bars->abort_flag = 1;
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bars->v_full[sv], (knext ? 4 : 2) * TILE64);
+          load_kv(&tmV, vv, A::OFF_V, sv, j, &bars->v_full[sv]);
+          if (knext) load_kv(&tmK, vk, A::OFF_K, sk, j + 1, &bars->v_full[sv]);
+          v_armed = (v_armed & ~(1u << sv)) | (static_cast<uint32_t>(v_cnt[sv] & 1) << sv);
+          ++v_cnt[sv];
+        }
+      } else
       for (int j = 0; j < nb && ok; ++j) {
         for (int kv = 0; kv < 2 && ok; ++kv) {
           for (int u = 0; u < KSUB; ++u) {
@@ -737,7 +772,9 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
           const int js = j * KSUB + u;
           if (js0 + js >= nsub) break;
           const int s = js & 1;
-          if (t == 0) {
+          // with one 128-key sub-tile per block, K(j) for j > 0 arrived with
+          // V(j - 1), whose barrier the PV MMAs of block j - 1 waited for
+          if (t == 0 && (KSUB != 1 || j == 0)) {
             if (!mbar_wait(&bars->k_full[s], (js >> 1) & 1, abort_flag, args.timeout_ns)) {
               fail(js, 0);
               return;

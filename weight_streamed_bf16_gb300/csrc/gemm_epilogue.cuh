@@ -21,11 +21,17 @@ __device__ __forceinline__ void record_error(DevError* e, int code, int where, i
 }
 
 __device__ __forceinline__ float gelu_tanh(float x) {
-  // tanh form of GELU: x/2 (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3)))
+  // tanh form of GELU: x/2 (1 + tanh(u)), u = sqrt(2/pi) (x + 0.044715 x^3).
+  // (1 + tanh u) / 2 is the logistic function of 2u, so the same value is
+  // x / (1 + e^{-2u}), with e^{-2u} = 2^{-2u log2(e)} from ex2 (relative
+  // error about 2^-22) and the approximate quotient (2 ulp).  Unlike
+  // 1 + tanh(u), which cancels for negative u, this keeps about 2^-21
+  // relative accuracy for every x; where e^{-2u} exceeds 2^126 (x below
+  // about -9.7) the quotient is 0, against a true magnitude below 2^-126 |x|.
   const float k0 = 0.7978845608028654f;
   const float k1 = 0.044715f;
   const float u = k0 * fmaf(k1 * x * x, x, x);
-  return 0.5f * x * (1.0f + tanhf(u));
+  return __fdividef(x, 1.0f + ex2_approx(-2.8853900817779268f * u));
 }
 
 __device__ __forceinline__ float round_bf16_f(float x) {
