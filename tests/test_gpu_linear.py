@@ -71,6 +71,33 @@ def test_linear_resident_streamed_sync_bitwise():
         assert torch.equal(a.view(torch.int16), o.view(torch.int16))
 
 
+@pytest.mark.parametrize("N,M,page_rows,flags", [
+    (512, 1536, 512, 0),                          # three whole pages
+    (300, 1280, 512, 0),                          # ragged last page of 256 rows
+    (600, 1024, 256, psi.PSI_BIAS_AFTER_BF16),    # four pages, baseline rounding order
+])
+def test_linear_resident_one_launch_bitwise(N, M, page_rows, flags):
+    """Resident pages on CTA pairs with 256-aligned page boundaries run as one
+    launch over all pages: the same tiles and per-element arithmetic as the
+    per-page launches of the streamed path, so the bytes are equal."""
+    g = torch.Generator().manual_seed(N + M)
+    K = 512
+    X = torch.randn(N, K, generator=g).to(torch.bfloat16)
+    W = (torch.randn(M, K, generator=g) / math.sqrt(K)).to(torch.bfloat16)
+    b = (torch.randn(M, generator=g) * 0.02).to(torch.bfloat16)
+    R = torch.randn(N, M, generator=g).to(torch.bfloat16)
+    n0 = psi.psi_kernel_launches()
+    s = run_linear(X, W, b, page_rows, 2, flags=flags, residual=R)
+    n1 = psi.psi_kernel_launches()
+    r = run_linear(X, W, b, page_rows, 2, flags=flags | psi.PSI_RESIDENT, residual=R)
+    n2 = psi.psi_kernel_launches()
+    assert n1 - n0 == -(-M // page_rows) and n2 - n1 == 1
+    assert torch.equal(s.view(torch.int16), r.view(torch.int16))
+    check(r, ops.linear(f64(X), f64(W), f64(b), residual=f64(R),
+                        bias_after_bf16=bool(flags & psi.PSI_BIAS_AFTER_BF16)),
+          what=f"resident one launch {N}x{K}x{M}")
+
+
 def test_linear_special_values():
     """W = I gives B(x + b); an all-zero input gives B(b)."""
     X = torch.randn(64, 128).to(torch.bfloat16)

@@ -117,6 +117,9 @@ struct GemmArgs {
 psi_status launch_page_gemm(const void* X, int64_t ldx, const void* P, int64_t ldp,
                             const GemmArgs& args, cudaStream_t stream,
                             const void* P2 = nullptr);
+// Whether an M x N page GEMM runs on CTA pairs (256 x 256 tiles); the choice
+// depends on the shape only.
+bool gemm_use_pair(int64_t M, int64_t N);
 
 // ------------------------------------------------------------ attention --
 struct AttnArgs {

@@ -284,7 +284,6 @@ psi_status launch_bn(const CUtensorMap& tx, const CUtensorMap& tp, const CUtenso
 int gemm_bn_for(int64_t N) { return N > 128 ? 256 : (N > 64 ? 128 : 64); }
 
 // page_gemm_pair.cu
-bool gemm_use_pair(int64_t M, int64_t N);
 psi_status launch_page_gemm_pair(const CUtensorMap& tx, const CUtensorMap& tp,
                                  const CUtensorMap& tp2, const CUtensorMap& to, const GemmArgs& a,
                                  cudaStream_t s);

@@ -633,16 +633,30 @@ static psi_status linear_paged(psi_arena* a, const void* X, int64_t N, int64_t K
       return set_error(PSI_ERR_INVALID_ARG,
                        "linear_rope_paged: page_rows must be a multiple of dh");
   }
-  const int64_t npages = (W->rows + W->page_rows - 1) / W->page_rows;
+  int64_t npages = (W->rows + W->page_rows - 1) / W->page_rows;
   DevError* err = dev_error_ptr();
+  // Resident weights need no page ring: when every page would run on CTA
+  // pairs with page boundaries on 256-row tile boundaries, one launch covers
+  // all pages with exactly the per-page launches' tiles (the same kernel and
+  // per-element arithmetic, so the result is bit for bit the same), and the
+  // ramp, last-tile epilogue and launch gap are paid once per operator.
+  const int64_t last_rows = W->rows - (npages - 1) * W->page_rows;
+  const bool one_launch = resident && npages > 1 && W->page_rows % 256 == 0 &&
+                          gemm_use_pair(N, W->page_rows) && gemm_use_pair(N, last_rows);
+  int64_t page_rows = W->page_rows;
+  if (one_launch) {
+    a->stats.resident_pages += npages - 1;  // pages covered, counted as before
+    page_rows = W->rows;
+    npages = 1;
+  }
   // pages alternate between the compute and the auxiliary stream (outputs are
   // disjoint column blocks); aux first catches up with the compute stream
   psi_status fst = stream_after(a->ev_fork, a->compute, a->aux);
   if (fst != PSI_OK) return fst;
   for (int64_t p = 0; p < npages; ++p) {
     cudaStream_t cs = (p & 1) ? a->aux : a->compute;
-    const int64_t r0 = p * W->page_rows;
-    const int64_t rows_p = std::min(W->page_rows, W->rows - r0);
+    const int64_t r0 = p * page_rows;
+    const int64_t rows_p = std::min(page_rows, W->rows - r0);
     const size_t off = static_cast<size_t>(r0) * K * 2;
     const size_t nbytes = static_cast<size_t>(rows_p) * K * 2;
     psi_page pg{};
