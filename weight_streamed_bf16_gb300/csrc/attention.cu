@@ -10,9 +10,10 @@
 // block), read as 128-key K/V sub-tiles.  A CTA holds NT query tiles of 128
 // (NT = 2 for 128-key blocks, 1 for 256-key blocks):
 //   warp 0      TMA producer: Q once, then per block its K sub-tiles and its
-//               V sub-tiles into 2-stage rings (with 128-key blocks, V of
-//               block j and K of block j + 1 complete one barrier, so the
-//               MMA issuer waits once per block for its copies)
+//               V sub-tiles into rings (V of block j and K of block j + 1
+//               complete one barrier per sub-tile, so the MMA issuer waits
+//               once per sub-tile for its copies; with 256-key blocks the K
+//               ring has 3 stages so that this pairing never delays V)
 //   warp 1      TMEM owner and MMA issuer:
 //                 S_t = Q_t K^T            (M=128, N=128 per sub-tile, K=128)
 //                                          into the S/P columns of tile t
@@ -64,8 +65,12 @@ struct AShape {
   static constexpr int SPLIT = KSUB == 1 ? 2 : 4;
   static constexpr int kThreads = 64 + NT * 128 * SPLIT;
   static constexpr int OFF_Q = 0;                          // NT tiles x 2 column blocks
-  static constexpr int OFF_K = OFF_Q + NT * 2 * TILE64;    // 2 stages x 2 column blocks
-  static constexpr int OFF_V = OFF_K + 2 * 2 * TILE64;
+  // K ring stages (x 2 column blocks): 3 with 256-key blocks, so that K of
+  // block j + 1 can share a copy barrier with V of block j without waiting
+  // for the scores that read the stage before it
+  static constexpr int KSTAGES = KSUB == 1 ? 2 : 3;
+  static constexpr int OFF_K = OFF_Q + NT * 2 * TILE64;
+  static constexpr int OFF_V = OFF_K + KSTAGES * 2 * TILE64;
   static constexpr int OFF_BAR = OFF_V + 2 * 2 * TILE64;
   // row-extremum and row-sum exchange between the key ranges of a row:
   // [2 parities][NT tiles][SPLIT ranges][128 rows] floats
@@ -91,7 +96,7 @@ struct PartSlot {
 
 struct __align__(8) ABars {
   uint64_t q_full;
-  uint64_t k_full[2], k_empty[2];
+  uint64_t k_full[2], k_empty[3];
   uint64_t v_full[2], v_empty[2];
   uint64_t s_full[2], p_full[2], pv_done[2];
   uint64_t xbar[2][4];  // per tile and lane quarter: the row's key ranges met
@@ -626,6 +631,7 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->k_empty[s], 1);
+      if (s == 0 && A::KSTAGES == 3) mbar_init(&bars->k_empty[2], 1);
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->v_empty[s], 1);
     }
@@ -670,16 +676,17 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
           tma_load_2d(smem + A::OFF_Q + (t * 2 + cb) * TILE64, &tmQ, &bars->q_full,
                       head * vq.hx + cb * 64, head * vq.hy + q0 + t * BQ);
       bool ok = true;
+      // sub-tile js of the range (128 keys) into ring stage `stage` at `off`
+      auto load_kv = [&](const CUtensorMap* m, const View& vw, int off, int stage, int js,
+                         uint64_t* full) {
+        uint8_t* dst = smem + off + stage * 2 * TILE64;
+        const int key0 = (js0 + js) * SUB;
+        tma_load_2d(dst, m, full, head * vw.hx, head * vw.hy + key0);
+        tma_load_2d(dst + TILE64, m, full, head * vw.hx + 64, head * vw.hy + key0);
+      };
       if constexpr (KSUB == 1) {
         // K(0) on k_full[0]; then per block j, V(j) and K(j+1) together on
         // v_full[j & 1], so the MMA issuer waits once per block for both
-        auto load_kv = [&](const CUtensorMap* m, const View& vw, int off, int stage, int j,
-                           uint64_t* full) {
-          uint8_t* dst = smem + off + stage * 2 * TILE64;
-          const int key0 = (js0 + j) * SUB;
-          tma_load_2d(dst, m, full, head * vw.hx, head * vw.hy + key0);
-          tma_load_2d(dst + TILE64, m, full, head * vw.hx + 64, head * vw.hy + key0);
-        };
         if (nb > 0) {
           mbar_arrive_expect_tx(&bars->k_full[0], 2 * TILE64);
           load_kv(&tmK, vk, A::OFF_K, 0, 0, &bars->k_full[0]);
@@ -702,36 +709,36 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
           v_armed = (v_armed & ~(1u << sv)) | (static_cast<uint32_t>(v_cnt[sv] & 1) << sv);
           ++v_cnt[sv];
         }
-      } else
-      for (int j = 0; j < nb && ok; ++j) {
-        for (int kv = 0; kv < 2 && ok; ++kv) {
-          for (int u = 0; u < KSUB; ++u) {
-            const int js = j * KSUB + u;       // sub-tile within the range
+      } else {
+        // 256-key blocks: K of block 0's sub-tiles on k_full[u]; then, per
+        // sub-tile u of block j, V(j, u) and K(j + 1, u) together on
+        // v_full[u].  K sub-tile js lives in stage js % 3, V sub-tile js in
+        // stage js & 1 (= u).
+        for (int u = 0; u < KSUB; ++u) {
+          if (js0 + u >= nsub) break;
+          mbar_arrive_expect_tx(&bars->k_full[u], 2 * TILE64);
+          load_kv(&tmK, vk, A::OFF_K, u, u, &bars->k_full[u]);
+          k_cnt[u] = 1;
+        }
+        for (int j = 0; j < nb && ok; ++j) {
+          for (int u = 0; u < KSUB && ok; ++u) {
+            const int js = j * KSUB + u;
             if (js0 + js >= nsub) break;
-            const int s = js & 1;
-            const uint32_t par = ((js >> 1) & 1) ^ 1;
-            uint64_t* empty = kv ? &bars->v_empty[s] : &bars->k_empty[s];
-            uint64_t* full = kv ? &bars->v_full[s] : &bars->k_full[s];
-            if (!mbar_wait(empty, par, abort_flag, args.timeout_ns)) {
-              record_error(args.err, 1, kWhere + 0, js, kv);
+            const int kn = js + KSUB, sk = kn % 3;
+            const bool knext = j + 1 < nb && js0 + kn < nsub;
+            if (!mbar_wait(&bars->v_empty[u], (j & 1) ^ 1, abort_flag, args.timeout_ns) ||
+                (knext && !mbar_wait(&bars->k_empty[sk], ((kn / 3) & 1) ^ 1, abort_flag,
+                                     args.timeout_ns))) {
+              record_error(args.err, 1, kWhere + 0, js, 2);
               bars->abort_flag = 1;
               ok = false;
               break;
             }
-            uint8_t* dst = smem + (kv ? A::OFF_V : A::OFF_K) + s * 2 * TILE64;
-            const CUtensorMap* m = kv ? &tmV : &tmK;
-            const View& vw = kv ? vv : vk;
-            mbar_arrive_expect_tx(full, 2 * TILE64);
-            const int key0 = (js0 + js) * SUB;
-            tma_load_2d(dst, m, full, head * vw.hx, head * vw.hy + key0);
-            tma_load_2d(dst + TILE64, m, full, head * vw.hx + 64, head * vw.hy + key0);
-            if (kv) {
-              v_armed = (v_armed & ~(1u << s)) | (static_cast<uint32_t>(v_cnt[s] & 1) << s);
-              ++v_cnt[s];
-            } else {
-              k_armed = (k_armed & ~(1u << s)) | (static_cast<uint32_t>(k_cnt[s] & 1) << s);
-              ++k_cnt[s];
-            }
+            mbar_arrive_expect_tx(&bars->v_full[u], (knext ? 4 : 2) * TILE64);
+            load_kv(&tmV, vv, A::OFF_V, u, js, &bars->v_full[u]);
+            if (knext) load_kv(&tmK, vk, A::OFF_K, sk, kn, &bars->v_full[u]);
+            v_armed = (v_armed & ~(1u << u)) | (static_cast<uint32_t>(v_cnt[u] & 1) << u);
+            ++v_cnt[u];
           }
         }
       }
@@ -802,12 +809,16 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
         auto issue_sub = [&](int j, int u) {
           const int js = j * KSUB + u;
           if (js0 + js < nsub) {
-            const int s = js & 1;
-            if (!mbar_wait(&bars->k_full[s], (js >> 1) & 1, abort_flag, args.timeout_ns)) {
-              fail(js, 0);
-              return;
+            // K of block j > 0 arrived with V of block j - 1, whose barrier
+            // the PV MMAs of that sub-tile waited for
+            const int s = js % 3;
+            if (j == 0) {
+              if (!mbar_wait(&bars->k_full[u], 0, abort_flag, args.timeout_ns)) {
+                fail(js, 0);
+                return;
+              }
+              tc_fence_after();
             }
-            tc_fence_after();
             const uint64_t dk = dk0 + static_cast<uint64_t>((s * 2 * TILE64) >> 4);
             const uint32_t d_tm = tmem + A::tm_s(0) + SUB * u;
 #pragma unroll
