@@ -183,14 +183,18 @@ def test_attention_tail_split(key_block, H, Nq, Nk):
     assert (a.float() - b.float()).abs().max().item() <= 2 ** -6
 
 
-def test_attention_tail_split_full_rows():
+@pytest.mark.parametrize("key_block,H,Nk", [
+    (128, 20, 2048),
+    (256, 10, 2000),   # key ranges start inside the K ring's three stages; ragged last block
+])
+def test_attention_tail_split_full_rows(key_block, H, Nk):
     """Every row of the split units against the oracle (one tail head)."""
-    H, Nq, Nk = 20, 2048, 2048
+    Nq = 2048
     Q, K, V = _qkv(H, Nq, Nk, 77)
     sc = 1 / math.sqrt(128)
-    a = run_attention(Q.cuda(), K.cuda(), V.cuda(), sc, key_block=128, split=True).cpu()
+    a = run_attention(Q.cuda(), K.cuda(), V.cuda(), sc, key_block=key_block, split=True).cpu()
     res = ops.attention(f64(Q)[H - 1], f64(K)[H - 1], f64(V)[H - 1], sc)
-    check(a[H - 1], res, what="tail head, all rows")
+    check(a[H - 1], res, what=f"tail head, all rows, key blocks of {key_block}")
 
 
 def test_attention_workspace_too_small():
