@@ -783,8 +783,15 @@ psi_status psi_ffn_paged_strided(psi_arena* a, const void* X, int64_t N, const p
   for (int64_t J0 = 0, g = 0; J0 < S; J0 += G, ++g) {
     const int64_t gs = std::min(G, S - J0);
     uint16_t* Hg = hid + static_cast<size_t>(g & 1) * N * G * sl;
-    if (g >= 2) {
-      cudaError_t e = cudaStreamWaitEvent(a->aux, a->ev_down[g & 1], 0);
+    // Streamed, the second group's up projection also waits for the first
+    // group's down projection: when the FFN starts, the copy stream is
+    // usually blocked on a full ring (the FFN pages queued while attention
+    // ran), and the first group, running alone, frees its slots sooner
+    // (block step 2.58 -> 2.53 ms; the order of the FP32 accumulation is
+    // unchanged)
+    if (g >= 2 || (!resident && g == 1)) {
+      const int64_t gw = g >= 2 ? g - 2 : 0;
+      cudaError_t e = cudaStreamWaitEvent(a->aux, a->ev_down[gw & 1], 0);
       if (e != cudaSuccess) return cuda_error(e, "ffn_paged: wait down projection");
     }
     psi_page pg[kFfnGroupMax]{};
