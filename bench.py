@@ -922,10 +922,18 @@ def write_trace(path, wl, arena, stream, flush, torch):
     marks of each step where the workload has them, and per-step sums of
     copy and GEMM busy time.  Written to `path`; nothing is printed."""
     from weight_streamed_bf16_gb300 import psi
-    arena.sync()
-    psi.psi_arena_trace_begin(arena.handle, 1 << 14)
     origin = torch.cuda.Event(enable_timing=True)
-    origin.record(stream)          # next to the library's origin event
+    origin.record(stream)          # creates the event (torch creates it on first record)
+    arena.sync()
+    torch.cuda.synchronize()
+    # The library's origin and this one are recorded behind a short device
+    # delay on the same stream, so both take the timestamp of its end; on an
+    # idle stream each would take the host time of its record call, and
+    # marks and page records would be offset by the host time in between.
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(1 << 21)
+    psi.psi_arena_trace_begin(arena.handle, 1 << 14)
+    origin.record(stream)
     names = getattr(wl, "phase_names", None)
     marks = []
     with torch.cuda.stream(stream):
