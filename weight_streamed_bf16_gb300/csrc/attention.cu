@@ -143,7 +143,7 @@ __device__ __forceinline__ bool exchange(float* slots, int h, float v, uint64_t*
   return true;
 }
 
-// The softmax role of one warp for 128-key blocks.  SPLIT warps share
+// The softmax role of one warp (both attention kernels).  SPLIT warps share
 // each TMEM lane quarter of a tile: warp h owns the keys
 // [h*KB/SPLIT, (h+1)*KB/SPLIT) of every block (and O columns
 // [h*DH/SPLIT, ...)); the warps of a row exchange the row extremum once per

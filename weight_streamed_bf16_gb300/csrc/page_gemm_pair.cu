@@ -14,7 +14,7 @@
 // in 512 tensor cycles, more than the shared-memory bandwidth.  In a pair,
 // each CTA holds 128 rows of X and 128 of the 256 page rows; the tensor cores
 // share the page rows across the pair, so each CTA moves 32 KiB in and 32 KiB
-// out per 64 of depth for the same MMA time.
+// out per k-block for the same MMA time.
 //
 // Roles in each CTA (320 threads):
 //   warp 0      TMA producer: this CTA's X rows [128 x 128] and page rows
