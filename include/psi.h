@@ -290,9 +290,13 @@ psi_status psi_debug_stall_next_gemm(uint64_t timeout_ns);
  *   Y    dev [N x W->rows] BF16 with row stride ldy (ldy >= rows, ldy % 8 == 0)
  * Weights stream through the arena page by page (or are read in place with
  * PSI_RESIDENT); page GEMMs alternate between the compute stream and the
- * arena's auxiliary stream (disjoint output columns), so one page's tail
- * overlaps the next page's start.  The per-element arithmetic is the same in
- * every mode, so resident and streamed results are bitwise equal.
+ * arena's auxiliary stream (disjoint output columns), so one launch's tail
+ * overlaps the next launch's start.  With four or more slots, streamed pages
+ * of 256-aligned row counts that run on CTA pairs go two to a launch after
+ * the first page (which runs alone: its slot is the ring's oldest) whenever
+ * the ring slot after the next one is also free; resident pages on CTA pairs
+ * run as one launch.  The per-element arithmetic is the
+ * same in every mode, so resident and streamed results are bitwise equal.
  * Flags: PSI_RESIDENT, PSI_SYNC_COPY, PSI_BIAS_AFTER_BF16. */
 psi_status psi_linear_paged(psi_arena* arena, const void* X, int64_t N, int64_t K,
                             const psi_linear_weight* W, const void* bias,

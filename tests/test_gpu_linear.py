@@ -98,6 +98,39 @@ def test_linear_resident_one_launch_bitwise(N, M, page_rows, flags):
           what=f"resident one launch {N}x{K}x{M}")
 
 
+@pytest.mark.parametrize("N,M,page_rows,flags,launches", [
+    (512, 2560, 512, 0, 3),                          # five pages: first alone, two pairs
+    (300, 1280, 512, 0, 2),                          # first alone, a pair with a ragged page
+    (600, 1792, 512, psi.PSI_BIAS_AFTER_BF16, 3),    # first, a pair, the ragged last alone
+    (256, 1152, 512, 0, 3),                          # last page of 128 rows: no pair
+    (257, 1536, 256, 0, 4),                          # six 256-row pages, ragged tokens
+])
+def test_linear_streamed_page_pairs_bitwise(N, M, page_rows, flags, launches):
+    """With four or more ring slots, streamed pages on CTA pairs after the
+    first go two to a launch (one tensor map per page); the bytes equal the
+    one-page-per-launch result of a two-slot ring and the resident single
+    launch."""
+    g = torch.Generator().manual_seed(3 * N + M)
+    K = 512
+    X = torch.randn(N, K, generator=g).to(torch.bfloat16)
+    W = (torch.randn(M, K, generator=g) / math.sqrt(K)).to(torch.bfloat16)
+    b = (torch.randn(M, generator=g) * 0.02).to(torch.bfloat16)
+    R = torch.randn(N, M, generator=g).to(torch.bfloat16)
+    pages = -(-M // page_rows)
+    n0 = psi.psi_kernel_launches()
+    merged = run_linear(X, W, b, page_rows, 5, flags=flags, residual=R)
+    n1 = psi.psi_kernel_launches()
+    single = run_linear(X, W, b, page_rows, 2, flags=flags, residual=R)
+    n2 = psi.psi_kernel_launches()
+    res = run_linear(X, W, b, page_rows, 2, flags=flags | psi.PSI_RESIDENT, residual=R)
+    assert n1 - n0 == launches and n2 - n1 == pages
+    assert torch.equal(merged.view(torch.int16), single.view(torch.int16))
+    assert torch.equal(merged.view(torch.int16), res.view(torch.int16))
+    check(merged, ops.linear(f64(X), f64(W), f64(b), residual=f64(R),
+                             bias_after_bf16=bool(flags & psi.PSI_BIAS_AFTER_BF16)),
+          what=f"streamed page pairs {N}x{K}x{M}")
+
+
 def test_linear_special_values():
     """W = I gives B(x + b); an all-zero input gives B(b)."""
     X = torch.randn(64, 128).to(torch.bfloat16)

@@ -649,18 +649,37 @@ static psi_status linear_paged(psi_arena* a, const void* X, int64_t N, int64_t K
     page_rows = W->rows;
     npages = 1;
   }
-  // pages alternate between the compute and the auxiliary stream (outputs are
-  // disjoint column blocks); aux first catches up with the compute stream
+  // After the first page, streamed pages go two to a launch when both run
+  // on CTA pairs and their boundary falls on a 256-row tile boundary: the
+  // launch reads its output columns from two tensor maps (one per page),
+  // with the tiles and per-element arithmetic of the two single-page
+  // launches, so the bytes are the same; the pair has 2 x 192 tiles of
+  // 256 x 256 on a 6144-token batch instead of two launches of 192, each
+  // with its own ramp and tail.  The first page runs alone because its slot
+  // is the ring's oldest, the one a copy stream blocked on a full ring waits
+  // for (in the streamed block, pairs from the first page measured 2.535 ms
+  // per step, one page per launch 2.521, pairs after the first 2.503).  The
+  // ring must hold the next pair while one computes (four slots or more).
+  // Launches with the RoPE epilogue keep one page each.
+  const bool merge2 = !resident && !rope && a->nslots >= 4 && W->page_rows % 256 == 0;
+  // launches alternate between the compute and the auxiliary stream (outputs
+  // are disjoint column blocks); aux first catches up with the compute stream
   psi_status fst = stream_after(a->ev_fork, a->compute, a->aux);
   if (fst != PSI_OK) return fst;
-  for (int64_t p = 0; p < npages; ++p) {
-    cudaStream_t cs = (p & 1) ? a->aux : a->compute;
+  for (int64_t p = 0, launch = 0; p < npages; ++launch) {
+    cudaStream_t cs = (launch & 1) ? a->aux : a->compute;
     const int64_t r0 = p * page_rows;
     const int64_t rows_p = std::min(page_rows, W->rows - r0);
+    int64_t rows_q = 0;  // rows of the second page of the launch (0: none)
+    if (merge2 && p > 0 && p + 1 < npages && a->state[(a->next + 1) % a->nslots] == SLOT_FREE) {
+      rows_q = std::min(page_rows, W->rows - r0 - page_rows);
+      if (!gemm_use_pair(N, rows_p) || !gemm_use_pair(N, rows_q)) rows_q = 0;
+    }
     const size_t off = static_cast<size_t>(r0) * K * 2;
     const size_t nbytes = static_cast<size_t>(rows_p) * K * 2;
-    psi_page pg{};
+    psi_page pg{}, pg2{};
     const void* dev;
+    const void* dev2 = nullptr;
     if (resident) {
       dev = src + off;
       a->stats.resident_pages++;
@@ -668,10 +687,17 @@ static psi_status linear_paged(psi_arena* a, const void* X, int64_t N, int64_t K
       psi_status st = page_stream_to(a, src + off, nbytes, flags, cs, &pg);
       if (st != PSI_OK) return st;
       dev = pg.dev;
+      if (rows_q) {
+        st = page_stream_to(a, src + off + nbytes, static_cast<size_t>(rows_q) * K * 2, flags,
+                            cs, &pg2);
+        if (st != PSI_OK) return st;
+        dev2 = pg2.dev;
+      }
     }
     GemmArgs g{};
     g.M = static_cast<int32_t>(N);
-    g.N = static_cast<int32_t>(rows_p);
+    g.N = static_cast<int32_t>(rows_p + rows_q);
+    g.n_split = rows_q ? static_cast<int32_t>(rows_p) : 0;
     g.K = static_cast<int32_t>(K);
     g.epi = EPI_LINEAR;
     g.bias_after_bf16 = (flags & PSI_BIAS_AFTER_BF16) ? 1 : 0;
@@ -681,7 +707,7 @@ static psi_status linear_paged(psi_arena* a, const void* X, int64_t N, int64_t K
     g.ldo = ldy;
     if (rope && rope->cols > r0) {
       g.rope_dh = rope->dh;
-      g.rope_cols = static_cast<int32_t>(std::min(rope->cols - r0, rows_p));
+      g.rope_cols = static_cast<int32_t>(std::min(rope->cols - r0, rows_p + rows_q));
       g.rope_after_bf16 = (flags & PSI_ROPE_AFTER_BF16) ? 1 : 0;
       g.rope_cos = rope->cos;
       g.rope_sin = rope->sin;
@@ -689,9 +715,11 @@ static psi_status linear_paged(psi_arena* a, const void* X, int64_t N, int64_t K
     }
     g.err = err;
     g.timeout_ns = kWaitLimitNs;
-    psi_status st = arena_gemm(a, cs, X, K, dev, K, g);
+    psi_status st = arena_gemm(a, cs, X, K, dev, K, g, dev2);
     if (st != PSI_OK) return st;
     if (!resident && (st = page_release_on(a, pg, cs)) != PSI_OK) return st;
+    if (rows_q && (st = page_release_on(a, pg2, cs)) != PSI_OK) return st;
+    p += rows_q ? 2 : 1;
   }
   return stream_after(a->ev_join, a->aux, a->compute);
 }
