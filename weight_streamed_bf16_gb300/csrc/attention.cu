@@ -853,7 +853,10 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
               const uint32_t pbase = tmem + (u == 0 ? A::TILE_COLS : SUB);
               const uint32_t o_tm = tmem + A::tm_o(0);
               const uint32_t first = (j | u) != 0 ? 1u : 0u;
-              for (int half = 0; half < halves; ++half) {
+              // both halves unrolled: one straight run of MMAs for the issuer
+#pragma unroll
+              for (int half = 0; half < 2; ++half) {
+                if (half == halves) break;
 #pragma unroll
                 for (int kk = 0; kk < SUB / 16; ++kk) {
                   const uint32_t pcol = 32 * (kk >> 1) + 8 * (kk & 1) + 16 * half;
@@ -895,7 +898,10 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
             const uint32_t pbase = tmem + A::tm_s(t) + SUB * u;
             const uint32_t o_tm = tmem + A::tm_o(t);
             const uint32_t first = (j | u) != 0 ? 1u : 0u;
-            for (int half = 0; half < halves; ++half) {
+            // both halves unrolled: one straight run of MMAs for the issuer
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              if (half == halves) break;
 #pragma unroll
               for (int kk = 0; kk < SUB / 16; ++kk) {
                 const uint32_t pcol = 32 * (kk >> 1) + 8 * (kk & 1) + 16 * half;
