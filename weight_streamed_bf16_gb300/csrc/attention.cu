@@ -180,6 +180,14 @@ __device__ __forceinline__ void softmax_role(Bars* bars, uint8_t* smem, int off_
       break;
     }
     tc_fence_after();
+    // S(j) of the last tile is issued after both tiles' S(j) and that tile's
+    // PV(j - 1), so once it is complete K(j) and V(j - 1) are free: one
+    // thread of the last tile hands both stages back to the producer (the
+    // MMA issuer then commits two barriers fewer per block)
+    if (t == NT - 1 && e % (4 * SPLIT) == 0 && lane == 0) {
+      mbar_arrive(&bars->k_empty[j & 1]);
+      if (j > 0) mbar_arrive(&bars->v_empty[(j - 1) & 1]);
+    }
     // pass 1: row extremum of this range's raw scores (max, or min for a
     // negative scale), then the other ranges' through shared memory
     const float c = args.scale_log2;  // scale * log2(e)
@@ -795,8 +803,7 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
             const uint32_t off = ((kk >> 2) * TILE64 + (kk & 3) * 32) >> 4;
             mma_bf16_ss(d_tm, dq + off, dk + off, idesc_s, kk > 0 ? 1u : 0u);
           }
-          if (t == NT - 1) mma_commit(&bars->k_empty[s]);  // every tile has read it
-          issued = true;
+          issued = true;  // K(j) is handed back by the softmax role (S-ready)
         }
         mma_commit(&bars->s_full[t]);
       };
@@ -916,9 +923,8 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
           // which the tensor core executes first
           if (j + 1 < nb) issue_s(j + 1, t);
         }
-        if (!ok) break;
-        for (int u = 0; u < KSUB; ++u)
-          if (js0 + j * KSUB + u < nsub) mma_commit(&bars->v_empty[(j * KSUB + u) & 1]);
+        // V(j) is handed back by the softmax role once S(j + 1) of the last
+        // tile is complete
       }
       }
       if (issued) {
