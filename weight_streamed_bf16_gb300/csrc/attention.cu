@@ -267,15 +267,9 @@ __device__ __forceinline__ void softmax_role(Bars* bars, uint8_t* smem, int off_
     expo(rb, ch0 + 1);
     l = eta * l + rs;
     m2 = m_new;
+    // O is stable: this tile's PV(j - 1) was issued before its S(j), whose
+    // completion (the S-ready barrier above) covers every earlier MMA
     if (j > 0) {
-      // the previous PV of this tile has finished: O is stable
-      if (!mbar_wait(&bars->pv_done[t], (j - 1) & 1, abort_flag, args.timeout_ns)) {
-        if (lane == 0) record_error(args.err, 1, kWhere + 3, j, t * 8 + h * 4 + q);
-        bars->abort_flag = 1;
-        ok = false;
-        break;
-      }
-      tc_fence_after();
       if (__any_sync(0xffffffffu, eta != 1.0f)) {
         // this range's O columns
         constexpr int OCH = DH / 32 / SPLIT;
@@ -310,7 +304,8 @@ __device__ __forceinline__ void softmax_role(Bars* bars, uint8_t* smem, int off_
   }
   if (ok && nb > 0) {
     float ls[SPLIT];
-    if (!mbar_wait(&bars->pv_done[t], (nb - 1) & 1, abort_flag, args.timeout_ns)) {
+    // the tile's last PV product (the only one with a completion barrier)
+    if (!mbar_wait(&bars->pv_done[t], 0, abort_flag, args.timeout_ns)) {
       if (lane == 0) record_error(args.err, 1, kWhere + 3, nb, t * 8 + h * 4 + q);
       bars->abort_flag = 1;
     } else if (!exchange<SPLIT>(xslots(nb & 1), h, l, xb, nb & 1, ls, abort_flag,
@@ -918,7 +913,9 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
             }
           }
           if (!ok) break;
-          mma_commit(&bars->pv_done[t]);
+          // the softmax learns that PV(j) is complete from S(j + 1)'s
+          // barrier; only the last block's PV gets a barrier of its own
+          if (j == nb - 1) mma_commit(&bars->pv_done[t]);
           // tile t's next scores overwrite its P: issued after its PV MMAs,
           // which the tensor core executes first
           if (j + 1 < nb) issue_s(j + 1, t);
