@@ -410,6 +410,15 @@ __device__ __forceinline__ void softmax_role_sub(Bars* bars, uint8_t* smem, int 
     }
     tc_fence_after();
     const int kvalid = args.Nk - (jb0 + j) * KB;  // keys of this block that exist
+    // S(j, u) is issued after PV(j - 1, u), so once it is complete K(j, u)
+    // and V(j - 1, u) are free: one thread hands both stages back to the
+    // producer (here for sub-tile 0, below for sub-tile 1), and the MMA
+    // issuer commits no barrier for them
+    const bool relay = e == 0 && lane == 0;
+    if (relay) {
+      mbar_arrive(&bars->k_empty[(2 * j) % 3]);
+      if (j > 0) mbar_arrive(&bars->v_empty[0]);
+    }
     // pass 1: row extremum of this range's raw scores (max, or min for a
     // negative scale), then the other ranges' through shared memory
     float ext = c >= 0.f ? -INFINITY : INFINITY;
@@ -475,6 +484,10 @@ __device__ __forceinline__ void softmax_role_sub(Bars* bars, uint8_t* smem, int 
       break;
     }
     tc_fence_after();
+    if (relay) {
+      if (kvalid > SUB) mbar_arrive(&bars->k_empty[(2 * j + 1) % 3]);  // K(j, 1) exists
+      if (j > 0) mbar_arrive(&bars->v_empty[1]);
+    }
     uint32_t rb[32];
     tmem_ld_32x32b_x32(tS + c1 * 32, rb);
     tmem_wait_ld();
@@ -506,15 +519,9 @@ __device__ __forceinline__ void softmax_role_sub(Bars* bars, uint8_t* smem, int 
       rs0 = 0.f;
       expo(ra, c0, tP0 + c0 * 32, m_new, rs0);
     }
+    // O is stable: PV(j - 1, 1) was issued before S(j, 1), whose completion
+    // (the S-ready barrier above) covers every earlier MMA
     if (j > 0) {
-      // the previous PV has finished: O is stable
-      if (!mbar_wait(&bars->pv_done[0], (j - 1) & 1, abort_flag, args.timeout_ns)) {
-        if (lane == 0) record_error(args.err, 1, kWhere + 3, j, h * 4 + q);
-        bars->abort_flag = 1;
-        ok = false;
-        break;
-      }
-      tc_fence_after();
       if (__any_sync(0xffffffffu, eta != 1.0f)) {  // this range's O columns
         uint32_t r[32];
         tmem_ld_32x32b_x32(tO + h * 32, r);
@@ -536,7 +543,8 @@ __device__ __forceinline__ void softmax_role_sub(Bars* bars, uint8_t* smem, int 
   }
   if (ok && nb > 0) {
     float ls[SPLIT];
-    if (!mbar_wait(&bars->pv_done[t], (nb - 1) & 1, abort_flag, args.timeout_ns)) {
+    // the last PV product (the only one with a completion barrier)
+    if (!mbar_wait(&bars->pv_done[t], 0, abort_flag, args.timeout_ns)) {
       if (lane == 0) record_error(args.err, 1, kWhere + 3, nb, t * 8 + h * 4 + q);
       bars->abort_flag = 1;
     } else if (!exchange<SPLIT>(xslots(nb & 1), h, l, xb, nb & 1, ls, abort_flag,
@@ -828,8 +836,7 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
               const uint32_t off = ((kk >> 2) * TILE64 + (kk & 3) * 32) >> 4;
               mma_bf16_ss(d_tm, dq0 + off, dk + off, idesc_s, kk > 0 ? 1u : 0u);
             }
-            mma_commit(&bars->k_empty[s]);
-            issued = true;
+            issued = true;  // K(j, u) is handed back by the softmax role
           }
           mma_commit(&bars->s_full[u]);  // also when the sub-tile is past the keys
         };
@@ -866,9 +873,11 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
                               (half | kk) != 0 ? 1u : first);
                 }
               }
-              mma_commit(&bars->v_empty[s]);
             }
-            if (u == KSUB - 1) mma_commit(&bars->pv_done[0]);
+            // V(j, u) is handed back by the softmax role once S(j + 1, u) is
+            // complete, which also tells it that this PV is; only the last
+            // block's PV gets a barrier of its own
+            if (u == KSUB - 1 && j == nb - 1) mma_commit(&bars->pv_done[0]);
             if (j + 1 < nb) issue_sub(j + 1, u);
           }
         }
