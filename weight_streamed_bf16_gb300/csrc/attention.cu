@@ -882,34 +882,39 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
           }
         }
       } else {
-      for (int t = 0; t < NT && ok; ++t) issue_s(0, t);
-      for (int j = 0; j < nb && ok; ++j) {
-        for (int t = 0; t < NT && ok; ++t) {
-          if (!mbar_wait(&bars->p_full[t], j & 1, abort_flag, args.timeout_ns)) {
-            fail(j, 3);
-            break;
-          }
-          tc_fence_after();
-          // O_t += P_hi V + P_lo V over the block's sub-tiles: P from tensor
-          // memory (keys 16kk.. of sub-tile u at column 128u + 32(kk/2) +
-          // 8(kk%2), lo 16 further), V rows 16kk.. of both 64-wide dh blocks
-          for (int u = 0; u < KSUB && ok; ++u) {
-            const int js = j * KSUB + u;
-            if (js0 + js >= nsub) break;
-            const int s = js & 1;
+        // two tiles of 128-key blocks (one sub-tile per block, every block of
+        // the range exists).  Per block and tile: wait for P, the PV run,
+        // then the tile's next scores, with every operand address formed
+        // before the waits, so the issuer runs no bookkeeping between MMA
+        // runs while the softmax warps keep its SM sub-partition busy.
+        static_assert(KSUB == 1, "the two-tile kernel takes 128-key blocks");
+        for (int t = 0; t < NT && ok; ++t) issue_s(0, t);
+        const int halves = args.bf16_weights ? 1 : 2;  // p_hi (and p_lo)
+        for (int j = 0; j < nb && ok; ++j) {
+          const uint64_t dv = dv0 + static_cast<uint64_t>(((j & 1) * 2 * TILE64) >> 4);
+          const uint64_t dkn = dk0 + static_cast<uint64_t>((((j + 1) & 1) * 2 * TILE64) >> 4);
+          const bool next = j + 1 < nb;
+          const uint32_t first = j != 0 ? 1u : 0u;
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            if (!mbar_wait(&bars->p_full[t], j & 1, abort_flag, args.timeout_ns)) {
+              fail(j, 3);
+              break;
+            }
+            tc_fence_after();
             if (t == 0) {
-              if (!mbar_wait(&bars->v_full[s], (js >> 1) & 1, abort_flag, args.timeout_ns)) {
-                fail(js, 4);
+              // V(j), and K(j + 1) with it
+              if (!mbar_wait(&bars->v_full[j & 1], (j >> 1) & 1, abort_flag, args.timeout_ns)) {
+                fail(j, 4);
                 break;
               }
               tc_fence_after();
             }
-            const uint64_t dv = dv0 + static_cast<uint64_t>((s * 2 * TILE64) >> 4);
-            const int halves = args.bf16_weights ? 1 : 2;  // p_hi (and p_lo)
-            const uint32_t pbase = tmem + A::tm_s(t) + SUB * u;
+            // O_t += P_hi V + P_lo V: P from tensor memory (keys 16kk.. at
+            // column 32(kk/2) + 8(kk%2), lo 16 further), V rows 16kk.. of
+            // both 64-wide dh blocks; both halves as one unrolled run
+            const uint32_t pbase = tmem + A::tm_s(t);
             const uint32_t o_tm = tmem + A::tm_o(t);
-            const uint32_t first = (j | u) != 0 ? 1u : 0u;
-            // both halves unrolled: one straight run of MMAs for the issuer
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
               if (half == halves) break;
@@ -920,18 +925,25 @@ __global__ void __launch_bounds__(AShape<KSUB>::kThreads, 1)
                             (half | kk) != 0 ? 1u : first);
               }
             }
+            if (!next) {
+              // the softmax learns that PV(j) is complete from S(j + 1)'s
+              // barrier; only the last block's PV gets a barrier of its own
+              mma_commit(&bars->pv_done[t]);
+              continue;
+            }
+            // tile t's next scores overwrite its P: the tensor core runs them
+            // after its PV MMAs.  K(j + 1) and V(j) are handed back to the
+            // producer by the softmax role when it sees these scores.
+            const uint64_t dq = dq0 + static_cast<uint64_t>((t * 2 * TILE64) >> 4);
+            const uint32_t d_tm = tmem + A::tm_s(t);
+#pragma unroll
+            for (int kk = 0; kk < DH / 16; ++kk) {
+              const uint32_t off = ((kk >> 2) * TILE64 + (kk & 3) * 32) >> 4;
+              mma_bf16_ss(d_tm, dq + off, dkn + off, idesc_s, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(&bars->s_full[t]);
           }
-          if (!ok) break;
-          // the softmax learns that PV(j) is complete from S(j + 1)'s
-          // barrier; only the last block's PV gets a barrier of its own
-          if (j == nb - 1) mma_commit(&bars->pv_done[t]);
-          // tile t's next scores overwrite its P: issued after its PV MMAs,
-          // which the tensor core executes first
-          if (j + 1 < nb) issue_s(j + 1, t);
         }
-        // V(j) is handed back by the softmax role once S(j + 1) of the last
-        // tile is complete
-      }
       }
       if (issued) {
         mma_commit(&bars->drain);
