@@ -107,7 +107,8 @@ def test_linear_resident_one_launch_bitwise(N, M, page_rows, flags):
 ])
 def test_linear_streamed_page_pairs_bitwise(N, M, page_rows, flags, launches):
     """With four or more ring slots, streamed pages on CTA pairs after the
-    first go two to a launch (one tensor map per page); the bytes equal the
+    first go two to a launch (one tensor map per page), with copies on the
+    copy stream or on the compute stream; the bytes equal the
     one-page-per-launch result of a two-slot ring and the resident single
     launch."""
     g = torch.Generator().manual_seed(3 * N + M)
@@ -123,9 +124,13 @@ def test_linear_streamed_page_pairs_bitwise(N, M, page_rows, flags, launches):
     single = run_linear(X, W, b, page_rows, 2, flags=flags, residual=R)
     n2 = psi.psi_kernel_launches()
     res = run_linear(X, W, b, page_rows, 2, flags=flags | psi.PSI_RESIDENT, residual=R)
-    assert n1 - n0 == launches and n2 - n1 == pages
+    n3 = psi.psi_kernel_launches()
+    sync = run_linear(X, W, b, page_rows, 5, flags=flags | psi.PSI_SYNC_COPY, residual=R)
+    n4 = psi.psi_kernel_launches()
+    assert n1 - n0 == launches and n2 - n1 == pages and n4 - n3 == launches
     assert torch.equal(merged.view(torch.int16), single.view(torch.int16))
     assert torch.equal(merged.view(torch.int16), res.view(torch.int16))
+    assert torch.equal(merged.view(torch.int16), sync.view(torch.int16))
     check(merged, ops.linear(f64(X), f64(W), f64(b), residual=f64(R),
                              bias_after_bf16=bool(flags & psi.PSI_BIAS_AFTER_BF16)),
           what=f"streamed page pairs {N}x{K}x{M}")
