@@ -243,7 +243,7 @@ __device__ __forceinline__ void softmax_role(Bars* bars, uint8_t* smem, int off_
     float rs = 0.f;
     auto expo = [&](const uint32_t (&r)[32], int cc) {
       float p[32];
-      uint32_t hi[16], lo[16];
+      uint32_t hl[32];  // the chunk's 32 columns: 16 of p_hi pairs, then 16 of p_lo
       if (kvalid >= KB) {
 #pragma unroll
         for (int i = 0; i < 32; ++i)
@@ -257,11 +257,10 @@ __device__ __forceinline__ void softmax_role(Bars* bars, uint8_t* smem, int off_
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         rs += p[2 * i] + p[2 * i + 1];
-        hi[i] = pack_bf16x2(p[2 * i], p[2 * i + 1]);
-        lo[i] = pack_bf16x2(p[2 * i] - bf16_lo(hi[i]), p[2 * i + 1] - bf16_hi(hi[i]));
+        hl[i] = pack_bf16x2(p[2 * i], p[2 * i + 1]);
+        hl[16 + i] = pack_bf16x2(p[2 * i] - bf16_lo(hl[i]), p[2 * i + 1] - bf16_hi(hl[i]));
       }
-      tmem_st_32x32b_x16(tS + cc * 32, hi);
-      tmem_st_32x32b_x16(tS + cc * 32 + 16, lo);
+      tmem_st_32x32b_x32(tS + cc * 32, hl);  // one store for both halves
     };
     expo(ra, ch0);
     expo(rb, ch0 + 1);
