@@ -93,6 +93,36 @@ def test_linear_rope_shapes(N, H, dh, page_rows):
     assert torch.equal(Y[:, 2 * H * dh:].view(torch.int16), plain[:, 2 * H * dh:].view(torch.int16))
 
 
+@pytest.mark.parametrize("N,H,dh,page_rows", [
+    (512, 4, 128, 256),    # six pages: pairs across the Q/K and the rotated/plain boundaries
+    (300, 6, 64, 256),     # ragged tokens, 64-wide heads, a short last page alone
+])
+def test_linear_rope_page_pairs_bitwise(N, H, dh, page_rows):
+    """With four or more ring slots, streamed pages after the first go two to
+    a launch with the RoPE epilogue too; the bytes equal one page per launch
+    (two slots) and the resident single launch."""
+    K = 256
+    M = 3 * H * dh
+    X = _bf16((N, K), 1.0, N + 3 * H)
+    W = _bf16((M, K), 1 / math.sqrt(K), M + 1)
+    b = _bf16((M,), 0.5, 11)
+    cos, sin = psi_synth.rope_table(N, dh, pos0=5)
+    pages = -(-M // page_rows)
+    n0 = psi.psi_kernel_launches()
+    merged = run_linear_rope(X, W, b, cos, sin, dh, 2 * H * dh, page_rows, 5)
+    n1 = psi.psi_kernel_launches()
+    single = run_linear_rope(X, W, b, cos, sin, dh, 2 * H * dh, page_rows, 2)
+    n2 = psi.psi_kernel_launches()
+    res = run_linear_rope(X, W, b, cos, sin, dh, 2 * H * dh, page_rows, 2,
+                          flags=psi.PSI_RESIDENT)
+    assert n2 - n1 == pages and n1 - n0 < pages
+    assert torch.equal(merged.view(torch.int16), single.view(torch.int16))
+    assert torch.equal(merged.view(torch.int16), res.view(torch.int16))
+    ref = ops.linear_rope(f64(X), f64(W), f64(b), cos.double().numpy(), sin.double().numpy(),
+                          dh, 2 * H * dh)
+    check(merged, ref, what=f"rope page pairs {N}x{M} dh{dh}")
+
+
 def test_linear_rope_identity_table_is_plain_projection():
     """c = 1, s = 0: the rotated columns equal the plain projection bitwise."""
     N, K, dh, H = 300, 512, 128, 2

@@ -298,7 +298,7 @@ psi_status launch_page_gemm(const void* X, int64_t ldx, const void* P, int64_t l
   const int bn = pair ? 128 : (a.rope_dh ? 256 : gemm_bn_for(a.N));  // page rows per CTA and box
   if (a.rope_dh) {
     if ((a.rope_dh != 64 && a.rope_dh != 128) || a.epi != EPI_LINEAR || a.resid ||
-        a.k_split > 0 || a.n_split > 0 || a.rope_cols % a.rope_dh || a.rope_ld % 4 ||
+        a.k_split > 0 || a.rope_cols % a.rope_dh || a.rope_ld % 4 ||
         (reinterpret_cast<uintptr_t>(a.rope_cos) & 15) ||
         (reinterpret_cast<uintptr_t>(a.rope_sin) & 15))
       return set_error(PSI_ERR_INVALID_ARG, "page_gemm: bad RoPE arguments");

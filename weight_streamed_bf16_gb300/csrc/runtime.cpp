@@ -660,8 +660,7 @@ static psi_status linear_paged(psi_arena* a, const void* X, int64_t N, int64_t K
   // for (in the streamed block, pairs from the first page measured 2.535 ms
   // per step, one page per launch 2.521, pairs after the first 2.503).  The
   // ring must hold the next pair while one computes (four slots or more).
-  // Launches with the RoPE epilogue keep one page each.
-  const bool merge2 = !resident && !rope && a->nslots >= 4 && W->page_rows % 256 == 0;
+  const bool merge2 = !resident && a->nslots >= 4 && W->page_rows % 256 == 0;
   // launches alternate between the compute and the auxiliary stream (outputs
   // are disjoint column blocks); aux first catches up with the compute stream
   psi_status fst = stream_after(a->ev_fork, a->compute, a->aux);
