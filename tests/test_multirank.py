@@ -63,3 +63,23 @@ def test_trace_busy_time_is_the_union_of_intervals():
     assert abs(bench.busy_ms(rec, "copy", 0.75, 3.0) - (0.75 + 0.25 + 0.1)) < 1e-12
     assert bench.busy_ms(rec, "gemm", 1.0, 2.0) == 1.0
     assert bench.busy_ms(rec, "copy", 5.0, 6.0) == 0.0
+
+
+def test_profile_traffic_is_gated_by_the_source_digest(tmp_path, monkeypatch):
+    """DRAM traffic from a committed ncu summary is reported only while the
+    summary's source digest matches the kernel sources it was taken on."""
+    import bench
+    src = tmp_path / "weight_streamed_bf16_gb300" / "csrc"
+    src.mkdir(parents=True)
+    (src / "k.cu").write_text("kernel v1\n")
+    (tmp_path / "profiles").mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    d1 = bench.source_digest("k.cu")
+    (tmp_path / "profiles" / "k_traffic.txt").write_text(
+        "a description without a separator\ncommand: ncu ...\n"
+        f"source_digest: {d1}\ntraffic_bytes_per_launch: 12345\n")
+    assert bench.profile_traffic("k_traffic.txt", d1) == 12345.0
+    (src / "k.cu").write_text("kernel v2\n")             # the source changed
+    d2 = bench.source_digest("k.cu")
+    assert d2 != d1 and bench.profile_traffic("k_traffic.txt", d2) is None
+    assert bench.profile_traffic("missing.txt", d1) is None
